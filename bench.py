@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Benchmark of the W4A16 decode step on GB300.
+
+One step = the 112 INT4 weight-only projections of a 28-layer Qwen2.5-7B
+decode step at M = 1 (per layer: qkv 4608x3584, o 3584x3584, gate_up
+37888x3584, down 3584x18944), replayed as one captured CUDA graph through the
+C ABI (w4_decode_seq_replay).  Weights (3.36 GB of packed INT4 + FP16 scales,
+far larger than the 129 MB L2) and activations are seeded synthetic data.
+
+Prints ONE JSON line (rank 0).  `value` is weight+scale bytes per step over
+the step time, in GB/s, summed over ranks (replicas: each rank runs its own
+step on its own GPU; there is no exchange).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import platform
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W4A16 GEMV achieved HBM GB/s (% of GB300 peak); µs per 28-layer M=1 projection step"
+LAYER = [("qkv", 4608, 3584), ("o", 3584, 3584), ("gate_up", 37888, 3584), ("down", 3584, 18944)]
+LAYERS = 28
+CONFIG_ID = 3  # seed family of the full-decode-step workload
+BYTES_PER_STEP = LAYERS * sum((N * K) // 2 + N * (K // 128) * 2 for _, N, K in LAYER)  # 3,364,601,856
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = ("decode step: 28 layers x {qkv 4608x3584, o 3584x3584, gate_up 37888x3584, down 3584x18944} "
+            "W4A16 projections, M=1, one CUDA-graph replay of 112 kernels")
+
+
+def rank_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---- clocks --------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            f = [t.strip() for t in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append({"sm": float(f[1]), "max": float(f[2]), "power": float(f[3]),
+                             "hw": f[5] == "Active", "hw_th": f[6] == "Active", "sw_th": f[7] == "Active",
+                             "pcap": f[8] == "Active"})
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        load = [r for r in rows if r["power"] > 250] or rows
+        reasons = sorted({name for r in load for name, key in
+                          (("hw_slowdown", "hw"), ("hw_thermal_slowdown", "hw_th"),
+                           ("sw_thermal_slowdown", "sw_th"), ("sw_power_cap", "pcap")) if r[key]})
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---- workload -----------------------------------------------------------------
+def build_step(torch, w4, synth, M: int):
+    """Packed weights of 28 layers (device-generated, device-packed), x and y
+    arenas, and the captured sequence."""
+    dev = torch.device("cuda")
+    ws, keep, meta = [], [], []
+    x_host_parts, xsz, ysz = [], [], []
+    for layer in range(LAYERS):
+        for pid, (_, N, K) in enumerate(LAYER):
+            G = K // 128
+            q = torch.empty((N, K), dtype=torch.int8, device=dev)
+            s = torch.empty((N, G), dtype=torch.int16, device=dev)
+            synth.q_device(synth.seed_of(CONFIG_ID, layer, pid, synth.T_Q), N, K, q)
+            synth.scale_device(synth.seed_of(CONFIG_ID, layer, pid, synth.T_SCALE), N, G, s)
+            packed = torch.empty(w4.w4_packed_bytes(N, K), dtype=torch.uint8, device=dev)
+            ws.append(w4.w4_pack(q, s, N, K, packed))
+            keep.append(packed)
+            del q, s
+            x_host_parts.append(synth.x_full(synth.seed_of(CONFIG_ID, layer, pid, synth.T_X), M, K).ravel())
+            xsz.append(M * K)
+            ysz.append(M * N)
+            meta.append((layer, pid, N, K))
+    x_host = np.concatenate(x_host_parts).view(np.int16)
+    x_arena = torch.from_numpy(x_host).to(dev)
+    y_arena = torch.zeros(sum(ysz), dtype=torch.int16, device=dev)
+    xs, ys, xo, yo = [], [], 0, 0
+    for nx, ny in zip(xsz, ysz):
+        xs.append(x_arena[xo:xo + nx])
+        ys.append(y_arena[yo:yo + ny])
+        xo += nx
+        yo += ny
+    return dict(ws=ws, keep=keep, meta=meta, x_host=x_host, x_arena=x_arena, y_arena=y_arena, xs=xs, ys=ys)
+
+
+def time_replays(torch, fn, reps: int) -> float:
+    """Average ms per call of fn() over reps calls, CUDA events on the current stream."""
+    s = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(s)
+    for _ in range(reps):
+        fn()
+    b.record(s)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    for name in ("gemv.cu", "w4_internal.cuh"):
+        with open(os.path.join(ROOT, "int4_weight_only_pack_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic_per_launch():
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "decode_step_M1_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    m = re.search(r"kernel_source_digest:\s*(\w+)", text)
+    t = re.search(r"dram_bytes_per_launch:\s*([0-9.]+)", text)
+    if not m or not t or m.group(1) != kernel_source_digest():
+        return None
+    return float(t.group(1))
+
+
+# ---- CPU oracle (the reported baseline and the reference arm) --------------------
+def oracle_sample(synth, rows_stride: int = 16):
+    """A bounded sample of the step: layer 0's four projections at M = 1,
+    every `rows_stride`-th output row.  Inputs drawn on the host."""
+    probs, nbytes = [], 0
+    for pid, (_, N, K) in enumerate(LAYER):
+        rows = np.arange(0, N, rows_stride)
+        q, s, x = synth.projection_inputs(CONFIG_ID, 0, pid, 1, N, K, rows=rows)
+        probs.append((x, q, s))
+        nbytes += len(rows) * ((K // 2) + (K // 128) * 2)
+    return probs, nbytes
+
+
+def oracle_step(oracle, probs, threads):
+    for x, q, s in probs:
+        oracle.linear(x, q, s, threads=threads)
+
+
+def run_reference(args):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return 0
+    import oracle
+    import synth
+    cores = host_cores()
+    probs, nbytes = oracle_sample(synth)
+    for _ in range(args.warmup):
+        oracle_step(oracle, probs, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(oracle, probs, cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes / dt / 1e9
+    sample = ("layer 0 of the step, all four projections at M=1, every 16th output row "
+              "(%d weight+scale bytes per step)" % nbytes)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": 1, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "host": {"arch": platform.machine(), "nproc": os.cpu_count()}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(oracle, synth, budget_s: float = 12.0):
+    cores = host_cores()
+    probs, nbytes = oracle_sample(synth)
+    oracle_step(oracle, probs, cores)  # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(oracle, probs, cores)
+        n += 1
+        if time.perf_counter() - t0 > budget_s or n >= 50:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "layer 0 of the step, four projections at M=1, every 16th output row, %d passes "
+                      "(%d weight+scale bytes each), FP64 C oracle over %d threads" % (n, nbytes, cores)}
+
+
+# ---- main ------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="skip the side measurements")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    rank, world, local = rank_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    import int4_weight_only_pack_gb300 as w4
+    from int4_weight_only_pack_gb300 import build as w4build
+    import synth
+    if rank == 0 or world == 1:
+        w4build.build()
+        synth.build_device()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.set_device(local)
+    M = 1
+    st = build_step(torch, w4, synth, M)
+    seq = w4.DecodeSeq(st["ws"], st["xs"], st["ys"], M, use_pdl=True)
+    for _ in range(args.warmup):
+        seq.replay()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # soak ~1.5 s so that the clock record sees the GPU under this load
+    sampler = ClockSampler(local)
+    soak = max(1, int(1.5 / max(time_replays(torch, seq.replay, 20) * 1e-3, 1e-5)))
+    for _ in range(soak):
+        seq.replay()
+    barrier()
+    s = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(s)
+    for _ in range(args.steps):
+        seq.replay()
+    ev1.record(s)
+    barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * BYTES_PER_STEP / (ms * 1e-3) / 1e9
+    per_gpu = BYTES_PER_STEP / (ms * 1e-3) / 1e9
+    launches = seq.kernels()
+
+    # e2e through the C ABI with host buffers: pinned x in, replay, y out, sync
+    x_pin = torch.from_numpy(st["x_host"]).pin_memory()
+    y_pin = torch.empty(st["y_arena"].numel(), dtype=torch.int16).pin_memory()
+    xb, yb = st["x_arena"].numel() * 2, st["y_arena"].numel() * 2
+    for _ in range(3):
+        seq.run_host(x_pin, st["x_arena"], xb, st["y_arena"], y_pin, yb, s)
+    e2e_steps = max(10, min(args.steps, 500))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        seq.run_host(x_pin, st["x_arena"], xb, st["y_arena"], y_pin, yb, s)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    extras = {}
+    if not args.no_extras:
+        extras["eager_us_per_step"] = time_replays(torch, seq.eager, 20) * 1e3
+        nopdl = w4.DecodeSeq(st["ws"], st["xs"], st["ys"], M, use_pdl=False)
+        extras["graph_no_pdl_us_per_step"] = time_replays(torch, nopdl.replay, 200) * 1e3
+        nopdl.close()
+        per = {}
+        for pid, (name, N, K) in enumerate(LAYER):
+            idx = [i for i, m in enumerate(st["meta"]) if m[1] == pid]
+            one = w4.DecodeSeq([st["ws"][i] for i in idx], [st["xs"][i] for i in idx],
+                               [st["ys"][i] for i in idx], M, use_pdl=True)
+            us = time_replays(torch, one.replay, 100) * 1e3 / len(idx)
+            nb = (N * K) // 2 + N * (K // 128) * 2
+            cfg = w4.w4a16_gemv_default_config(M, N, K)
+            per[name] = {"us": us, "GB/s": nb / (us * 1e-6) / 1e9, "bytes": nb,
+                         "launch": {"bands_per_cta": cfg.bands_per_cta, "splits": cfg.splits,
+                                    "depth": cfg.depth}}
+            one.close()
+        extras["per_projection_back_to_back_28_layers"] = per
+
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    roof = {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s", "frac": per_gpu / peak,
+            "traffic": ncu_traffic_per_launch(),
+            "kernel": "decode kernel (all 112 launches of the step); achieved = algorithmic bytes per "
+                      "launch (%d) / average launch duration over the timed region (step time / %d)" %
+                      (BYTES_PER_STEP // launches, launches),
+            "peak_source": "%s hbm_gbs (MEASURED_PEAKS.json)" % peak_kind if peak_kind == "measured"
+            else "fallback 6.8 TB/s"}
+    if roof["traffic"] is not None:
+        roof["traffic"] = roof["traffic"]
+
+    cpu = None
+    if rank == 0:
+        import oracle
+        cpu = cpu_baseline(oracle, synth)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "M": M, "layers": LAYERS, "projections_per_step": launches,
+                           "bytes_per_step": BYTES_PER_STEP, "accumulate": "f32",
+                           "l2": "inputs larger than L2: 3.36 GB of weights per step vs 129 MB L2",
+                           "launch": "one cudaGraphLaunch per step; programmatic dependent launch edges",
+                           "parallelism": "replicas" if world > 1 else "single GPU"},
+                "roofline": roof,
+                "cpu_baseline": cpu,
+                "e2e": {"value": world * BYTES_PER_STEP / e2e_s / 1e9, "unit": "GB/s",
+                        "us_per_step": e2e_s * 1e6, "h2d_bytes_per_step": xb, "d2h_bytes_per_step": yb,
+                        "via": "w4_decode_seq_run_host (pinned host x -> device, replay, device y -> pinned host, sync)"},
+                "gpu_launches": launches * args.steps,
+                "clocks": clocks,
+                "target_us_per_step": 550.0,
+                "extras": extras,
+                "host": {"arch": platform.machine(), "nproc": os.cpu_count(),
+                         "gpu": torch.cuda.get_device_name(local),
+                         "sm_count": torch.cuda.get_device_properties(local).multi_processor_count}}
+        print(json.dumps(line), flush=True)
+    seq.close()
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

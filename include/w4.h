@@ -1,0 +1,212 @@
+/*
+ * w4.h -- C ABI of libw4.so: symmetric group-wise INT4 weight-only
+ * projections (W4A16) for NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("Building a Custom LLM Inference Runtime for
+ * Qwen2.5-Coder-7B on NVIDIA H100 Hopper Architecture", section "Technical
+ * Specifications and Hardware Alignment"): weights are signed 4-bit integers
+ * q in [-8, 7], symmetric (no zero point), grouped 128 at a time along K,
+ * each group of one output row with one FP16 scale s; w[n,k] = q[n,k] *
+ * s[n, k/128].  Activations stay FP16 (same page, "The INT8 vs. FP16
+ * Activation Trade-off", Path B).  Every projection computes
+ *     y[m,n] = fp16( sum_k x[m,k] * w[n,k] )
+ * with exact products, FP32 accumulation and one round-to-nearest-even
+ * conversion to FP16 at the end.
+ *
+ * Conventions shared by every entry point
+ *  - Ownership: the caller allocates and owns every buffer (packed weights,
+ *    x, y, workspace).  The projection entry points and the sequence replay
+ *    allocate nothing ("The Architecture of Modern Inference ...",
+ *    ".nanoqwen Format": no heap allocation during generation).
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Device work is enqueued on it and the call returns
+ *    without waiting, unless the entry point says it is synchronous.
+ *  - Errors: arguments are checked before anything is launched; a failed
+ *    check launches nothing.  A CUDA launch error maps to W4_ERR_CUDA and
+ *    w4_last_error() gives its text (thread-local).
+ *  - Alignment: device pointers to packed weights, x and y must be 16-byte
+ *    aligned.
+ *  - Data types: fp16 values travel as their 16-bit IEEE-754 binary16
+ *    patterns (uint16_t); q travels as int8_t, one value per byte.
+ */
+#ifndef W4_H
+#define W4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4_OK = 0,
+    W4_ERR_ARG = 1,         /* NULL pointer, bad flag, wrong descriptor magic */
+    W4_ERR_SHAPE = 2,       /* K % 128 != 0, N < 1, M out of range */
+    W4_ERR_RANGE = 3,       /* a q outside [-8, 7] */
+    W4_ERR_ALIGN = 4,       /* a pointer not 16-byte aligned */
+    W4_ERR_WORKSPACE = 5,   /* workspace missing or too small */
+    W4_ERR_CUDA = 6,        /* a CUDA runtime call failed; see w4_last_error() */
+    W4_ERR_UNSUPPORTED = 7  /* no kernel for this device / configuration */
+} w4_status;
+
+/* Descriptor of a packed weight in device memory (a host-side struct). */
+#define W4_PACK_MAGIC 0x4B503457u /* "W4PK" */
+#define W4_PACK_VERSION 1u
+typedef struct {
+    const void* data; /* device pointer to w4_packed_bytes(N, K) bytes */
+    int64_t N;        /* output rows */
+    int64_t K;        /* reduction length, a multiple of 128 */
+    uint32_t magic;   /* W4_PACK_MAGIC */
+    uint32_t version; /* W4_PACK_VERSION */
+} w4_weight;
+
+const char* w4_strerror(w4_status status);
+/* Text of the last failure on the calling thread ("" if none). */
+const char* w4_last_error(void);
+/* Library version, major * 10000 + minor * 100 + patch. */
+int w4_version(void);
+
+/* ------------------------------------------------------------------------
+ * Packed layout (the offline repack).  The pages describe a "ValueShuffle"
+ * layout that interleaves even and odd nibbles for the byte-permute
+ * datapath ("Building a Custom LLM Inference Runtime ...", ".nanoqwen File
+ * Format and Safety Protocols"; "The Architecture of Modern Inference ...",
+ * ".nanoqwen Format"), without the exact permutation.  This library's
+ * layout puts each nibble where one warp lane needs it as a tensor-core
+ * operand fragment:
+ *
+ *   - The weight is cut into tiles of 16 rows x 128 K (one scale group per
+ *     row).  Tile (band b, group g) starts at byte (b * (K/128) + g) * 1056;
+ *     a band's tiles are contiguous along K.  ceil(N/16) bands.
+ *   - A tile holds 1024 bytes of nibbles then 32 bytes of scales; every
+ *     tile starts on a 32-byte boundary relative to the base.
+ *   - Nibbles are offset binary, u = q + 8.  Lane L = 4r + c (r = 0..7,
+ *     c = 0..3) and k16-step j = 0..7 own the little-endian 32-bit word at
+ *     byte (j < 4 ? 0 : 512) + 16 L + 4 (j mod 4), whose nibble i (bits
+ *     4i..4i+3) is, for i = 0..7:
+ *        u[r][16j+2c],   u[r+8][16j+2c],   u[r][16j+2c+8], u[r+8][16j+2c+8],
+ *        u[r][16j+2c+1], u[r+8][16j+2c+1], u[r][16j+2c+9], u[r+8][16j+2c+9]
+ *     (row relative to the band, k relative to the group).  Masking nibbles
+ *     {0,4} and {1,5} of a word (and of the word shifted right by 8) gives
+ *     the four f16x2 registers of an m16n8k16 A fragment.
+ *   - Bytes 1024 + 4p .. +3 (p = 0..7) hold the fp16 scales of rows p (low
+ *     half) and p + 8 (high half).
+ *   - Rows n >= N of the last band are padding: u = 8 (q = 0), scale 0.
+ * ---------------------------------------------------------------------- */
+
+/* Bytes of the packed layout for an N x K weight; 0 if N < 1, K < 128 or
+ * K % 128 != 0. */
+size_t w4_packed_bytes(int64_t N, int64_t K);
+
+/* Fill a descriptor for an already packed device buffer (no device work). */
+w4_status w4_weight_view(const void* packed_dev, int64_t N, int64_t K,
+                         w4_weight* out);
+
+/* Host-only repack (no GPU needed): q int8 [N, K] row-major, scales fp16
+ * [N, K/128] row-major -> dst (dst_bytes >= w4_packed_bytes(N, K)).
+ * W4_ERR_RANGE if any q is outside [-8, 7] (nothing is clamped). */
+w4_status w4_pack_host(const int8_t* q, const uint16_t* scales, int64_t N,
+                       int64_t K, void* dst, size_t dst_bytes);
+
+/* Host-only inverse of w4_pack_host: packed -> q [N, K], scales [N, K/128]. */
+w4_status w4_unpack_host(const void* packed, int64_t N, int64_t K, int8_t* q,
+                         uint16_t* scales);
+
+/* Offline repack into device memory (the hot path never calls it).
+ * src_on_device = 0: q and scales are host arrays, packed on the host and
+ * copied in.  src_on_device = 1: they are device arrays, packed by a
+ * kernel.  SYNCHRONOUS: returns after the packed bytes are in dst_dev, so
+ * that an out-of-range q can be reported (W4_ERR_RANGE; dst_dev contents are
+ * then unspecified).  May allocate temporary host or device memory.  On
+ * success fills *out (may be NULL). */
+w4_status w4_pack(const int8_t* q, const uint16_t* scales, int64_t N, int64_t K,
+                  void* dst_dev, size_t dst_bytes, int src_on_device,
+                  void* stream, w4_weight* out);
+
+/* Inverse of w4_pack (round trip): q [N, K] int8 and scales [N, K/128]
+ * fp16.  dst_on_device selects device (a kernel) or host outputs.
+ * Synchronous. */
+w4_status w4_unpack(const w4_weight* w, int8_t* q, uint16_t* scales,
+                    int dst_on_device, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Projections
+ * ---------------------------------------------------------------------- */
+
+/* Workspace bytes w4a16_gemv / w4a16_gemm need for this shape (0 = none;
+ * pass NULL, 0). */
+size_t w4_workspace_bytes(int M, int64_t N, int64_t K);
+
+/* Decode projection, 1 <= M <= 16:  y[M, N] = x[M, K] . W^T.
+ * x fp16 [M, K] row-major, y fp16 [M, N] row-major, both device.  Each packed
+ * weight byte is read once per call whatever M.  Asynchronous on `stream`;
+ * deterministic (same bits run to run).  Launched with programmatic
+ * dependent launch enabled: the weight stream starts before the previous
+ * kernel on the stream has finished; x is read only after it has. */
+w4_status w4a16_gemv(const void* x, const w4_weight* w, void* y, int M,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Launch shape of the decode kernel, for tuning sweeps.  Zero fields take
+ * the library's choice. */
+typedef struct {
+    int bands_per_cta; /* 16-row bands per CTA: 1, 2 or 4 */
+    int splits;        /* K splits = CTAs per cluster: 1..8 */
+    int depth;         /* groups in flight per warp: 1..4 (1, 2, 4) */
+    int pdl;           /* 1: programmatic dependent launch (default), 0: off, -1: default */
+} w4_gemv_config;
+
+/* w4a16_gemv with an explicit launch shape (W4_ERR_UNSUPPORTED if the shape
+ * has no kernel). */
+w4_status w4a16_gemv_config(const void* x, const w4_weight* w, void* y, int M,
+                            const w4_gemv_config* cfg, void* stream);
+
+/* The launch shape w4a16_gemv picks for (M, N, K). */
+w4_status w4a16_gemv_default_config(int M, int64_t N, int64_t K,
+                                    w4_gemv_config* out);
+
+/* Prefill projection, any M >= 1 (tuned for M = 512): same contract as
+ * w4a16_gemv.  M <= 16 uses the decode kernel. */
+w4_status w4a16_gemm(const void* x, const w4_weight* w, void* y, int M,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Decode step sequence ("Building a Custom LLM Inference Runtime ...",
+ * "The Impact of CUDA Graphs": capturing the whole decode step in one CUDA
+ * graph took eager launches from ~119 ms to ~17 ms per token).
+ * ---------------------------------------------------------------------- */
+typedef struct w4_seq w4_seq;
+
+/* Build the projection chain w[0] .. w[n-1] (in that order), projection i
+ * reading x[i] and writing y[i], all with the same M (1..16), and capture it
+ * once as a CUDA graph.  Consecutive projections are joined by programmatic
+ * dependent launch edges when use_pdl != 0.  The pointers are baked into the
+ * graph: create a new sequence to change them.  Allocates host-side graph
+ * objects and a private capture stream (not on the hot path); synchronous. */
+w4_status w4_decode_seq_create(const w4_weight* w, const void* const* x,
+                               void* const* y, int n, int M, int use_pdl,
+                               void* stream, w4_seq** out);
+
+/* One replay of the captured chain: a single cudaGraphLaunch on `stream`. */
+w4_status w4_decode_seq_replay(w4_seq* seq, void* stream);
+
+/* The same launches issued one by one, without the graph (for comparison). */
+w4_status w4_decode_seq_eager(w4_seq* seq, void* stream);
+
+/* End to end with host buffers: copy x_bytes from pinned host memory x_host
+ * to the device range x_dev, replay, copy y_bytes from y_dev to y_host, and
+ * wait for the stream.  x_dev / y_dev are device ranges that hold the
+ * sequence's x and y buffers (e.g. one arena each).  Synchronous. */
+w4_status w4_decode_seq_run_host(w4_seq* seq, const void* x_host, void* x_dev,
+                                 size_t x_bytes, void* y_dev, void* y_host,
+                                 size_t y_bytes, void* stream);
+
+/* Number of kernels one replay launches. */
+int w4_decode_seq_kernels(const w4_seq* seq);
+
+void w4_decode_seq_destroy(w4_seq* seq);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* W4_H */

@@ -34,6 +34,11 @@ never need to agree between two implementations.
 """
 from __future__ import annotations
 
+import ctypes
+import os
+import shutil
+import subprocess
+
 import numpy as np
 
 GOLDEN = np.uint64(0x9E3779B97F4A7C15)
@@ -125,3 +130,52 @@ def projection_inputs(config: int, layer: int, proj: int, M: int, N: int, K: int
     if rows is None:
         rows = np.arange(N)
     return q_rows(sq, K, rows), scale_rows(ss, G, rows), x_full(sx, M, K)
+
+
+# ---- device generator (synth/gen.cu) ------------------------------------
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_GEN_SRC = os.path.join(_HERE, "gen.cu")
+_GEN_LIB = os.path.join(_HERE, "libsynth.so")
+_gen = None
+
+
+def build_device(force: bool = False) -> str:
+    """Compile the device generator for sm_103a (nvcc)."""
+    if force or not os.path.exists(_GEN_LIB) or os.path.getmtime(_GEN_LIB) < os.path.getmtime(_GEN_SRC):
+        nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+        tmp = _GEN_LIB + ".tmp.%d" % os.getpid()
+        subprocess.check_call([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+                               "-Xcompiler", "-fPIC", "-shared", "-cudart", "shared", "-o", tmp, _GEN_SRC])
+        os.replace(tmp, _GEN_LIB)
+    return _GEN_LIB
+
+
+def _device_lib():
+    global _gen
+    if _gen is None:
+        build_device()
+        L = ctypes.CDLL(_GEN_LIB)
+        for name in ("synth_q_device", "synth_scale_device"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [ctypes.c_uint64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+        _gen = L
+    return _gen
+
+
+def q_device(seed: int, N: int, K: int, out, stream=None):
+    """Fill the int8 device tensor ``out`` ([N, K]) with q of this seed."""
+    import torch
+    st = (stream or torch.cuda.current_stream()).cuda_stream
+    rc = _device_lib().synth_q_device(seed & _MASK64, 0, N * K, out.data_ptr(), st)
+    if rc != 0:
+        raise RuntimeError("synth_q_device failed: cuda error %d" % rc)
+
+
+def scale_device(seed: int, N: int, G: int, out, stream=None):
+    """Fill the int16/uint16 device tensor ``out`` ([N, G]) with fp16 scale bits."""
+    import torch
+    st = (stream or torch.cuda.current_stream()).cuda_stream
+    rc = _device_lib().synth_scale_device(seed & _MASK64, 0, N * G, out.data_ptr(), st)
+    if rc != 0:
+        raise RuntimeError("synth_scale_device failed: cuda error %d" % rc)

@@ -1,0 +1,122 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point that
+include/w4.h declares, and its host-side pack/unpack is bit-exact against the
+oracle's writer of the layout.  No device compute is called here."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import ROOT
+
+w4 = pytest.importorskip("int4_weight_only_pack_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from int4_weight_only_pack_gb300 import build
+    build.build()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "w4.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    names = re.findall(r"\b(w4\w*)\s*\([^;{}]*\)\s*;", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 20
+    L = w4.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(w4.EXPORTED)
+
+
+def test_strerror_and_version():
+    assert w4.w4_strerror(0) == "ok"
+    assert "[-8, 7]" in w4.w4_strerror(3)
+    assert w4.lib().w4_version() >= 10000
+
+
+@pytest.mark.parametrize("N,K", [(16, 128), (4608 // 64, 3584 // 4), (37, 256), (1, 128), (100, 384)])
+def test_packed_bytes(N, K):
+    assert w4.w4_packed_bytes(N, K) == ((N + 15) // 16) * (K // 128) * 1056
+
+
+def test_packed_bytes_of_the_layer_shapes():
+    total = sum(w4.w4_packed_bytes(N, K) for N, K in
+                [(4608, 3584), (3584, 3584), (37888, 3584), (3584, 18944)])
+    assert total == 120_164_352
+    assert w4.w4_packed_bytes(4608, 3584) == 8_515_584
+
+
+@pytest.mark.parametrize("N,K,seed", [(16, 128, 0), (37, 384, 1), (100, 256, 2), (5, 1280, 3)])
+def test_host_pack_matches_oracle_layout_bit_exact(N, K, seed):
+    rng = np.random.default_rng(seed)
+    q = rng.integers(-8, 8, (N, K)).astype(np.int8)
+    s = rng.integers(0, 0x7C00, (N, K // 128)).astype(np.uint16)
+    got = w4.w4_pack_host(q, s)
+    want = oracle.pack_layout(q, s)
+    assert np.array_equal(got, want)
+    q2, s2 = w4.w4_unpack_host(got, N, K)
+    assert np.array_equal(q2, q) and np.array_equal(s2, s)
+
+
+def test_host_pack_every_nibble_value_in_every_position():
+    N, K = 16, 128
+    base = np.arange(N * K).reshape(N, K)
+    for shift in range(16):
+        q = (((base + shift) % 16) - 8).astype(np.int8)
+        s = np.full((N, 1), 0x3C00, np.uint16)
+        p = w4.w4_pack_host(q, s)
+        assert np.array_equal(p, oracle.pack_layout(q, s))
+        assert np.array_equal(w4.w4_unpack_host(p, N, K)[0], q)
+
+
+def test_host_pack_rejects_out_of_range_and_bad_shapes():
+    q = np.zeros((4, 128), np.int8)
+    s = np.zeros((4, 1), np.uint16)
+    q[2, 5] = 8
+    with pytest.raises(w4.W4Error) as e:
+        w4.w4_pack_host(q, s)
+    assert e.value.status == 3
+    with pytest.raises(w4.W4Error) as e:
+        w4.w4_pack_host(np.zeros((4, 100), np.int8), np.zeros((4, 1), np.uint16))
+    assert e.value.status == 2
+    assert w4.w4_packed_bytes(0, 128) == 0 and w4.w4_packed_bytes(4, 100) == 0
+
+
+def test_weight_view_checks():
+    w = w4.w4_weight_view(0x1000, 16, 128)
+    assert w.magic == w4.W4_PACK_MAGIC and w.version == w4.W4_PACK_VERSION
+    with pytest.raises(w4.W4Error) as e:
+        w4.w4_weight_view(0x1008, 16, 128)
+    assert e.value.status == 4
+    with pytest.raises(w4.W4Error) as e:
+        w4.w4_weight_view(0x1000, 16, 200)
+    assert e.value.status == 2
+
+
+def test_projection_argument_checks_need_no_gpu():
+    """Bad arguments are rejected before anything is launched."""
+    w = w4.w4_weight_view(0x1000, 64, 256)
+    for M, x, y, code in [(0, 0x2000, 0x3000, 2), (17, 0x2000, 0x3000, 2), (1, 0x2004, 0x3000, 4),
+                          (1, 0, 0x3000, 1)]:
+        with pytest.raises(w4.W4Error) as e:
+            w4.w4a16_gemv(x, w, y, M, stream=0)
+        assert e.value.status == code
+    bad = w4.Weight(0x1000, 64, 256, 0x12345678, 1)
+    with pytest.raises(w4.W4Error) as e:
+        w4.w4a16_gemv(0x2000, bad, 0x3000, 1, stream=0)
+    assert e.value.status == 1
+
+
+def test_default_configs_of_the_layer_shapes():
+    for M in (1, 2, 4, 8, 16):
+        for N, K in [(4608, 3584), (3584, 3584), (37888, 3584), (3584, 18944)]:
+            c = w4.w4a16_gemv_default_config(M, N, K)
+            assert c.bands_per_cta in (1, 2, 4) and 1 <= c.splits <= 8 and c.depth in (1, 2, 4)

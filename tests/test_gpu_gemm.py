@@ -1,0 +1,55 @@
+"""Prefill projection (M > 16) through the C ABI against the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_helpers import LAYER, assert_close, dev, host, oracle_rows, pack_on_device, rand_problem, synth_weight
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+w4 = pytest.importorskip("int4_weight_only_pack_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from int4_weight_only_pack_gb300 import build
+    build.build()
+
+
+def run(x, w, N, M):
+    y = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
+    ws = w4.w4_workspace_bytes(M, N, w.K)
+    buf = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
+    w4.w4a16_gemm(dev(x), w, y, M, buf if ws else None, ws)
+    torch.cuda.synchronize()
+    return host(y)
+
+
+@pytest.mark.parametrize("M,N,K", [(17, 64, 256), (40, 136, 384), (128, 256, 512), (512, 256, 1024),
+                                   (512, 200, 1280), (300, 128, 2048), (1, 64, 256), (16, 64, 256)])
+def test_parity(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    x, q, s = rand_problem(rng, M, N, K)
+    packed, w = pack_on_device(q, s)
+    assert_close(run(x, w, N, M), oracle.linear(x, q, s), "M=%d N=%d K=%d" % (M, N, K))
+
+
+@pytest.mark.parametrize("proj", list(LAYER))
+def test_full_layer_shapes_m512_sampled(proj):
+    M = 512
+    N, K = LAYER[proj]
+    pid = list(LAYER).index(proj)
+    packed, w = synth_weight(5, 0, pid, N, K)
+    rows = np.unique(np.concatenate([[0, 1, N - 1], np.random.default_rng(pid).integers(0, N, 13)]))
+    ref, x = oracle_rows(5, 0, pid, M, N, K, rows)
+    assert_close(run(x, w, N, M)[:, rows], ref, "%s M=512" % proj)
+
+
+def test_deterministic():
+    rng = np.random.default_rng(4)
+    x, q, s = rand_problem(rng, 256, 512, 1024)
+    packed, w = pack_on_device(q, s)
+    a, b = run(x, w, 512, 256), run(x, w, 512, 256)
+    assert np.array_equal(a, b)
