@@ -85,11 +85,15 @@ int w4_version(void);
  *     c = 0..3) and k16-step j = 0..7 own the little-endian 32-bit word at
  *     byte (j < 4 ? 0 : 512) + 16 L + 4 (j mod 4), whose nibble i (bits
  *     4i..4i+3) is, for i = 0..7:
- *        u[r][16j+2c],   u[r+8][16j+2c],   u[r][16j+2c+8], u[r+8][16j+2c+8],
- *        u[r][16j+2c+1], u[r+8][16j+2c+1], u[r][16j+2c+9], u[r+8][16j+2c+9]
- *     (row relative to the band, k relative to the group).  Masking nibbles
- *     {0,4} and {1,5} of a word (and of the word shifted right by 8) gives
- *     the four f16x2 registers of an m16n8k16 A fragment.
+ *        u[r][16j+4c],   u[r+8][16j+4c],   u[r][16j+4c+2], u[r+8][16j+4c+2],
+ *        u[r][16j+4c+1], u[r+8][16j+4c+1], u[r][16j+4c+3], u[r+8][16j+4c+3]
+ *     (row relative to the band, k relative to the group): a lane holds four
+ *     consecutive k of rows r and r + 8.  Masking nibbles {0,4} and {1,5} of
+ *     a word (and of the word shifted right by 8) gives four f16x2 registers,
+ *     (r, 4c..4c+1), (r+8, 4c..4c+1), (r, 4c+2..4c+3), (r+8, 4c+2..4c+3):
+ *     an m16n8k16 A fragment once k inside each 16-block is relabelled
+ *     (fragment k 2c, 2c+1, 2c+8, 2c+9 <-> 4c .. 4c+3, the same relabelling
+ *     applied to the activations), and two 8-byte rows of a K-major tile.
  *   - Bytes 1024 + 4p .. +3 (p = 0..7) hold the fp16 scales of rows p (low
  *     half) and p + 8 (high half).
  *   - Rows n >= N of the last band are padding: u = 8 (q = 0), scale 0.
@@ -134,8 +138,12 @@ w4_status w4_unpack(const w4_weight* w, int8_t* q, uint16_t* scales,
  * Projections
  * ---------------------------------------------------------------------- */
 
-/* Workspace bytes w4a16_gemv / w4a16_gemm need for this shape (0 = none;
- * pass NULL, 0). */
+/* Device workspace bytes a projection of this shape needs (0 = none; pass
+ * NULL, 0).  The decode kernel (M <= 16) needs none.  The prefill kernel
+ * (M > 16) needs at least 256 bytes: the first 4 hold a status word that the
+ * call clears and the kernel sets non-zero if one of its pipeline waits gave
+ * up (it then exits instead of hanging; y is not valid); when K is split
+ * across CTAs the FP32 partials [splits][M][N] follow at byte 256. */
 size_t w4_workspace_bytes(int M, int64_t N, int64_t K);
 
 /* Decode projection, 1 <= M <= 16:  y[M, N] = x[M, K] . W^T.
@@ -166,7 +174,11 @@ w4_status w4a16_gemv_default_config(int M, int64_t N, int64_t K,
                                     w4_gemv_config* out);
 
 /* Prefill projection, any M >= 1 (tuned for M = 512): same contract as
- * w4a16_gemv.  M <= 16 uses the decode kernel. */
+ * w4a16_gemv, plus the workspace of w4_workspace_bytes (W4_ERR_WORKSPACE if
+ * it is missing or short).  M <= 16 uses the decode kernel.  M > 16 runs on
+ * the tensor cores (tcgen05, accumulators in TMEM): exact fp16 q times fp16 x
+ * summed in FP32 per 128-wide group, then scaled and added in FP32.
+ * Deterministic.  Not launched with programmatic dependent launch. */
 w4_status w4a16_gemm(const void* x, const w4_weight* w, void* y, int M,
                      void* workspace, size_t workspace_bytes, void* stream);
 

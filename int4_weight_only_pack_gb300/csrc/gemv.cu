@@ -32,6 +32,7 @@
 #include <set>
 #include <utility>
 
+#include "w4_device.cuh"
 #include "w4_internal.cuh"
 
 namespace cg = cooperative_groups;
@@ -48,45 +49,6 @@ struct GemvParams {
     uint16_t* y;        // fp16 [M, N]
     int M, N, K, G, bands;
 };
-
-__device__ __forceinline__ uint4 ld_stream16(const uint8_t* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t ld_stream4(const uint8_t* p) {
-    uint32_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-
-// (v & mask) | magic in one LOP3.
-__device__ __forceinline__ uint32_t and_or(uint32_t v, uint32_t mask, uint32_t magic) {
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(mask), "r"(magic));
-    return r;
-}
-
-// Eight nibbles u (offset binary) -> four f16x2 registers holding q = u - 8,
-// in the register order of an m16n8k16 A fragment (see include/w4.h).
-__device__ __forceinline__ void unpack_word(uint32_t v, uint32_t (&a)[4]) {
-    const uint32_t lo_mask = 0x000F000Fu, hi_mask = 0x00F000F0u, magic = 0x64006400u;
-    const uint32_t v8 = v >> 8;
-    const uint32_t t0 = and_or(v, lo_mask, magic);   // 1024 + u  (nibbles 0, 4)
-    const uint32_t t1 = and_or(v, hi_mask, magic);   // 1024 + 16u (nibbles 1, 5)
-    const uint32_t t2 = and_or(v8, lo_mask, magic);  // nibbles 2, 6
-    const uint32_t t3 = and_or(v8, hi_mask, magic);  // nibbles 3, 7
-    const uint32_t k1032 = 0x64086408u;              // 1032
-    const uint32_t k1_16 = 0x2C002C00u;              // 1/16
-    const uint32_t km72 = 0xD480D480u;               // -72
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(a[0]) : "r"(t0), "r"(k1032));
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(a[1]) : "r"(t1), "r"(k1_16), "r"(km72));
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(a[2]) : "r"(t2), "r"(k1032));
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(a[3]) : "r"(t3), "r"(k1_16), "r"(km72));
-}
 
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -153,8 +115,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
         for (int idx = threadIdx.x; idx < M * per_row; idx += kThreads) {
             const int m = idx / per_row, r = idx - m * per_row;
             const uint32_t v = __ldcg(xg + (size_t)m * kp + r);
+            // pair kk2 of the group = k 2*kk2, 2*kk2+1; lane class c owns
+            // k 4c..4c+3 of each k16 step (the lower pair is b0, the upper b1)
             const int gl = r >> 6, kk2 = r & 63;
-            const int j = kk2 >> 3, c = kk2 & 3, hi = (kk2 >> 2) & 1;
+            const int j = kk2 >> 3, c = (kk2 >> 1) & 3, hi = kk2 & 1;
             xs[gl * (M * 64) + (j >> 1) * (M * 16) + (m * 4 + c) * 4 + (j & 1) * 2 + hi] = v;
         }
     }
@@ -422,13 +386,6 @@ w4_status check_gemv_args(const void* x, const w4_weight* w, const void* y, int 
 }  // namespace w4
 
 using namespace w4;
-
-extern "C" size_t w4_workspace_bytes(int M, int64_t N, int64_t K) {
-    (void)M;
-    (void)N;
-    (void)K;
-    return 0;
-}
 
 extern "C" w4_status w4a16_gemv_default_config(int M, int64_t N, int64_t K, w4_gemv_config* out) {
     clear_error();

@@ -18,10 +18,10 @@ namespace w4 {
 
 // Nibble i (0..7) of the word owned by lane L = 4r + c at k16-step j holds the
 // element at (row within band, k within group):
-//   row = r + 8 * (i & 1),  k = 16 j + 2 c + 8 * ((i >> 1) & 1) + (i >> 2).
+//   row = r + 8 * (i & 1),  k = 16 j + 4 c + 2 * ((i >> 1) & 1) + (i >> 2).
 __host__ __device__ inline int nib_row(int L, int i) { return (L >> 2) + 8 * (i & 1); }
 __host__ __device__ inline int nib_k(int L, int j, int i) {
-    return 16 * j + 2 * (L & 3) + 8 * ((i >> 1) & 1) + (i >> 2);
+    return 16 * j + 4 * (L & 3) + 2 * ((i >> 1) & 1) + (i >> 2);
 }
 // Byte offset of that word inside its tile.
 __host__ __device__ inline int word_offset(int L, int j) { return (j >> 2) * 512 + 16 * L + 4 * (j & 3); }

@@ -184,10 +184,10 @@ int w4o_pack_layout(const int8_t* q, const uint16_t* s, int64_t N, int64_t K,
                     /* (row offset within band, k offset within group) of
                      * nibbles 0..7 of the word, as the definition lists */
                     const int row[8] = {r, r + 8, r, r + 8, r, r + 8, r, r + 8};
-                    const int kk[8] = {16 * j + 2 * c,     16 * j + 2 * c,
-                                       16 * j + 2 * c + 8, 16 * j + 2 * c + 8,
-                                       16 * j + 2 * c + 1, 16 * j + 2 * c + 1,
-                                       16 * j + 2 * c + 9, 16 * j + 2 * c + 9};
+                    const int kk[8] = {16 * j + 4 * c,     16 * j + 4 * c,
+                                       16 * j + 4 * c + 2, 16 * j + 4 * c + 2,
+                                       16 * j + 4 * c + 1, 16 * j + 4 * c + 1,
+                                       16 * j + 4 * c + 3, 16 * j + 4 * c + 3};
                     uint32_t word = 0;
                     for (int i = 0; i < 8; ++i) {
                         int64_t n = b * 16 + row[i];

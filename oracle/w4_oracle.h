@@ -60,10 +60,10 @@ int w4o_linear(const uint16_t* x, const int8_t* q, const uint16_t* s,
  * of warp lane L (L = 4*r + c, r in 0..7, c in 0..3) and k16-step j (0..7)
  * sits at byte (j < 4 ? 0 : 512) + 16*L + 4*(j % 4) of the tile, little
  * endian, and holds in nibble i (bits 4i..4i+3):
- *   i=0: u[r][16j+2c]    i=1: u[r+8][16j+2c]
- *   i=2: u[r][16j+2c+8]  i=3: u[r+8][16j+2c+8]
- *   i=4: u[r][16j+2c+1]  i=5: u[r+8][16j+2c+1]
- *   i=6: u[r][16j+2c+9]  i=7: u[r+8][16j+2c+9]
+ *   i=0: u[r][16j+4c]    i=1: u[r+8][16j+4c]
+ *   i=2: u[r][16j+4c+2]  i=3: u[r+8][16j+4c+2]
+ *   i=4: u[r][16j+4c+1]  i=5: u[r+8][16j+4c+1]
+ *   i=6: u[r][16j+4c+3]  i=7: u[r+8][16j+4c+3]
  * (rows relative to the band, k relative to the group).  Bytes
  * 1024 + 4p .. 1024 + 4p + 3 (p = 0..7) hold the fp16 scales of rows p
  * (low half) and p + 8 (high half).  Rows n >= N are padding: u = 8, scale 0.
