@@ -1,7 +1,36 @@
-// Prefill projection y[M, N] = x[M, K] . W^T for any M >= 1.
+// Prefill projection y[M, N] = x[M, K] . W^T for M > 16 on the sm_103a
+// tensor cores (tcgen05 + TMEM); M <= 16 goes to the decode kernel.
 //
-// M <= 16 goes to the decode kernel.  Larger M is processed as consecutive
-// 16-token slices of the decode kernel, each reading the whole weight again.
+// Same arithmetic as the decode kernel and the pages' definition (symmetric
+// group-wise INT4, group 128, FP16 scale per group, FP16 activations:
+// "Building a Custom LLM Inference Runtime ...", "Technical Specifications and
+// Hardware Alignment"): FP16 x FP16 products are exact, each 128-wide group is
+// summed in FP32 by the tensor core, and the group's FP32 partial is scaled by
+// its FP32 scale and added in FP32 registers.  The scale is never folded into
+// an FP16 weight, so the weights reach the tensor core exactly.
+//
+// One CTA computes a 128 (weight rows) x 128 (tokens) tile over a K range,
+// one 128-wide group per pipeline stage, with warp-specialised roles:
+//   warp 0     TMA producer: x tile [128 tokens][128 K] as two 128-byte
+//              swizzled boxes (zero fill past M)
+//   warp 1     one thread issues 8 tcgen05.mma (128x128x16) per group into a
+//              TMEM buffer (two buffers alternate), then commits
+//   warps 4-7  dequant: stream the 8 packed tiles of the group (16-byte
+//              non-coherent loads, next group prefetched), unpack nibbles to
+//              exact fp16 q, write them K-major with the 128-byte swizzle
+//   warps 8-15 promote: read the group's FP32 partial from TMEM, multiply by
+//              the group scale and add to FP32 accumulators in registers;
+//              finally write y (or an FP32 split-K partial)
+// Every mbarrier wait is bounded; a timeout sets the status word in the
+// workspace and the CTA drains and exits instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "tc_ptx.cuh"
+#include "w4_device.cuh"
 #include "w4_internal.cuh"
 
 namespace w4 {
@@ -9,37 +38,372 @@ void default_gemv_config(int M, int64_t N, int64_t K, w4_gemv_config* c);
 w4_status launch_gemv(const void* x, const w4_weight* w, void* y, int M, const w4_gemv_config& c,
                       cudaStream_t stream);
 w4_status check_gemv_args(const void* x, const w4_weight* w, const void* y, int M);
+
+namespace {
+
+constexpr int kBM = 128;                   // weight rows per CTA (8 bands)
+constexpr int kBN = 128;                   // tokens per CTA
+constexpr int kStages = 3;                 // one 128-wide K group per stage
+constexpr int kAStage = kBM * 128 * 2;     // 32 KB of fp16 q
+constexpr int kBStage = kBN * 128 * 2;     // 32 KB of fp16 x
+constexpr int kThreads = 512;
+constexpr int kTmemCols = 256;             // two 128-column FP32 accumulators
+constexpr int kSmemBytes = kStages * (kAStage + kBStage) + 1024 + 256;
+constexpr size_t kStatusBytes = 256;       // workspace head: status word (+ padding)
+
+struct GemmParams {
+    const uint8_t* w;
+    uint16_t* y;
+    float* part;  // split-K partials [splits][M][N], or null
+    int* status;
+    int M, N, K, G, bands, splits;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + kStages * kAStage;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBStage);
+    // barrier slots
+    const uint32_t x_full = tc::smem_addr(bars), a_full = x_full + 8 * kStages, empty = a_full + 8 * kStages,
+                   d_full = empty + 8 * kStages, d_empty = d_full + 16;
+    __shared__ uint32_t tmem_base_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tok0 = blockIdx.x * kBN;
+    const int band0 = blockIdx.y * (kBM / 16);
+    const int split = blockIdx.z;
+    const int g_lo = (int)((long long)p.G * split / p.splits);
+    const int g_hi = (int)((long long)p.G * (split + 1) / p.splits);
+    const int ng = g_hi - g_lo;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(x_full + 8 * s, 1);
+            tc::mbar_init(a_full + 8 * s, 4);
+            tc::mbar_init(empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(d_full + 8 * b, 1);
+            tc::mbar_init(d_empty + 8 * b, 8);
+        }
+        tc::mbar_init_fence();
+        tc::prefetch_tensormap(&xmap);
+    }
+    if (warp == 1) tc::tmem_alloc(tc::smem_addr(&tmem_base_sh), kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == 0) {
+        // ---- TMA producer ---------------------------------------------------
+        if (lane == 0) {
+            int issued = 0;
+            for (int it = 0; it < ng; ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1;
+                if (!tc::mbar_wait(empty + 8 * s, ph ^ 1)) {
+                    atomicOr(p.status, 1);
+                    break;
+                }
+                const uint32_t dst = tc::smem_addr(sB + s * kBStage);
+                tc::mbar_arrive_expect_tx(x_full + 8 * s, kBStage);
+                const int k0 = (g_lo + it) * 128;
+                tc::tma_load_2d(dst, &xmap, k0, tok0, x_full + 8 * s);
+                tc::tma_load_2d(dst + kBStage / 2, &xmap, k0 + 64, tok0, x_full + 8 * s);
+                ++issued;
+            }
+            // drain: the last load of every stage has landed before the CTA exits
+            for (int it = issued - 1; it >= 0 && it >= issued - kStages; --it)
+                if (!tc::mbar_wait(x_full + 8 * (it % kStages), (it / kStages) & 1)) atomicOr(p.status, 2);
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer -------------------------------------------------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_f16_f32(kBM, kBN);
+            int done = 0;
+            for (int it = 0; it < ng; ++it) {
+                const int s = it % kStages, b = it & 1;
+                const uint32_t ph = (it / kStages) & 1, bph = (it >> 1) & 1;
+                if (!tc::mbar_wait(x_full + 8 * s, ph) || !tc::mbar_wait(a_full + 8 * s, ph) ||
+                    !tc::mbar_wait(d_empty + 8 * b, bph ^ 1)) {
+                    atomicOr(p.status, 4);
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t a0 = tc::smem_addr(sA + s * kAStage), b0 = tc::smem_addr(sB + s * kBStage);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t off = (j >> 2) * (kAStage / 2) + (j & 3) * 32;
+                    tc::mma_f16(tmem + b * 128, tc::sw128_kmajor_desc(a0 + off), tc::sw128_kmajor_desc(b0 + off), idesc,
+                                j > 0);
+                }
+                tc::mma_commit(empty + 8 * s);
+                tc::mma_commit(d_full + 8 * b);
+                done = it + 1;
+            }
+            // drain: every issued MMA has completed before TMEM is released
+            if (done > 0 && !tc::mbar_wait(d_full + 8 * ((done - 1) & 1), ((done - 1) >> 1) & 1))
+                atomicOr(p.status, 8);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---- dequant: 2 bands per warp ----------------------------------------
+        const int dw = warp - 4;
+        const int r = lane >> 2, c = lane & 3;
+        uint4 lo[2], hi[2], nlo[2], nhi[2];
+        auto load = [&](int it, uint4 (&L)[2], uint4 (&H)[2]) {
+#pragma unroll
+            for (int bi = 0; bi < 2; ++bi) {
+                const int bg = band0 + 2 * dw + bi;
+                if (bg < p.bands) {
+                    const uint8_t* t = p.w + ((size_t)bg * p.G + g_lo + it) * kTileBytes;
+                    L[bi] = ld_stream16(t + 16 * lane);
+                    H[bi] = ld_stream16(t + 512 + 16 * lane);
+                } else {
+                    L[bi] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);  // q = 0
+                    H[bi] = L[bi];
+                }
+            }
+        };
+        if (ng > 0) load(0, lo, hi);
+        for (int it = 0; it < ng; ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (it / kStages) & 1;
+            if (it + 1 < ng) load(it + 1, nlo, nhi);
+            if (!tc::mbar_wait(empty + 8 * s, ph ^ 1)) {
+                atomicOr(p.status, 16);
+                break;
+            }
+            const uint32_t a0 = tc::smem_addr(sA + s * kAStage);
+#pragma unroll
+            for (int bi = 0; bi < 2; ++bi) {
+                const uint32_t wd[8] = {lo[bi].x, lo[bi].y, lo[bi].z, lo[bi].w, hi[bi].x, hi[bi].y, hi[bi].z, hi[bi].w};
+                const int row0 = 16 * (2 * dw + bi) + r;  // row1 = row0 + 8 shares row0's swizzle phase
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t a[4];
+                    unpack_word(wd[j], a);
+                    const uint32_t chunk = 2 * (j & 3) + (c >> 1);
+                    const uint32_t addr = a0 + (j >> 2) * (kAStage / 2) + row0 * 128 + ((chunk ^ (uint32_t)r) << 4) +
+                                          (c & 1) * 8;
+                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a[0]), "r"(a[2]) : "memory");
+                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr + 1024), "r"(a[1]), "r"(a[3])
+                                 : "memory");
+                }
+            }
+            tc::fence_async_shared();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(a_full + 8 * s);
+#pragma unroll
+            for (int bi = 0; bi < 2; ++bi) {
+                lo[bi] = nlo[bi];
+                hi[bi] = nhi[bi];
+            }
+        }
+    } else if (warp >= 8) {
+        // ---- promote + epilogue -------------------------------------------------
+        const int quarter = warp & 3, half = (warp - 8) >> 2;
+        const int row = 32 * quarter + lane;  // TMEM lane = weight row within the tile
+        const int bandg = band0 + (row >> 4), rr = row & 15;
+        const bool row_ok = bandg < p.bands;
+        const uint8_t* sc = p.w + (size_t)bandg * p.G * kTileBytes + kScaleOffset + 4 * (rr & 7) + 2 * (rr >> 3);
+        float acc[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+        auto scale_of = [&](int it) -> float {
+            if (!row_ok) return 0.f;
+            const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(sc + (size_t)(g_lo + it) * kTileBytes));
+            return __half2float(__ushort_as_half(h));
+        };
+        float s_cur = ng > 0 ? scale_of(0) : 0.f;
+        bool ok = true;
+        for (int it = 0; it < ng; ++it) {
+            const int b = it & 1;
+            const uint32_t bph = (it >> 1) & 1;
+            const float s_next = (it + 1 < ng) ? scale_of(it + 1) : 0.f;
+            if (!tc::mbar_wait(d_full + 8 * b, bph)) {
+                atomicOr(p.status, 32);
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + b * 128 + 64 * half;
+            uint32_t v[32];
+            tc::tmem_ld_32x32(taddr, v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = fmaf(s_cur, __uint_as_float(v[i]), acc[i]);
+            tc::tmem_ld_32x32(taddr + 32, v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(s_cur, __uint_as_float(v[i]), acc[32 + i]);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(d_empty + 8 * b);
+            s_cur = s_next;
+        }
+        const int n = band0 * 16 + row;
+        if (ok && row_ok && n < p.N) {
+            const int t0 = tok0 + 64 * half;
+            if (p.part == nullptr) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    if (t0 + i < p.M) p.y[(size_t)(t0 + i) * p.N + n] = __half_as_ushort(__float2half_rn(acc[i]));
+            } else {
+                float* dst = p.part + (size_t)split * p.M * p.N;
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    if (t0 + i < p.M) dst[(size_t)(t0 + i) * p.N + n] = acc[i];
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Fixed-order sum of the split-K partials: y = fp16(sum_s part[s]).
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, int splits, size_t count,
+                                                            uint16_t* __restrict__ y) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count; i += (size_t)gridDim.x * blockDim.x) {
+        float s = 0.f;
+        for (int k = 0; k < splits; ++k) s += part[(size_t)k * count + i];
+        y[i] = __half_as_ushort(__float2half_rn(s));
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+int gemm_splits(int M, int64_t N, int64_t K) {
+    const int64_t tiles = ((N + kBM - 1) / kBM) * ((M + kBN - 1) / kBN);
+    const int G = (int)(K / kGroupK);
+    if (tiles >= 120 || G < 64) return 1;
+    // smallest waves-per-split among 1..8 splits with >= 16 groups each
+    int best = 1;
+    double best_t = 1e30;
+    for (int s = 1; s <= 8 && G / s >= 16; ++s) {
+        const double t = (double)((tiles * s + 151) / 152) / s + 0.02 * (s > 1);
+        if (t < best_t - 1e-9) {
+            best_t = t;
+            best = s;
+        }
+    }
+    return best;
+}
+
+size_t gemm_workspace(int M, int64_t N, int64_t K) {
+    const int s = gemm_splits(M, N, K);
+    return kStatusBytes + (s > 1 ? (size_t)s * M * N * sizeof(float) : 0);
+}
+
+}  // namespace
+
+w4_status launch_gemm_tc(const void* x, const w4_weight* w, void* y, int M, void* ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+    const size_t need = gemm_workspace(M, w->N, w->K);
+    if (!ws || ws_bytes < need) {
+        set_error("workspace of %zu bytes needed (got %zu)", need, ws_bytes);
+        return W4_ERR_WORKSPACE;
+    }
+    if (!aligned16(ws)) {
+        set_error("workspace not 16-byte aligned");
+        return W4_ERR_ALIGN;
+    }
+    if (w->N > 0x7FFFFFF0 || w->K > 0x7FFFFFF0 || (int64_t)M * w->N > ((int64_t)1 << 40)) {
+        set_error("shape too large");
+        return W4_ERR_SHAPE;
+    }
+    auto encode = tensor_map_encoder();
+    if (!encode) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return W4_ERR_UNSUPPORTED;
+    }
+    CUtensorMap map;
+    const cuuint64_t gdim[2] = {(cuuint64_t)w->K, (cuuint64_t)M};
+    const cuuint64_t gstride[1] = {(cuuint64_t)w->K * 2};
+    const cuuint32_t box[2] = {64, kBN};
+    const cuuint32_t estride[2] = {1, 1};
+    CUresult cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), gdim, gstride, box, estride,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed (%d)", (int)cr);
+        return W4_ERR_CUDA;
+    }
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(prefill)");
+
+    GemmParams p;
+    p.w = static_cast<const uint8_t*>(w->data);
+    p.y = static_cast<uint16_t*>(y);
+    p.status = static_cast<int*>(ws);
+    p.M = M;
+    p.N = (int)w->N;
+    p.K = (int)w->K;
+    p.G = (int)num_groups(w->K);
+    p.bands = (int)num_bands(w->N);
+    p.splits = gemm_splits(M, w->N, w->K);
+    p.part = p.splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(ws) + kStatusBytes) : nullptr;
+
+    W4_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(int), stream));
+    const dim3 grid((unsigned)((M + kBN - 1) / kBN), (unsigned)((p.N + kBM - 1) / kBM), (unsigned)p.splits);
+    gemm_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map, p);
+    W4_CUDA_TRY(cudaGetLastError());
+    if (p.splits > 1) {
+        const size_t count = (size_t)M * p.N;
+        size_t blocks = (count + 255) / 256;
+        if (blocks > 152 * 16) blocks = 152 * 16;
+        splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p.part, p.splits, count, p.y);
+        W4_CUDA_TRY(cudaGetLastError());
+    }
+    return W4_OK;
+}
+
 }  // namespace w4
 
 using namespace w4;
 
+extern "C" size_t w4_workspace_bytes(int M, int64_t N, int64_t K) {
+    if (M <= 16 || N < 1 || K < kGroupK || K % kGroupK != 0) return 0;
+    return gemm_workspace(M, N, K);
+}
+
 extern "C" w4_status w4a16_gemm(const void* x, const w4_weight* w, void* y, int M, void* workspace,
                                 size_t workspace_bytes, void* stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     clear_error();
     if (M < 1) {
         set_error("M=%d: need M >= 1", M);
         return W4_ERR_SHAPE;
     }
-    const int first = M < 16 ? M : 16;
-    w4_status st = check_gemv_args(x, w, y, first);
+    w4_status st = check_gemv_args(x, w, y, M < 16 ? M : 16);
     if (st != W4_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    for (int m0 = 0; m0 < M; m0 += 16) {
-        const int mc = (M - m0) < 16 ? (M - m0) : 16;
-        const char* xs = static_cast<const char*>(x) + (size_t)m0 * w->K * 2;
-        char* ys = static_cast<char*>(y) + (size_t)m0 * w->N * 2;
-        // slices after the first start at row m0 of x and y: 16-byte aligned
-        // whenever K and N are multiples of 8 (always true for K)
-        if (!aligned16(ys)) {
-            set_error("y row %d is not 16-byte aligned (N=%lld)", m0, (long long)w->N);
-            return W4_ERR_ALIGN;
-        }
+    if (M <= 16) {
         w4_gemv_config c;
-        default_gemv_config(mc, w->N, w->K, &c);
-        st = launch_gemv(xs, w, ys, mc, c, s);
-        if (st != W4_OK) return st;
+        default_gemv_config(M, w->N, w->K, &c);
+        return launch_gemv(x, w, y, M, c, s);
     }
-    return W4_OK;
+    return launch_gemm_tc(x, w, y, M, workspace, workspace_bytes, s);
 }
