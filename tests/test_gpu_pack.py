@@ -33,7 +33,7 @@ def test_device_generator_matches_host_generator(N, K):
     assert np.array_equal(host(s), synth.scale_full(ss, N, G))
 
 
-@pytest.mark.parametrize("N,K,seed", [(16, 128, 0), (37, 384, 1), (1000, 1280, 2), (3584, 18944 // 8, 3)])
+@pytest.mark.parametrize("N,K,seed", [(16, 128, 0), (37, 384, 1), (1000, 1280, 2), (3584, 2432, 3)])
 def test_device_pack_is_bit_exact(N, K, seed):
     rng = np.random.default_rng(seed)
     q = rng.integers(-8, 8, (N, K)).astype(np.int8)
