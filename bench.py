@@ -156,7 +156,7 @@ def time_replays(torch, fn, reps: int) -> float:
 
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
-    for name in ("gemv.cu", "w4_internal.cuh"):
+    for name in ("gemv.cu", "w4_internal.cuh", "w4_device.cuh", "tc_ptx.cuh"):
         with open(os.path.join(ROOT, "int4_weight_only_pack_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -238,6 +238,37 @@ def cpu_baseline(oracle, synth, budget_s: float = 12.0):
                       "(%d weight+scale bytes each), FP64 C oracle over %d threads" % (n, nbytes, cores)}
 
 
+def run_one_projection(args):
+    """One projection of layer 0 at M = 1, launched --warmup + --steps times
+    back to back (a profiler target; weights larger than L2 only for gate_up
+    and down, so the printed rate of the others is L2-assisted)."""
+    import torch
+    import int4_weight_only_pack_gb300 as w4
+    from int4_weight_only_pack_gb300 import build as w4build
+    import synth
+    w4build.build()
+    synth.build_device()
+    pid = [n for n, _, _ in LAYER].index(args.profile_projection)
+    _, N, K = LAYER[pid]
+    G = K // 128
+    q = torch.empty((N, K), dtype=torch.int8, device="cuda")
+    s = torch.empty((N, G), dtype=torch.int16, device="cuda")
+    synth.q_device(synth.seed_of(CONFIG_ID, 0, pid, synth.T_Q), N, K, q)
+    synth.scale_device(synth.seed_of(CONFIG_ID, 0, pid, synth.T_SCALE), N, G, s)
+    packed = torch.empty(w4.w4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
+    w = w4.w4_pack(q, s, N, K, packed)
+    del q, s
+    x = torch.from_numpy(synth.x_full(synth.seed_of(CONFIG_ID, 0, pid, synth.T_X), 1, K).view(np.int16)).cuda()
+    y = torch.zeros((1, N), dtype=torch.int16, device="cuda")
+    for _ in range(args.warmup):
+        w4.w4a16_gemv(x, w, y, 1)
+    ms = time_replays(torch, lambda: w4.w4a16_gemv(x, w, y, 1), args.steps)
+    nb = w4.w4_packed_bytes(N, K)
+    print(json.dumps({"projection": args.profile_projection, "N": N, "K": K, "launches": args.steps,
+                      "us_per_launch": ms * 1e3, "GB/s": nb / (ms * 1e-3) / 1e9}), flush=True)
+    return 0
+
+
 # ---- main ------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
@@ -245,12 +276,18 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--no-extras", action="store_true", help="skip the side measurements")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time the step only (no clock soak, e2e, side measurements or CPU baseline): for profilers")
+    ap.add_argument("--profile-projection", choices=[n for n, _, _ in LAYER], default=None,
+                    help="launch one projection of layer 0 (M=1, library launch shape) --steps times: a small "
+                         "case for a profiler")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_projection:
+        return run_one_projection(args)
 
     import torch
     rank, world, local = rank_info()
@@ -280,10 +317,11 @@ def main():
         torch.cuda.synchronize()
 
     # soak ~1.5 s so that the clock record sees the GPU under this load
-    sampler = ClockSampler(local)
-    soak = max(1, int(1.5 / max(time_replays(torch, seq.replay, 20) * 1e-3, 1e-5)))
-    for _ in range(soak):
-        seq.replay()
+    sampler = ClockSampler(local) if not args.no_extras else None
+    if not args.no_extras:
+        soak = max(1, int(1.5 / max(time_replays(torch, seq.replay, 20) * 1e-3, 1e-5)))
+        for _ in range(soak):
+            seq.replay()
     barrier()
     s = torch.cuda.current_stream()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -292,7 +330,7 @@ def main():
         seq.replay()
     ev1.record(s)
     barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop() if sampler else None
     ms = ev0.elapsed_time(ev1) / args.steps
     if world > 1:
         t = torch.tensor([ms], device="cuda")
@@ -303,21 +341,23 @@ def main():
     launches = seq.kernels()
 
     # e2e through the C ABI with host buffers: pinned x in, replay, y out, sync
-    x_pin = torch.from_numpy(st["x_host"]).pin_memory()
-    y_pin = torch.empty(st["y_arena"].numel(), dtype=torch.int16).pin_memory()
     xb, yb = st["x_arena"].numel() * 2, st["y_arena"].numel() * 2
-    for _ in range(3):
-        seq.run_host(x_pin, st["x_arena"], xb, st["y_arena"], y_pin, yb, s)
-    e2e_steps = max(10, min(args.steps, 500))
-    barrier()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        seq.run_host(x_pin, st["x_arena"], xb, st["y_arena"], y_pin, yb, s)
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = None
+    if not args.no_extras:
+        x_pin = torch.from_numpy(st["x_host"]).pin_memory()
+        y_pin = torch.empty(st["y_arena"].numel(), dtype=torch.int16).pin_memory()
+        for _ in range(3):
+            seq.run_host(x_pin, st["x_arena"], xb, st["y_arena"], y_pin, yb, s)
+        e2e_steps = max(10, min(args.steps, 500))
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            seq.run_host(x_pin, st["x_arena"], xb, st["y_arena"], y_pin, yb, s)
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_s], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
 
     extras = {}
     if not args.no_extras:
@@ -352,7 +392,7 @@ def main():
         roof["traffic"] = roof["traffic"]
 
     cpu = None
-    if rank == 0:
+    if rank == 0 and not args.no_extras:
         import oracle
         cpu = cpu_baseline(oracle, synth)
 
@@ -367,9 +407,10 @@ def main():
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "roofline": roof,
                 "cpu_baseline": cpu,
-                "e2e": {"value": world * BYTES_PER_STEP / e2e_s / 1e9, "unit": "GB/s",
-                        "us_per_step": e2e_s * 1e6, "h2d_bytes_per_step": xb, "d2h_bytes_per_step": yb,
-                        "via": "w4_decode_seq_run_host (pinned host x -> device, replay, device y -> pinned host, sync)"},
+                "e2e": None if e2e_s is None else {
+                    "value": world * BYTES_PER_STEP / e2e_s / 1e9, "unit": "GB/s",
+                    "us_per_step": e2e_s * 1e6, "h2d_bytes_per_step": xb, "d2h_bytes_per_step": yb,
+                    "via": "w4_decode_seq_run_host (pinned host x -> device, replay, device y -> pinned host, sync)"},
                 "gpu_launches": launches * args.steps,
                 "clocks": clocks,
                 "target_us_per_step": 550.0,

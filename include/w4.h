@@ -156,11 +156,14 @@ w4_status w4a16_gemv(const void* x, const w4_weight* w, void* y, int M,
                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* Launch shape of the decode kernel, for tuning sweeps.  Zero fields take
- * the library's choice. */
+ * the library's choice.  The kernel is persistent: one CTA per SM (a cluster
+ * of `splits` CTAs per K split), each walking blocks of `bands_per_cta`
+ * 16-row bands and streaming their tiles through a shared-memory ring of
+ * `depth` slots. */
 typedef struct {
-    int bands_per_cta; /* 16-row bands per CTA: 1, 2 or 4 */
-    int splits;        /* K splits = CTAs per cluster: 1..8 */
-    int depth;         /* groups in flight per warp: 1..4 (1, 2, 4) */
+    int bands_per_cta; /* 16-row bands per work block: 1, 2 or 4 */
+    int splits;        /* K splits = CTAs per cluster: 1..8 (at most K/128) */
+    int depth;         /* ring slots (tiles in flight per CTA): 2..96 */
     int pdl;           /* 1: programmatic dependent launch (default), 0: off, -1: default */
 } w4_gemv_config;
 

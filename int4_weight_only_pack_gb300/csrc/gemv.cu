@@ -6,48 +6,85 @@
 // and "The INT8 vs. FP16 Activation Trade-off", Path B).  The pages' own kernel
 // is an sm_90 GEMV with prmt-based unpacking; this one is designed for GB300:
 //
-//  * HBM-bound: every packed byte is read exactly once with 16-byte
-//    non-coherent streaming loads (ld.global.nc.L1::no_allocate), and all of a
-//    warp's first `D` tile groups are requested before the kernel waits on the
-//    previous grid (programmatic dependent launch), so the weight stream of
-//    consecutive projections overlaps.
-//  * Unpacking: one 32-bit word per lane and k16-step holds eight nibbles; two
-//    LOP3 masks with the fp16 exponent pattern 0x6400 (and the same after a
-//    shift by 8) give 1024 + u and 1024 + 16u, and one f16x2 subtract or FMA
-//    turns them into q exactly.  The four registers are an m16n8k16 A fragment.
+//  * HBM-bound streaming.  One persistent CTA per SM (a cluster of `splits`
+//    CTAs when K is split).  Its producer lane streams the CTA's packed tiles,
+//    in order, into a ring of shared-memory slots with 1-D bulk copies
+//    (cp.async.bulk, one 1056-byte tile per slot, completion on the slot's
+//    mbarrier).  The producer starts before the kernel waits on the previous
+//    grid (programmatic dependent launch), so a projection's weights are in
+//    flight while its predecessor drains; every CTA lets its dependents launch
+//    at once, so the next projection's CTAs can do the same.
+//  * Eight consumer warps take the ring's tiles round-robin.  Unpacking: one
+//    32-bit word per lane and k16 step holds eight nibbles; two LOP3 masks
+//    with the fp16 exponent pattern 0x6400 (and the same after a shift by 8)
+//    give 1024 + u and 1024 + 16u, and one f16x2 subtract or FMA turns them
+//    into q exactly: an m16n8k16 A fragment.
 //  * MACs: mma.sync m16n8k16 (FP16 x FP16 products are exact, FP32
-//    accumulation) per 128-wide group; the group's FP32 partial is then scaled
-//    by the group's FP16 scale and added in FP32.  x is the B operand, tokens
-//    padded to 8 (NT = 1) or 16 (NT = 2).
-//  * x is staged once per CTA in shared memory in fragment order (four 16-byte
-//    LDS per lane per group, conflict-free).
-//  * Reductions: fixed-order sums over the CTA's 8 warps in shared memory; when
-//    K is split across a thread-block cluster, fixed-order sums over the
-//    cluster's CTAs through distributed shared memory.  No atomics, no global
-//    scratch: results are bit-identical run to run.
-#include <cooperative_groups.h>
+//    accumulation) per 128-wide group; the group's FP32 partial is scaled by
+//    the group's FP32 scale and added in FP32.  x is the B operand (tokens
+//    padded to 8 or 16), staged once per CTA in shared memory in fragment
+//    order after the wait on the previous grid.
+//  * Work unit: a block of `bands_per_cta` 16-row bands over the CTA's K range.
+//    Per block, the warps' partials are summed in fixed order in shared
+//    memory; with a K split, every non-leader CTA of the cluster stores its
+//    block partial into the leader's shared memory and arrives on the leader's
+//    mbarrier, and the leader adds them in rank order.  No atomics, no global
+//    scratch: bit-identical results run to run.
+//  * Every wait is bounded (about a second); a timeout writes NaN into the
+//    block's outputs instead of hanging.
 #include <cuda_fp16.h>
 
 #include <mutex>
 #include <set>
 #include <utility>
 
+#include "tc_ptx.cuh"
 #include "w4_device.cuh"
 #include "w4_internal.cuh"
 
-namespace cg = cooperative_groups;
-
 namespace w4 {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kMaxSmem = 200 * 1024;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kMaxSmem = 220 * 1024;
+constexpr int kDefaultRing = 48;
+constexpr int kMaxRing = 96;
+
+// SM count of the current device (looked up once per device).
+static int sm_count() {
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 152;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
 
 struct GemvParams {
     const uint32_t* x;  // fp16 pairs, [M, K/2]
     const uint8_t* w;   // packed tiles
     uint16_t* y;        // fp16 [M, N]
     int M, N, K, G, bands;
+    int nblocks;        // ceil(bands / BB)
+    int ring;           // ring slots
+};
+
+// Shared-memory carve-up, identical on host and device.
+struct SmemLayout {
+    int bar, x, red, cpart, total;
+    __host__ __device__ SmemLayout(int ring, int M, int gpc, int BB, int NT, int S) {
+        bar = ring * kTileBytes;                                        // ring of tile slots first
+        x = (bar + (2 * ring + 4) * 8 + 15) & ~15;                      // full/empty per slot, cfull[2], cempty[2]
+        red = x + M * gpc * 256;                                        // x slice in fragment order
+        cpart = red + 2 * kConsumerWarps * BB * NT * 4 * 32 * 4;        // per-warp block partials, 2 buffers
+        total = cpart + 2 * (S > 1 ? S - 1 : 0) * BB * 16 * M * 4;      // leader's receive buffers
+    }
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -57,90 +94,126 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Shared memory: x slice in fragment order, then the per-warp partials, then
-// the CTA partial read by the cluster.
-__host__ __device__ inline int smem_x_bytes(int M, int gpc) { return M * gpc * 256; }
-__host__ __device__ inline int smem_red_bytes(int BB, int NT) { return kWarps * BB * NT * 4 * 32 * 4; }
-__host__ __device__ inline int smem_part_bytes(int BB, int M) { return BB * 16 * M * 4; }
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
 
-template <int NT, int BB, int D>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
-    extern __shared__ __align__(16) uint8_t smem[];
+template <int NT, int BB>
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(GemvParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int S = gridDim.y, rank = blockIdx.y;  // cluster (1, S, 1): rank = K split
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int S = gridDim.y, split = blockIdx.y;
-    const int g_lo = (int)(((long long)p.G * split) / S);
-    const int g_hi = (int)(((long long)p.G * (split + 1)) / S);
-    const int ng = g_hi - g_lo;
+    const int g_lo = (int)(((long long)p.G * rank) / S);
+    const int g_hi = (int)(((long long)p.G * (rank + 1)) / S);
+    const int Gs = g_hi - g_lo;
     const int gpc = (p.G + S - 1) / S;
-    const int my_n = (ng - warp + kWarps - 1) / kWarps;  // my groups: warp, warp + 8, ...
-    const int band0 = blockIdx.x * BB;
-    const int M = p.M;
+    const int M = p.M, ring = p.ring;
+    const SmemLayout L(ring, M, gpc, BB, NT, S);
+    const uint32_t sbase = tc::smem_addr(smem);
+    const uint32_t full0 = sbase + L.bar, empty0 = full0 + 8 * ring, cfull0 = empty0 + 8 * ring,
+                   cempty0 = cfull0 + 16;
 
-    const uint8_t* tile0[BB];
-    bool bvalid[BB];
-#pragma unroll
-    for (int bb = 0; bb < BB; ++bb) {
-        bvalid[bb] = band0 + bb < p.bands;
-        tile0[bb] = p.w + ((size_t)(band0 + bb) * p.G + g_lo + warp) * kTileBytes;
-    }
-    const size_t step = (size_t)kWarps * kTileBytes;
-
-    uint4 wlo[D][BB], whi[D][BB];
-    uint32_t wsc[D][BB];
-#pragma unroll
-    for (int d = 0; d < D; ++d) {
-#pragma unroll
-        for (int bb = 0; bb < BB; ++bb) {
-            wlo[d][bb] = make_uint4(0, 0, 0, 0);
-            whi[d][bb] = make_uint4(0, 0, 0, 0);
-            wsc[d][bb] = 0;
-            if (d < my_n && bvalid[bb]) {
-                const uint8_t* t = tile0[bb] + d * step;
-                wlo[d][bb] = ld_stream16(t + 16 * lane);
-                whi[d][bb] = ld_stream16(t + 512 + 16 * lane);
-                wsc[d][bb] = ld_stream4(t + kScaleOffset + 4 * (lane >> 2));
-            }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ring; ++s) {
+            tc::mbar_init(full0 + 8 * s, 1);
+            tc::mbar_init(empty0 + 8 * s, 1);
         }
-    }
-
-    // x may be produced by the previous kernel on the stream: read it only now.
-    pdl_wait();
-    pdl_launch_dependents();
-
-    uint32_t* xs = reinterpret_cast<uint32_t*>(smem);
-    {
-        const int per_row = ng * 64;  // fp16 pairs of this split's K range
-        const uint32_t* xg = p.x + (size_t)g_lo * 64;
-        const int kp = p.K / 2;
-        for (int idx = threadIdx.x; idx < M * per_row; idx += kThreads) {
-            const int m = idx / per_row, r = idx - m * per_row;
-            const uint32_t v = __ldcg(xg + (size_t)m * kp + r);
-            // pair kk2 of the group = k 2*kk2, 2*kk2+1; lane class c owns
-            // k 4c..4c+3 of each k16 step (the lower pair is b0, the upper b1)
-            const int gl = r >> 6, kk2 = r & 63;
-            const int j = kk2 >> 3, c = (kk2 >> 1) & 3, hi = kk2 & 1;
-            xs[gl * (M * 64) + (j >> 1) * (M * 16) + (m * 4 + c) * 4 + (j & 1) * 2 + hi] = v;
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(cfull0 + 8 * b, S > 1 ? S - 1 : 1);
+            tc::mbar_init(cempty0 + 8 * b, 1);
         }
+        tc::mbar_init_fence();
     }
     __syncthreads();
+    if (S > 1) tc::cluster_sync_all();  // every CTA's barriers exist before any remote access
+    // The next kernel on the stream may start now: it only streams its own
+    // weights until it, too, waits for this grid to finish.
+    pdl_launch_dependents();
 
-    float acc[BB][NT][4];
-#pragma unroll
-    for (int bb = 0; bb < BB; ++bb)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) acc[bb][nt][r] = 0.f;
+    const int P = gridDim.x;
+    if (warp == kConsumerWarps) {
+        // ---- producer: stream this CTA's tiles into the ring ------------------
+        if (lane == 0) {
+            int seq = 0;
+            bool ok = true;
+            for (int blk = blockIdx.x; blk < p.nblocks && ok; blk += P) {
+                const int band0 = blk * BB;
+                const int T = min(BB, p.bands - band0) * Gs;
+                for (int t = 0; t < T; ++t, ++seq) {
+                    const int slot = seq % ring, use = seq / ring;
+                    if (use > 0 && !tc::mbar_wait(empty0 + 8 * slot, (use - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const int bb = t / Gs, g = g_lo + (t - bb * Gs);
+                    const uint8_t* src = p.w + ((size_t)(band0 + bb) * p.G + g) * kTileBytes;
+                    tc::mbar_arrive_expect_tx(full0 + 8 * slot, kTileBytes);
+                    tc::bulk_load(sbase + slot * kTileBytes, src, kTileBytes, full0 + 8 * slot);
+                }
+            }
+            // every copy has landed before the CTA may exit
+            for (int sq = seq - 1; sq >= 0 && sq >= seq - ring; --sq)
+                tc::mbar_wait(full0 + 8 * (sq % ring), (sq / ring) & 1);
+        }
+        __syncwarp();
+    } else {
+        // ---- consumers -----------------------------------------------------------
+        // x may be produced by the previous kernel on the stream: read it only now.
+        pdl_wait();
+        uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L.x);
+        {
+            const int per_row = Gs * 64;  // fp16 pairs of this split's K range
+            const uint32_t* xg = p.x + (size_t)g_lo * 64;
+            const int kp = p.K / 2;
+            for (int idx = threadIdx.x; idx < M * per_row; idx += kConsumers) {
+                const int m = idx / per_row, r = idx - m * per_row;
+                const uint32_t v = __ldcg(xg + (size_t)m * kp + r);
+                // pair kk2 of the group = k 2*kk2, 2*kk2+1; lane class c owns
+                // k 4c..4c+3 of each k16 step (the lower pair is b0, the upper b1)
+                const int gl = r >> 6, kk2 = r & 63;
+                const int j = kk2 >> 3, c = (kk2 >> 1) & 3, hi = kk2 & 1;
+                xs[gl * (M * 64) + (j >> 1) * (M * 16) + (m * 4 + c) * 4 + (j & 1) * 2 + hi] = v;
+            }
+        }
+        tc::named_barrier(1, kConsumers);
 
-    const uint4* xs4 = reinterpret_cast<const uint4*>(smem);
-    const int tok = lane >> 2, cl4 = lane & 3;
-
-    for (int i0 = 0; i0 < my_n; i0 += D) {
+        const uint4* xs4 = reinterpret_cast<const uint4*>(smem + L.x);
+        const int tok = lane >> 2, cl4 = lane & 3;
+        float* red_base = reinterpret_cast<float*>(smem + L.red);
+        const int red_buf = kConsumerWarps * BB * NT * 4 * 32;
+        const int part_buf = (S > 1 ? S - 1 : 0) * BB * 16 * M;
+        int seq = 0, kblk = 0;
+        for (int blk = blockIdx.x; blk < p.nblocks; blk += P, ++kblk) {
+            const int band0 = blk * BB;
+            const int nb = min(BB, p.bands - band0);
+            const int T = nb * Gs;
+            bool ok = true;
+            float acc[BB][NT][4];
 #pragma unroll
-        for (int d = 0; d < D; ++d) {
-            const int i = i0 + d;
-            if (i < my_n) {
-                const int gl = warp + kWarps * i;
+            for (int bb = 0; bb < BB; ++bb)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) acc[bb][nt][r] = 0.f;
+
+            for (int t = warp; t < T; t += kConsumerWarps) {
+                const int sq = seq + t;
+                const int slot = sq % ring;
+                if (!tc::mbar_wait(full0 + 8 * slot, (sq / ring) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t ta = sbase + slot * kTileBytes;
+                const uint4 lo = lds128(ta + 16 * lane), hi = lds128(ta + 512 + 16 * lane);
+                const uint32_t sc = lds32(ta + kScaleOffset + 4 * (lane >> 2));
+                const int bb = t / Gs, gl = t - bb * Gs;
                 uint4 xb[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
@@ -149,132 +222,159 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
                     for (int q = 0; q < 4; ++q)
                         xb[nt][q] = (m < M) ? xs4[gl * (M * 16) + q * (M * 4) + m * 4 + cl4] : make_uint4(0, 0, 0, 0);
                 }
+                float part[NT][4];
 #pragma unroll
-                for (int bb = 0; bb < BB; ++bb) {
-                    float part[NT][4];
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
+                    for (int r = 0; r < 4; ++r) part[nt][r] = 0.f;
+                const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) part[nt][r] = 0.f;
-                    const uint32_t wd[8] = {wlo[d][bb].x, wlo[d][bb].y, wlo[d][bb].z, wlo[d][bb].w,
-                                            whi[d][bb].x, whi[d][bb].y, whi[d][bb].z, whi[d][bb].w};
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        uint32_t a[4];
-                        unpack_word(wd[j], a);
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const uint4& v = xb[nt][j >> 1];
-                            mma16816(part[nt], a, (j & 1) ? v.z : v.x, (j & 1) ? v.w : v.y);
-                        }
-                    }
-                    const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&wsc[d][bb]));
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t a[4];
+                    unpack_word(wd[j], a);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        acc[bb][nt][0] = fmaf(sf.x, part[nt][0], acc[bb][nt][0]);
-                        acc[bb][nt][1] = fmaf(sf.x, part[nt][1], acc[bb][nt][1]);
-                        acc[bb][nt][2] = fmaf(sf.y, part[nt][2], acc[bb][nt][2]);
-                        acc[bb][nt][3] = fmaf(sf.y, part[nt][3], acc[bb][nt][3]);
+                        const uint4& v = xb[nt][j >> 1];
+                        mma16816(part[nt], a, (j & 1) ? v.z : v.x, (j & 1) ? v.w : v.y);
                     }
                 }
-                if (i + D < my_n) {
+                // the tile's words are consumed: hand the slot back
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(empty0 + 8 * slot);
+                const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sc));
 #pragma unroll
-                    for (int bb = 0; bb < BB; ++bb) {
-                        if (bvalid[bb]) {
-                            const uint8_t* t = tile0[bb] + (size_t)(i + D) * step;
-                            wlo[d][bb] = ld_stream16(t + 16 * lane);
-                            whi[d][bb] = ld_stream16(t + 512 + 16 * lane);
-                            wsc[d][bb] = ld_stream4(t + kScaleOffset + 4 * (lane >> 2));
+                for (int b2 = 0; b2 < BB; ++b2) {
+                    if (b2 == bb) {
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            acc[b2][nt][0] = fmaf(sf.x, part[nt][0], acc[b2][nt][0]);
+                            acc[b2][nt][1] = fmaf(sf.x, part[nt][1], acc[b2][nt][1]);
+                            acc[b2][nt][2] = fmaf(sf.y, part[nt][2], acc[b2][nt][2]);
+                            acc[b2][nt][3] = fmaf(sf.y, part[nt][3], acc[b2][nt][3]);
                         }
                     }
                 }
             }
+            seq += T;
+
+            // ---- fixed-order reduction of the block over the warps --------------
+            float* red = red_base + (kblk & 1) * red_buf;
+#pragma unroll
+            for (int bb = 0; bb < BB; ++bb)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        red[(((warp * BB + bb) * NT + nt) * 4 + r) * 32 + lane] = ok ? acc[bb][nt][r] : __int_as_float(0x7FC00000);
+            tc::named_barrier(1, kConsumers);
+            const int Tout = nb * 16 * M;  // outputs of this block: [m][band row]
+            float v[4];                    // <= 4 outputs per thread (BB * 16 * 16 <= 1024)
+            int cnt = 0;
+            for (int t = threadIdx.x; t < Tout; t += kConsumers, ++cnt) {
+                const int m = t / (nb * 16), rl = t - m * (nb * 16);
+                const int bb = rl >> 4, rr = rl & 15;
+                const int nt = m >> 3, col = m & 7;
+                const int ln = (rr & 7) * 4 + (col >> 1), r = (rr >> 3) * 2 + (col & 1);
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) sum += red[(((w * BB + bb) * NT + nt) * 4 + r) * 32 + ln];
+                v[cnt & 3] = sum;
+                if (S == 1) {
+                    const int n = band0 * 16 + rl;
+                    if (n < p.N) p.y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(sum));
+                }
+            }
+            if (S > 1) {
+                const int buf = kblk & 1;
+                const uint32_t use = (uint32_t)(kblk >> 1);
+                float* cpart = reinterpret_cast<float*>(smem + L.cpart) + buf * part_buf;
+                if (rank != 0) {
+                    // wait until the leader has read this buffer's previous contents
+                    bool got = tc::mbar_wait_cluster(cempty0 + 8 * buf, (use & 1) ^ 1);
+                    const uint32_t remote = tc::map_rank(tc::smem_addr(cpart), 0) + (uint32_t)(rank - 1) * BB * 16 * M * 4;
+                    cnt = 0;
+                    for (int t = threadIdx.x; t < Tout; t += kConsumers, ++cnt)
+                        tc::st_cluster_f32(remote + 4u * t, got ? v[cnt & 3] : __int_as_float(0x7FC00000));
+                    tc::fence_acq_rel_cluster();
+                    tc::named_barrier(1, kConsumers);
+                    if (threadIdx.x == 0) tc::mbar_arrive_remote(tc::map_rank(cfull0 + 8 * buf, 0));
+                } else {
+                    const bool got = tc::mbar_wait_cluster(cfull0 + 8 * buf, use & 1);
+                    cnt = 0;
+                    for (int t = threadIdx.x; t < Tout; t += kConsumers, ++cnt) {
+                        float sum = v[cnt & 3];
+                        for (int r2 = 1; r2 < S; ++r2) sum += cpart[(r2 - 1) * BB * 16 * M + t];
+                        if (!got) sum = __int_as_float(0x7FC00000);
+                        const int m = t / (nb * 16), rl = t - m * (nb * 16);
+                        const int n = band0 * 16 + rl;
+                        if (n < p.N) p.y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(sum));
+                    }
+                    tc::named_barrier(1, kConsumers);
+                    if (threadIdx.x == 0)
+                        for (int r2 = 1; r2 < S; ++r2) tc::mbar_arrive_remote(tc::map_rank(cempty0 + 8 * buf, r2));
+                }
+            }
         }
     }
-
-    // ---- fixed-order reduction over the CTA's warps -------------------------
-    float* red = reinterpret_cast<float*>(smem + smem_x_bytes(M, gpc));
-#pragma unroll
-    for (int bb = 0; bb < BB; ++bb)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) red[(((warp * BB + bb) * NT + nt) * 4 + r) * 32 + lane] = acc[bb][nt][r];
-    __syncthreads();
-
-    const int T = BB * 16 * M;  // outputs of this CTA: [m][band row]
-    float* cta_part = red + kWarps * BB * NT * 4 * 32;
-    for (int t = threadIdx.x; t < T; t += kThreads) {
-        const int m = t / (BB * 16), rl = t - m * (BB * 16);
-        const int bb = rl >> 4, rr = rl & 15;
-        const int nt = m >> 3, col = m & 7;
-        const int ln = (rr & 7) * 4 + (col >> 1), r = (rr >> 3) * 2 + (col & 1);
-        float sum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) sum += red[(((w * BB + bb) * NT + nt) * 4 + r) * 32 + ln];
-        if (S == 1) {
-            const int n = (band0 + bb) * 16 + rr;
-            if (n < p.N) p.y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(sum));
-        } else {
-            cta_part[t] = sum;
-        }
-    }
-
-    // ---- fixed-order reduction over the cluster's K splits (DSMEM) ----------
-    if (S > 1) {
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
-        const int rank = (int)cluster.block_rank();
-        const int t0 = T * rank / S, t1 = T * (rank + 1) / S;
-        for (int t = t0 + threadIdx.x; t < t1; t += kThreads) {
-            float sum = 0.f;
-            for (int s = 0; s < S; ++s) sum += cluster.map_shared_rank(cta_part, s)[t];
-            const int m = t / (BB * 16), rl = t - m * (BB * 16);
-            const int n = (band0 + (rl >> 4)) * 16 + (rl & 15);
-            if (n < p.N) p.y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(sum));
-        }
-        cluster.sync();  // keep this CTA's shared memory alive until every rank has read it
-    }
+    // leave no remote access pending: the leader's last arrivals land before
+    // any CTA of the cluster exits
+    if (S > 1) tc::cluster_sync_all();
 }
 
 // ---- host side -------------------------------------------------------------
 using KernelFn = void (*)(GemvParams);
 
-template <int NT, int BB, int D>
+template <int NT, int BB>
 static KernelFn kernel_ptr() {
-    return gemv_kernel<NT, BB, D>;
+    return gemv_kernel<NT, BB>;
 }
 
-static KernelFn pick_kernel(int NT, int BB, int D) {
-#define W4_CASE(nt, bb, d) \
-    if (NT == nt && BB == bb && D == d) return kernel_ptr<nt, bb, d>();
-    W4_CASE(1, 1, 1) W4_CASE(1, 1, 2) W4_CASE(1, 1, 4)
-    W4_CASE(1, 2, 1) W4_CASE(1, 2, 2) W4_CASE(1, 2, 4)
-    W4_CASE(1, 4, 1) W4_CASE(1, 4, 2)
-    W4_CASE(2, 1, 1) W4_CASE(2, 1, 2) W4_CASE(2, 1, 4)
-    W4_CASE(2, 2, 1) W4_CASE(2, 2, 2)
-    W4_CASE(2, 4, 1)
-#undef W4_CASE
+static KernelFn pick_kernel(int NT, int BB) {
+    if (NT == 1 && BB == 1) return kernel_ptr<1, 1>();
+    if (NT == 1 && BB == 2) return kernel_ptr<1, 2>();
+    if (NT == 1 && BB == 4) return kernel_ptr<1, 4>();
+    if (NT == 2 && BB == 1) return kernel_ptr<2, 1>();
+    if (NT == 2 && BB == 2) return kernel_ptr<2, 2>();
+    if (NT == 2 && BB == 4) return kernel_ptr<2, 4>();
     return nullptr;
 }
 
-static int gemv_smem_bytes(int M, int G, int BB, int S) {
+static int gemv_smem_bytes(int M, int G, int BB, int S, int ring) {
     const int NT = M <= 8 ? 1 : 2;
-    const int gpc = (G + S - 1) / S;
-    return smem_x_bytes(M, gpc) + smem_red_bytes(BB, NT) + smem_part_bytes(BB, M);
+    return SmemLayout(ring, M, (G + S - 1) / S, BB, NT, S).total;
+}
+
+// Critical-path tiles per consumer warp of a launch shape (lower is better):
+// waves of blocks over the persistent clusters x tiles per warp per block.
+static double shape_cost(int64_t bands, int G, int BB, int S, int sms) {
+    const int64_t nblocks = (bands + BB - 1) / BB;
+    const int64_t clusters = sms / S;
+    const int64_t P = nblocks < clusters ? nblocks : clusters;
+    const int64_t waves = (nblocks + P - 1) / P;
+    const int Gs = (G + S - 1) / S;
+    return (double)waves * (double)((BB * Gs + kConsumerWarps - 1) / kConsumerWarps) * (S > 1 ? 1.05 : 1.0);
 }
 
 void default_gemv_config(int M, int64_t N, int64_t K, w4_gemv_config* c) {
     const int64_t bands = num_bands(N);
     const int G = (int)num_groups(K);
-    c->bands_per_cta = M <= 2 ? 1 : (M <= 8 ? 2 : 4);
-    c->depth = c->bands_per_cta == 1 ? 4 : (c->bands_per_cta == 2 ? 2 : 1);
-    const int64_t ctas = (bands + c->bands_per_cta - 1) / c->bands_per_cta;
-    int S = 1;
-    while (S < 8 && 2 * S <= G &&
-           (gemv_smem_bytes(M, G, c->bands_per_cta, S) > 64 * 1024 || ctas * S < 228))
-        S *= 2;
-    c->splits = S;
+    const int sms = sm_count();
+    double best = 1e30;
+    c->bands_per_cta = 1;
+    c->splits = 8;
+    for (int S = 1; S <= 8; S *= 2) {
+        if (S > G) break;
+        for (int BB = 1; BB <= 4; BB *= 2) {
+            if (gemv_smem_bytes(M, G, BB, S, kDefaultRing) > 128 * 1024) continue;
+            const double cost = shape_cost(bands, G, BB, S, sms);
+            if (cost < best - 1e-9) {
+                best = cost;
+                c->bands_per_cta = BB;
+                c->splits = S;
+            }
+        }
+    }
+    c->depth = kDefaultRing;
     c->pdl = 1;
 }
 
@@ -290,45 +390,51 @@ static w4_status allow_large_smem(KernelFn fn) {
     std::lock_guard<std::mutex> lock(mu);
     if (done.count({dev, fn})) return W4_OK;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     done.insert({dev, fn});
     return W4_OK;
 }
 
-// Validate a launch shape and prepare its kernel without launching it.
-w4_status prepare_gemv(const w4_weight* w, int M, const w4_gemv_config& c) {
+static w4_status resolve(const w4_weight* w, int M, const w4_gemv_config& c, KernelFn* fn, int* smem) {
     const int NT = M <= 8 ? 1 : 2;
-    KernelFn fn = pick_kernel(NT, c.bands_per_cta, c.depth);
-    if (!fn) return W4_ERR_UNSUPPORTED;
-    const int smem = gemv_smem_bytes(M, (int)num_groups(w->K), c.bands_per_cta, c.splits);
-    if (smem > 48 * 1024 && smem <= kMaxSmem) return allow_large_smem(fn);
-    return W4_OK;
-}
-
-// Launch with an explicit shape; every argument already validated.
-w4_status launch_gemv(const void* x, const w4_weight* w, void* y, int M, const w4_gemv_config& c,
-                      cudaStream_t stream) {
-    const int NT = M <= 8 ? 1 : 2;
-    KernelFn fn = pick_kernel(NT, c.bands_per_cta, c.depth);
-    if (!fn || c.splits < 1 || c.splits > 8 || c.splits > w->K / kGroupK) {
-        set_error("no decode kernel for M=%d bands_per_cta=%d depth=%d splits=%d", M, c.bands_per_cta, c.depth,
-                  c.splits);
+    *fn = pick_kernel(NT, c.bands_per_cta);
+    const int G = (int)num_groups(w->K);
+    if (!*fn || c.splits < 1 || c.splits > 8 || c.splits > G || c.depth < 2 || c.depth > kMaxRing) {
+        set_error("no decode kernel for M=%d bands_per_cta=%d splits=%d depth=%d", M, c.bands_per_cta, c.splits,
+                  c.depth);
         return W4_ERR_UNSUPPORTED;
     }
-    const int G = (int)num_groups(w->K);
-    const int smem = gemv_smem_bytes(M, G, c.bands_per_cta, c.splits);
-    if (smem > kMaxSmem) {
-        set_error("decode kernel needs %d bytes of shared memory (max %d); use more splits", smem, kMaxSmem);
+    *smem = gemv_smem_bytes(M, G, c.bands_per_cta, c.splits, c.depth);
+    if (*smem > kMaxSmem) {
+        set_error("decode kernel needs %d bytes of shared memory (max %d); use more splits", *smem, kMaxSmem);
         return W4_ERR_UNSUPPORTED;
     }
     if (w->N > (int64_t)0x7FFFFFF0 || w->K > (int64_t)0x7FFFFFF0) {
         set_error("N or K too large");
         return W4_ERR_SHAPE;
     }
-    if (smem > 48 * 1024) {
-        w4_status st = allow_large_smem(fn);
-        if (st != W4_OK) return st;
-    }
+    return W4_OK;
+}
+
+// Validate a launch shape and prepare its kernel without launching it.
+w4_status prepare_gemv(const w4_weight* w, int M, const w4_gemv_config& c) {
+    KernelFn fn;
+    int smem;
+    w4_status st = resolve(w, M, c, &fn, &smem);
+    if (st != W4_OK) return st;
+    return allow_large_smem(fn);
+}
+
+// Launch with an explicit shape; every argument already validated.
+w4_status launch_gemv(const void* x, const w4_weight* w, void* y, int M, const w4_gemv_config& c,
+                      cudaStream_t stream) {
+    KernelFn fn;
+    int smem;
+    w4_status st = resolve(w, M, c, &fn, &smem);
+    if (st != W4_OK) return st;
+    st = allow_large_smem(fn);
+    if (st != W4_OK) return st;
     GemvParams p;
     p.x = static_cast<const uint32_t*>(x);
     p.w = static_cast<const uint8_t*>(w->data);
@@ -336,11 +442,15 @@ w4_status launch_gemv(const void* x, const w4_weight* w, void* y, int M, const w
     p.M = M;
     p.N = (int)w->N;
     p.K = (int)w->K;
-    p.G = G;
+    p.G = (int)num_groups(w->K);
     p.bands = (int)num_bands(w->N);
+    p.nblocks = (p.bands + c.bands_per_cta - 1) / c.bands_per_cta;
+    p.ring = c.depth;
+    const int clusters = sm_count() / c.splits;
+    const int P = p.nblocks < clusters ? p.nblocks : clusters;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((p.bands + c.bands_per_cta - 1) / c.bands_per_cta), (unsigned)c.splits, 1);
+    cfg.gridDim = dim3((unsigned)P, (unsigned)c.splits, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;

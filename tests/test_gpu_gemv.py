@@ -47,7 +47,7 @@ def test_parity_default_config(M, N, K):
     assert_close(y, oracle.linear(x, q, s), "M=%d N=%d K=%d" % (M, N, K))
 
 
-CONFIGS = [(bb, sp, d) for bb, d in [(1, 1), (1, 2), (1, 4), (2, 1), (2, 2), (2, 4), (4, 1), (4, 2)]
+CONFIGS = [(bb, sp, d) for bb, d in [(1, 2), (1, 48), (2, 5), (2, 96), (4, 16), (4, 48)]
            for sp in (1, 2, 3, 5, 8)]
 
 
@@ -61,8 +61,19 @@ def test_every_instantiation_and_split_nt1(bb, splits, depth):
     assert_close(run(x, w, N, M, cfg), oracle.linear(x, q, s), "cfg %s" % ((bb, splits, depth),))
 
 
-@pytest.mark.parametrize("bb,splits,depth", [(1, 1, 1), (1, 2, 2), (1, 8, 4), (2, 1, 1), (2, 3, 2),
-                                             (4, 1, 1), (4, 5, 1), (4, 8, 1)])
+def test_unsupported_launch_shapes_are_rejected():
+    rng = np.random.default_rng(1)
+    x, q, s = rand_problem(rng, 1, 32, 256)
+    packed, w = pack_on_device(q, s)
+    for cfg in [w4.GemvConfig(3, 1, 8, 1), w4.GemvConfig(1, 3, 8, 1), w4.GemvConfig(1, 1, 1, 1),
+                w4.GemvConfig(1, 9, 8, 1), w4.GemvConfig(1, 1, 200, 1)]:
+        with pytest.raises(w4.W4Error) as e:
+            run(x, w, 32, 1, cfg)
+        assert e.value.status == 7
+
+
+@pytest.mark.parametrize("bb,splits,depth", [(1, 1, 3), (1, 2, 48), (1, 8, 7), (2, 1, 48), (2, 3, 16),
+                                             (4, 1, 48), (4, 5, 8), (4, 8, 2)])
 def test_every_instantiation_and_split_nt2(bb, splits, depth):
     M, N, K = 14, 72, 2304
     rng = np.random.default_rng(bb * 100 + splits * 10 + depth + 5000)
