@@ -185,6 +185,29 @@ w4_status w4a16_gemv_default_config(int M, int64_t N, int64_t K,
 w4_status w4a16_gemm(const void* x, const w4_weight* w, void* y, int M,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* Prefill projection for callers that cannot allocate device memory.
+ * No passage of the pages corresponds to this entry point: it exists for
+ * callers that cannot call cudaMalloc themselves (for example a plugin whose
+ * host framework owns every device allocation, or code that must not risk the
+ * device synchronisation or the out-of-memory failure an allocation can
+ * bring), and so cannot pass w4a16_gemm a workspace.  It runs the same
+ * kernels with the same results as w4a16_gemm, taking its workspace from a
+ * file-scope device array of W4_STATIC_SCRATCH_BYTES that the library
+ * reserves on every GPU that loads it, until the process exits.  It calls no
+ * allocator.
+ *  - The caller passes x, w and y exactly as for w4a16_gemm.
+ *  - Shapes whose workspace (w4_workspace_bytes) exceeds
+ *    W4_STATIC_SCRATCH_BYTES are rejected with W4_ERR_WORKSPACE before any
+ *    launch; M <= 16 needs no scratch.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the previous
+ *    call's contents (the call clears the status word it relies on).  Calls
+ *    whose kernels overlap on the GPU (other streams, concurrent graphs) race
+ *    on it: serialise them. */
+#define W4_STATIC_SCRATCH_BYTES (4u << 20)
+w4_status w4a16_gemm_static_scratch(const void* x, const w4_weight* w, void* y, int M, void* stream);
+
 /* ------------------------------------------------------------------------
  * Decode step sequence ("Building a Custom LLM Inference Runtime ...",
  * "The Impact of CUDA Graphs": capturing the whole decode step in one CUDA

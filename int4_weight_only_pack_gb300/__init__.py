@@ -60,6 +60,7 @@ _SIGNATURES = {
     "w4a16_gemv_config": (_int, [_vp, ctypes.POINTER(Weight), _vp, _int, ctypes.POINTER(GemvConfig), _vp]),
     "w4a16_gemv_default_config": (_int, [_int, _i64, _i64, ctypes.POINTER(GemvConfig)]),
     "w4a16_gemm": (_int, [_vp, ctypes.POINTER(Weight), _vp, _int, _vp, _sz, _vp]),
+    "w4a16_gemm_static_scratch": (_int, [_vp, ctypes.POINTER(Weight), _vp, _int, _vp]),
     "w4_decode_seq_create": (_int, [ctypes.POINTER(Weight), ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _int,
                                     _int, _vp, ctypes.POINTER(_vp)]),
     "w4_decode_seq_replay": (_int, [_vp, _vp]),
@@ -187,6 +188,14 @@ def w4a16_gemv_default_config(M: int, N: int, K: int) -> GemvConfig:
 def w4a16_gemm(x, w: Weight, y, M: int, workspace=None, workspace_bytes: int = 0, stream=None):
     _check(lib().w4a16_gemm(_addr(x), ctypes.byref(w), _addr(y), M, _addr(workspace), workspace_bytes,
                             _stream(stream)))
+
+
+W4_STATIC_SCRATCH_BYTES = 4 << 20
+
+
+def w4a16_gemm_static_scratch(x, w: Weight, y, M: int, stream=None):
+    """w4a16_gemm without a workspace: the library's static device scratch."""
+    _check(lib().w4a16_gemm_static_scratch(_addr(x), ctypes.byref(w), _addr(y), M, _stream(stream)))
 
 
 class DecodeSeq:

@@ -383,7 +383,75 @@ w4_status launch_gemm_tc(const void* x, const w4_weight* w, void* y, int M, void
 
 }  // namespace w4
 
+// ---- prefill without a caller workspace -------------------------------------
+// Some callers cannot allocate device memory at all (a plugin whose host
+// framework owns every device allocation, or code that must not call
+// cudaMalloc because it can synchronise the device or fail at a memory cap),
+// so they cannot provide the prefill kernel's workspace.  For them the
+// workspace lives in this file-scope array: the CUDA module reserves it on
+// every device that loads the library, for the life of the process.
+namespace w4 {
+namespace {
+
+__device__ __align__(256) unsigned char g_static_scratch[W4_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (with that device current).  In host code the array's name is only a
+// host-side stand-in, never a device address.
+w4_status static_scratch_address(void** out) {
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) {
+        set_error("device ordinal %d out of range", dev);
+        return W4_ERR_UNSUPPORTED;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return W4_OK;
+}
+
+}  // namespace
+}  // namespace w4
+
 using namespace w4;
+
+extern "C" w4_status w4a16_gemm_static_scratch(const void* x, const w4_weight* w, void* y, int M, void* stream) {
+    clear_error();
+    if (M < 1) {
+        set_error("M=%d: need M >= 1", M);
+        return W4_ERR_SHAPE;
+    }
+    w4_status st = check_gemv_args(x, w, y, M < 16 ? M : 16);
+    if (st != W4_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M <= 16) {  // the decode kernel needs no scratch at all
+        w4_gemv_config c;
+        default_gemv_config(M, w->N, w->K, &c);
+        return launch_gemv(x, w, y, M, c, s);
+    }
+    const size_t need = gemm_workspace(M, w->N, w->K);
+    if (need > W4_STATIC_SCRATCH_BYTES) {
+        set_error("M=%d N=%lld K=%lld needs %zu bytes of scratch; the static scratch holds %zu "
+                  "(use w4a16_gemm with a workspace)",
+                  M, (long long)w->N, (long long)w->K, need, (size_t)W4_STATIC_SCRATCH_BYTES);
+        return W4_ERR_WORKSPACE;
+    }
+    void* scratch = nullptr;
+    st = static_scratch_address(&scratch);
+    if (st != W4_OK) return st;
+    return launch_gemm_tc(x, w, y, M, scratch, W4_STATIC_SCRATCH_BYTES, s);
+}
 
 extern "C" size_t w4_workspace_bytes(int M, int64_t N, int64_t K) {
     if (M <= 16 || N < 1 || K < kGroupK || K % kGroupK != 0) return 0;
