@@ -38,7 +38,7 @@ CONFIG_ID = 3  # seed family of the full-decode-step workload
 BYTES_PER_STEP = LAYERS * sum((N * K) // 2 + N * (K // 128) * 2 for _, N, K in LAYER)  # 3,364,601,856
 FALLBACK_HBM_GBS = 6800.0
 WORKLOAD = ("decode step: 28 layers x {qkv 4608x3584, o 3584x3584, gate_up 37888x3584, down 3584x18944} "
-            "W4A16 projections, M=1, one CUDA-graph replay of 112 kernels")
+            "W4A16 projections, M=1, one CUDA-graph replay per step")
 
 
 def rank_info():
@@ -269,6 +269,65 @@ def run_one_projection(args):
     return 0
 
 
+def small_batch_sweep(torch, w4, synth, st, Ms=(2, 4, 8, 16), reps=50):
+    """The full 112-projection step at M tokens (same weights): us/step and
+    weight GB/s; weight bytes are read once per step whatever M."""
+    out = {}
+    for M in Ms:
+        xs, ys, keep = [], [], []
+        for (layer, pid, N, K) in st["meta"]:
+            x = torch.randn((M, K), device="cuda").half().view(torch.int16)
+            y = torch.zeros((M, N), dtype=torch.int16, device="cuda")
+            xs.append(x)
+            ys.append(y)
+        peak = measured_peaks()[0].get("hbm_gbs", FALLBACK_HBM_GBS)
+        entry = {}
+        nbw = w4.w4_decode_seq_workspace_bytes(st["ws"], M)
+        buf = torch.zeros(nbw + 256, dtype=torch.uint8, device="cuda")
+        off = (-buf.data_ptr()) % 256
+        for mode, seq in (("persistent", w4.DecodeSeq(st["ws"], xs, ys, M, workspace=buf[off:off + nbw])),
+                          ("graph_pdl", w4.DecodeSeq(st["ws"], xs, ys, M, use_pdl=True))):
+            for _ in range(3):
+                seq.replay()
+            ms = time_replays(torch, seq.replay, reps)
+            entry[mode] = {"us_per_step": ms * 1e3, "GB/s": BYTES_PER_STEP / (ms * 1e-3) / 1e9,
+                           "frac_of_hbm": BYTES_PER_STEP / (ms * 1e-3) / 1e9 / peak}
+            if mode == "persistent":
+                entry[mode]["status_word"] = seq.status()
+            seq.close()
+        out["M%d" % M] = entry
+        del xs, ys, buf
+    return out
+
+
+def prefill_layer(torch, w4, synth, st, M=512, layers=4, reps=5):
+    """Prefill-shaped projections (M = 512) of the first layers' weights:
+    us per projection and TFLOP/s (2*M*N*K useful flops)."""
+    peaks, _ = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", 1899.7))
+    out = {}
+    for pid, (name, N, K) in enumerate(LAYER):
+        x = torch.from_numpy(synth.x_full(synth.seed_of(5, 0, pid, synth.T_X), M, K).view(np.int16)).cuda()
+        y = torch.zeros((M, N), dtype=torch.int16, device="cuda")
+        nb = w4.w4_workspace_bytes(M, N, K)
+        wsb = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")
+        idx = [i for i, m in enumerate(st["meta"]) if m[1] == pid][:layers]
+
+        def run():
+            for i in idx:
+                w4.w4a16_gemm(x, st["ws"][i], y, M, wsb, nb)
+        run()
+        ms = time_replays(torch, run, reps) / len(idx)
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        out[name] = {"us": ms * 1e3, "TFLOP/s": tf, "frac_of_dense_peak": tf / peak,
+                     "status_word": int(wsb[:4].view(torch.int32).item())}
+    tot_us = sum(v["us"] for v in out.values())
+    out["layer"] = {"us": tot_us, "TFLOP/s": 2.0 * M * sum(N * K for _, N, K in LAYER) / (tot_us * 1e-6) / 1e12,
+                    "peak_TFLOP/s": peak, "peak_source": "bf16_tflops of MEASURED_PEAKS.json (f16 runs at the "
+                                                         "bf16 tensor rate)"}
+    return out
+
+
 # ---- main ------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
@@ -306,7 +365,10 @@ def main():
     torch.cuda.set_device(local)
     M = 1
     st = build_step(torch, w4, synth, M)
-    seq = w4.DecodeSeq(st["ws"], st["xs"], st["ys"], M, use_pdl=True)
+    nbw = w4.w4_decode_seq_workspace_bytes(st["ws"], M)
+    ws_buf = torch.zeros(nbw + 256, dtype=torch.uint8, device="cuda")
+    ws_off = (-ws_buf.data_ptr()) % 256
+    seq = w4.DecodeSeq(st["ws"], st["xs"], st["ys"], M, workspace=ws_buf[ws_off:ws_off + nbw])
     for _ in range(args.warmup):
         seq.replay()
     torch.cuda.synchronize()
@@ -361,9 +423,15 @@ def main():
 
     extras = {}
     if not args.no_extras:
-        extras["eager_us_per_step"] = time_replays(torch, seq.eager, 20) * 1e3
+        extras["persistent_launch_without_graph_us_per_step"] = time_replays(torch, seq.eager, 50) * 1e3
+        extras["persistent_status_word"] = seq.status()
+        g = w4.DecodeSeq(st["ws"], st["xs"], st["ys"], M, use_pdl=True)
+        extras["graph_of_112_kernels_pdl_us_per_step"] = time_replays(torch, g.replay, 100) * 1e3
+        extras["eager_112_kernels_pdl_us_per_step"] = time_replays(torch, g.eager, 20) * 1e3
+        g.close()
         nopdl = w4.DecodeSeq(st["ws"], st["xs"], st["ys"], M, use_pdl=False)
-        extras["graph_no_pdl_us_per_step"] = time_replays(torch, nopdl.replay, 200) * 1e3
+        extras["graph_of_112_kernels_no_pdl_us_per_step"] = time_replays(torch, nopdl.replay, 100) * 1e3
+        extras["eager_112_kernels_no_pdl_us_per_step"] = time_replays(torch, nopdl.eager, 20) * 1e3
         nopdl.close()
         per = {}
         for pid, (name, N, K) in enumerate(LAYER):
@@ -378,14 +446,16 @@ def main():
                                     "depth": cfg.depth}}
             one.close()
         extras["per_projection_back_to_back_28_layers"] = per
+        extras["small_batch_step"] = small_batch_sweep(torch, w4, synth, st)
+        extras["prefill_M512"] = prefill_layer(torch, w4, synth, st)
 
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     roof = {"bound": "hbm", "achieved": per_gpu, "peak": peak, "unit": "GB/s", "frac": per_gpu / peak,
             "traffic": ncu_traffic_per_launch(),
-            "kernel": "decode kernel (all 112 launches of the step); achieved = algorithmic bytes per "
-                      "launch (%d) / average launch duration over the timed region (step time / %d)" %
-                      (BYTES_PER_STEP // launches, launches),
+            "kernel": "persistent decode-step kernel (one launch per step streams all 112 projections); "
+                      "achieved = algorithmic bytes per launch (%d) / average launch duration over the timed "
+                      "region" % (BYTES_PER_STEP // launches),
             "peak_source": "%s hbm_gbs (MEASURED_PEAKS.json)" % peak_kind if peak_kind == "measured"
             else "fallback 6.8 TB/s"}
     if roof["traffic"] is not None:
@@ -400,10 +470,11 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-                "config": {"workload": WORKLOAD, "M": M, "layers": LAYERS, "projections_per_step": launches,
+                "config": {"workload": WORKLOAD, "M": M, "layers": LAYERS, "projections_per_step": len(st["ws"]),
                            "bytes_per_step": BYTES_PER_STEP, "accumulate": "f32",
                            "l2": "inputs larger than L2: 3.36 GB of weights per step vs 129 MB L2",
-                           "launch": "one cudaGraphLaunch per step; programmatic dependent launch edges",
+                           "launch": "one cudaGraphLaunch per step of a one-node graph: the persistent "
+                                     "cooperative decode-step kernel (2 CTAs/SM)",
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "roofline": roof,
                 "cpu_baseline": cpu,

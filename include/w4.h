@@ -16,8 +16,9 @@
  * Conventions shared by every entry point
  *  - Ownership: the caller allocates and owns every buffer (packed weights,
  *    x, y, workspace).  The projection entry points and the sequence replay
- *    allocate nothing ("The Architecture of Modern Inference ...",
- *    ".nanoqwen Format": no heap allocation during generation).
+ *    allocate nothing ("The Architecture of Modern Inference ...", "Data
+ *    Integrity and Serialization: The .nanoqwen Format": no heap allocation
+ *    during generation).
  *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *    default stream).  Device work is enqueued on it and the call returns
  *    without waiting, unless the entry point says it is synchronous.
@@ -70,9 +71,10 @@ int w4_version(void);
 /* ------------------------------------------------------------------------
  * Packed layout (the offline repack).  The pages describe a "ValueShuffle"
  * layout that interleaves even and odd nibbles for the byte-permute
- * datapath ("Building a Custom LLM Inference Runtime ...", ".nanoqwen File
- * Format and Safety Protocols"; "The Architecture of Modern Inference ...",
- * ".nanoqwen Format"), without the exact permutation.  This library's
+ * datapath ("Building a Custom LLM Inference Runtime ...", "The .nanoqwen
+ * File Format and Safety Protocols"; "The Architecture of Modern Inference
+ * ...", "Data Integrity and Serialization: The .nanoqwen Format"), without the
+ * exact permutation.  This library's
  * layout puts each nibble where one warp lane needs it as a tensor-core
  * operand fragment:
  *
@@ -158,13 +160,15 @@ w4_status w4a16_gemv(const void* x, const w4_weight* w, void* y, int M,
 /* Launch shape of the decode kernel, for tuning sweeps.  Zero fields take
  * the library's choice.  The kernel is persistent: one CTA per SM (a cluster
  * of `splits` CTAs per K split), each walking blocks of `bands_per_cta`
- * 16-row bands and streaming their tiles through a shared-memory ring of
- * `depth` slots. */
+ * 16-row bands and streaming their tiles through a shared-memory ring that
+ * holds `depth` tiles. */
 typedef struct {
     int bands_per_cta; /* 16-row bands per work block: 1, 2 or 4 */
     int splits;        /* K splits = CTAs per cluster: 1..8 (at most K/128) */
-    int depth;         /* ring slots (tiles in flight per CTA): 2..96 */
-    int pdl;           /* 1: programmatic dependent launch (default), 0: off, -1: default */
+    int depth;         /* tiles in flight per CTA (ring size): a multiple of 8, 8..96 */
+    int pdl;           /* programmatic dependent launch: 1 (default) = dependents may launch once
+                          this grid's loads are issued, 2 = at once, 0 = off, -1 = default */
+    int ctas_per_sm;   /* persistent CTAs per SM: 1 or 2 */
 } w4_gemv_config;
 
 /* w4a16_gemv with an explicit launch shape (W4_ERR_UNSUPPORTED if the shape
@@ -239,7 +243,32 @@ w4_status w4_decode_seq_run_host(w4_seq* seq, const void* x_host, void* x_dev,
                                  size_t x_bytes, void* y_dev, void* y_host,
                                  size_t y_bytes, void* stream);
 
-/* Number of kernels one replay launches. */
+/* Device workspace bytes of a persistent sequence over these n weights at M
+ * tokens (0 on bad arguments).  Caller-owned, 256-byte aligned. */
+size_t w4_decode_seq_workspace_bytes(const w4_weight* w, int n, int M);
+
+/* The same projection chain as w4_decode_seq_create, run by ONE persistent
+ * cooperative kernel (two CTAs per SM) captured as a one-node graph.  Each
+ * CTA's producer streams the weights of every projection back to back into a
+ * shared-memory ring, never waiting on the chain, while its consumers compute
+ * projection i only after every CTA has finished projection i - 1 (completion
+ * counters in `workspace`), so the data dependency of a real decode step
+ * (x[i] computed from y[i-1]) is honoured.  Same arithmetic and results as
+ * w4a16_gemv.  `workspace` holds the projection table, the counters and
+ * K-split partials; it must stay alive and unshared while the sequence
+ * exists, and replays of one sequence must not overlap on the GPU.
+ * Synchronous (initialises the workspace). */
+w4_status w4_decode_seq_create_persistent(const w4_weight* w, const void* const* x,
+                                          void* const* y, int n, int M, void* workspace,
+                                          size_t workspace_bytes, void* stream, w4_seq** out);
+
+/* Status word of a persistent sequence (a synchronous device read): 0 when
+ * every wait of its replays so far completed, non-zero when one gave up after
+ * about a second (the outputs of that replay are then invalid).  0 for graph
+ * sequences, -1 on error. */
+int w4_decode_seq_status(const w4_seq* seq);
+
+/* Number of kernels one replay launches (1 for a persistent sequence). */
 int w4_decode_seq_kernels(const w4_seq* seq);
 
 void w4_decode_seq_destroy(w4_seq* seq);

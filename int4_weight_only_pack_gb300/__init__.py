@@ -41,7 +41,7 @@ class Weight(ctypes.Structure):
 class GemvConfig(ctypes.Structure):
     """w4_gemv_config: launch shape of the decode kernel."""
     _fields_ = [("bands_per_cta", ctypes.c_int), ("splits", ctypes.c_int), ("depth", ctypes.c_int),
-                ("pdl", ctypes.c_int)]
+                ("pdl", ctypes.c_int), ("ctas_per_sm", ctypes.c_int)]
 
 
 _vp, _i64, _sz, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
@@ -67,6 +67,10 @@ _SIGNATURES = {
     "w4_decode_seq_eager": (_int, [_vp, _vp]),
     "w4_decode_seq_run_host": (_int, [_vp, _vp, _vp, _sz, _vp, _vp, _sz, _vp]),
     "w4_decode_seq_kernels": (_int, [_vp]),
+    "w4_decode_seq_workspace_bytes": (_sz, [ctypes.POINTER(Weight), _int, _int]),
+    "w4_decode_seq_create_persistent": (_int, [ctypes.POINTER(Weight), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                               _int, _int, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
+    "w4_decode_seq_status": (_int, [_vp]),
     "w4_decode_seq_destroy": (None, [_vp]),
 }
 EXPORTED = tuple(_SIGNATURES)
@@ -198,18 +202,39 @@ def w4a16_gemm_static_scratch(x, w: Weight, y, M: int, stream=None):
     _check(lib().w4a16_gemm_static_scratch(_addr(x), ctypes.byref(w), _addr(y), M, _stream(stream)))
 
 
-class DecodeSeq:
-    """w4_decode_seq_*: a captured chain of decode projections."""
+def w4_decode_seq_workspace_bytes(weights, M: int) -> int:
+    n = len(weights)
+    return lib().w4_decode_seq_workspace_bytes((Weight * n)(*weights), n, M)
 
-    def __init__(self, weights, xs, ys, M: int, use_pdl: bool = True, stream=None):
+
+class DecodeSeq:
+    """w4_decode_seq_*: a captured chain of decode projections.  With
+    ``workspace`` (a 256-byte-aligned device buffer of
+    w4_decode_seq_workspace_bytes), the chain runs as one persistent kernel
+    (w4_decode_seq_create_persistent); otherwise as a graph of one kernel per
+    projection (w4_decode_seq_create)."""
+
+    def __init__(self, weights, xs, ys, M: int, use_pdl: bool = True, stream=None, workspace=None,
+                 workspace_bytes: int | None = None):
         n = len(weights)
         self._w = (Weight * n)(*weights)
         self._x = (ctypes.c_void_p * n)(*[_addr(t) for t in xs])
         self._y = (ctypes.c_void_p * n)(*[_addr(t) for t in ys])
         self._h = ctypes.c_void_p()
         self.n, self.M = n, M
-        _check(lib().w4_decode_seq_create(self._w, self._x, self._y, n, M, int(use_pdl), _stream(stream),
-                                          ctypes.byref(self._h)))
+        self.persistent = workspace is not None
+        if self.persistent:
+            if workspace_bytes is None:
+                workspace_bytes = workspace.numel() * workspace.element_size()
+            self._ws = workspace
+            _check(lib().w4_decode_seq_create_persistent(self._w, self._x, self._y, n, M, _addr(workspace),
+                                                         workspace_bytes, _stream(stream), ctypes.byref(self._h)))
+        else:
+            _check(lib().w4_decode_seq_create(self._w, self._x, self._y, n, M, int(use_pdl), _stream(stream),
+                                              ctypes.byref(self._h)))
+
+    def status(self) -> int:
+        return lib().w4_decode_seq_status(self._h)
 
     def replay(self, stream=None):
         _check(lib().w4_decode_seq_replay(self._h, _stream(stream)))

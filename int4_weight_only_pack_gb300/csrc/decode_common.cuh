@@ -1,0 +1,209 @@
+// Consumer-side building blocks shared by the single-projection decode kernel
+// (gemv.cu) and the persistent decode-step kernel (step.cu): staging x in
+// shared memory, the per-tile multiply-accumulate, and the fixed-order
+// reduction of a block's per-warp partials.
+//
+// Arithmetic of one tile (16 rows x 128 K, one scale group per row): the
+// nibbles u enter the tensor core as exact fp16 subnormals (u * 2^-24 for rows
+// r, u * 2^-20 for rows r + 8), x as fp16; mma.sync m16n8k16 multiplies
+// exactly and sums in FP32 (two independent chains).  The group's partial
+//     sum_k x*q = 2^24 * D - 8 * sum_k x        (2^20 for rows r + 8)
+// is then scaled by the group's FP32 scale and added in FP32.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "tc_ptx.cuh"
+#include "w4_device.cuh"
+#include "w4_internal.cuh"
+
+namespace w4 {
+namespace dec {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kChunk = 8;  // tiles per ring slot: one per consumer warp
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// First MMA of a chain: C = 0.
+__device__ __forceinline__ void mma16816_zero(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// Shared-memory bytes of an x slice of Gs groups for MP padded tokens, and of
+// its per-group sums.
+__host__ __device__ constexpr int x_bytes(int MP, int Gs) { return MP * Gs * 256; }
+__host__ __device__ constexpr int xsum_bytes(int Gs) { return Gs * 16 * 4; }
+
+// Stage x[0:M, 128*g_lo : 128*(g_lo+Gs)) (fp16 pairs; row stride K/2 words)
+// into `xs` in fragment order -- word (gl, q, m, c, e) at
+// gl*MP*64 + q*MP*16 + (m*4 + c)*4 + e holds k16 step 2q + (e >> 1) of group
+// gl, k 4c + 2(e & 1) .. +1 -- with rows M..MP-1 zero, and the sum of x over
+// every group and token into xsum[gl*16 + m] (0 for m >= M).  Called by the
+// consumer threads only; returns with all of them synchronised.
+template <int MP>
+__device__ __forceinline__ void stage_x(const uint32_t* x, int M, int K, int g_lo, int Gs, uint32_t* xs,
+                                        float* xsum) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int per_row = Gs * 64;  // fp16 pairs of this K range
+    const uint32_t* xg = x + (size_t)g_lo * 64;
+    const int kp = K / 2;
+    const int total = MP * per_row;
+    // eight independent loads in flight per thread, then the stores
+    for (int base = tid; base < total; base += 8 * kConsumers) {
+        uint32_t v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = base + u * kConsumers;
+            v[u] = 0;
+            if (idx < total) {
+                const int m = idx / per_row, r = idx - m * per_row;
+                if (m < M) v[u] = __ldcg(xg + (size_t)m * kp + r);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = base + u * kConsumers;
+            if (idx < total) {
+                const int m = idx / per_row, r = idx - m * per_row;
+                // pair kk2 of the group = k 2*kk2, 2*kk2+1; lane class c owns
+                // k 4c..4c+3 of each k16 step (lower pair is b0, upper b1)
+                const int gl = r >> 6, kk2 = r & 63;
+                const int j = kk2 >> 3, c = (kk2 >> 1) & 3, hi = kk2 & 1;
+                xs[gl * (MP * 64) + (j >> 1) * (MP * 16) + (m * 4 + c) * 4 + (j & 1) * 2 + hi] = v[u];
+            }
+        }
+    }
+    for (int idx = tid; idx < Gs * 16; idx += kConsumers)
+        if ((idx & 15) >= M) xsum[idx] = 0.f;
+    tc::named_barrier(1, kConsumers);
+    // FP32 sums in a fixed order: four values per lane, then a butterfly
+    for (int idx = warp; idx < Gs * M; idx += kConsumerWarps) {
+        const int gl = idx / M, m = idx - gl * M;
+        const int q = lane >> 3, c = (lane >> 1) & 3, e = (lane & 1) * 2;
+        const uint32_t* src = xs + gl * (MP * 64) + q * (MP * 16) + (m * 4 + c) * 4 + e;
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(src));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(src + 1));
+        float sum = (f0.x + f0.y) + (f1.x + f1.y);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+        if (lane == 0) xsum[gl * 16 + m] = sum;
+    }
+    tc::named_barrier(1, kConsumers);
+}
+
+// Per-lane state of the tile multiply-accumulate.
+template <int MP>
+struct TileMac {
+    static constexpr int NT = (MP + 7) / 8;  // n8 token tiles of the MMA
+    uint32_t xfrag;                          // this lane's B-fragment words of group 0
+    uint32_t xsum;                           // this lane's token pair's sums of group 0
+    bool xlane;                              // lanes of padding tokens keep zero fragments
+    uint4 xb[NT][4];
+
+    __device__ __forceinline__ TileMac(uint32_t x_smem, uint32_t xsum_smem, int lane) {
+        const int tok = lane >> 2, cl4 = lane & 3;
+        xfrag = x_smem + (uint32_t)((tok * 4 + cl4) * 16);
+        xsum = xsum_smem + (uint32_t)(2 * cl4 * 4);
+        xlane = tok < MP;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xb[nt][q] = make_uint4(0, 0, 0, 0);
+    }
+
+    // acc += s * sum_{k in group gl} x * q for the tile at shared address ta.
+    __device__ __forceinline__ void run(uint32_t ta, int gl, int lane, float (&acc)[NT][4]) {
+        const uint4 lo = lds128(ta + 16 * lane), hi = lds128(ta + 512 + 16 * lane);
+        const uint32_t sc = lds32(ta + kScaleOffset + 4 * (lane >> 2));
+        if (xlane) {
+            const uint32_t xa = xfrag + (uint32_t)gl * (MP * 256);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) xb[nt][q] = lds128(xa + (uint32_t)(q * MP * 64 + nt * 512));
+        }
+        float pe[NT][4], po[NT][4];
+        const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t a[4];
+            unpack_word_biased(wd[j], a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint4& v = xb[nt][j >> 1];
+                if (j == 0)
+                    mma16816_zero(pe[nt], a, v.x, v.y);
+                else if (j == 1)
+                    mma16816_zero(po[nt], a, v.z, v.w);
+                else if (j & 1)
+                    mma16816(po[nt], a, v.z, v.w);
+                else
+                    mma16816(pe[nt], a, v.x, v.y);
+            }
+        }
+        const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sc));
+        const float sa = sf.x * 16777216.f, sb = sf.y * 1048576.f;
+        const float ca = -8.f * sf.x, cb = -8.f * sf.y;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float2 X;
+            asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];"
+                         : "=f"(X.x), "=f"(X.y)
+                         : "r"(xsum + (uint32_t)((gl * 16 + nt * 8) * 4)));
+            acc[nt][0] = fmaf(ca, X.x, fmaf(sa, pe[nt][0] + po[nt][0], acc[nt][0]));
+            acc[nt][1] = fmaf(ca, X.y, fmaf(sa, pe[nt][1] + po[nt][1], acc[nt][1]));
+            acc[nt][2] = fmaf(cb, X.x, fmaf(sb, pe[nt][2] + po[nt][2], acc[nt][2]));
+            acc[nt][3] = fmaf(cb, X.y, fmaf(sb, pe[nt][3] + po[nt][3], acc[nt][3]));
+        }
+    }
+};
+
+// Shared-memory floats of one buffer of per-warp block partials:
+// [warp][band][nt][lane][4].
+__host__ __device__ constexpr int red_floats(int BB, int NT) { return kConsumerWarps * BB * NT * 128; }
+
+// Fixed-order sum over the consumer warps of the block partials for the
+// outputs t = tid + i * kConsumers < nb*16*M (t = m * nb*16 + band row);
+// NaN where !ok.
+template <int NT>
+__device__ __forceinline__ void block_sums(const float* red, int BB, int nb, int M, bool ok, float (&v)[4]) {
+    const int Tout = nb * 16 * M;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = threadIdx.x + i * kConsumers;
+        v[i] = 0.f;
+        if (t < Tout) {
+            const int m = t / (nb * 16), rl = t - m * (nb * 16);
+            const int bb = rl >> 4, rr = rl & 15;
+            const int nt = m >> 3, col = m & 7;
+            const int ln = (rr & 7) * 4 + (col >> 1), r = (rr >> 3) * 2 + (col & 1);
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) sum += red[((w * BB + bb) * NT + nt) * 128 + ln * 4 + r];
+            v[i] = ok ? sum : __int_as_float(0x7FC00000);
+        }
+    }
+}
+
+}  // namespace dec
+}  // namespace w4

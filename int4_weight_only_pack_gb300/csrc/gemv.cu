@@ -9,12 +9,13 @@
 //  * HBM-bound streaming.  One persistent CTA per SM (a cluster of `splits`
 //    CTAs when K is split).  Its producer lane streams the CTA's packed tiles,
 //    in order, into a ring of shared-memory slots with 1-D bulk copies
-//    (cp.async.bulk, one 1056-byte tile per slot, completion on the slot's
-//    mbarrier).  The producer starts before the kernel waits on the previous
+//    (cp.async.bulk; a slot holds 8 consecutive tiles, copied as one or two
+//    contiguous runs, completion on the slot's mbarrier).  The producer starts before the kernel waits on the previous
 //    grid (programmatic dependent launch), so a projection's weights are in
 //    flight while its predecessor drains; every CTA lets its dependents launch
 //    at once, so the next projection's CTAs can do the same.
-//  * Eight consumer warps take the ring's tiles round-robin.  Unpacking: one
+//  * Eight consumer warps consume every slot in order, warp w taking the
+//    slot's tile w, and all eight hand the slot back.  Unpacking: one
 //    32-bit word per lane and k16 step holds eight nibbles; two LOP3 masks
 //    with the fp16 exponent pattern 0x6400 (and the same after a shift by 8)
 //    give 1024 + u and 1024 + 16u, and one f16x2 subtract or FMA turns them
@@ -38,17 +39,16 @@
 #include <set>
 #include <utility>
 
-#include "tc_ptx.cuh"
-#include "w4_device.cuh"
-#include "w4_internal.cuh"
+#include "decode_common.cuh"
 
 namespace w4 {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
+using dec::kChunk;
+using dec::kConsumers;
+using dec::kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr int kMaxSmem = 220 * 1024;
-constexpr int kDefaultRing = 48;
+constexpr int kDefaultRing = 64;
 constexpr int kMaxRing = 96;
 
 // SM count of the current device (looked up once per device).
@@ -71,42 +71,29 @@ struct GemvParams {
     const uint8_t* w;   // packed tiles
     uint16_t* y;        // fp16 [M, N]
     int M, N, K, G, bands;
+    int BB;             // bands per work block
     int nblocks;        // ceil(bands / BB)
     int ring;           // ring slots
+    int early_trigger;  // let dependents launch at once instead of after the loads are issued
 };
 
 // Shared-memory carve-up, identical on host and device.
 struct SmemLayout {
-    int bar, x, red, cpart, total;
-    __host__ __device__ SmemLayout(int ring, int M, int gpc, int BB, int NT, int S) {
-        bar = ring * kTileBytes;                                        // ring of tile slots first
-        x = (bar + (2 * ring + 4) * 8 + 15) & ~15;                      // full/empty per slot, cfull[2], cempty[2]
-        red = x + M * gpc * 256;                                        // x slice in fragment order
-        cpart = red + 2 * kConsumerWarps * BB * NT * 4 * 32 * 4;        // per-warp block partials, 2 buffers
-        total = cpart + 2 * (S > 1 ? S - 1 : 0) * BB * 16 * M * 4;      // leader's receive buffers
+    int bar, x, xsum, red, cpart, total;
+    __host__ __device__ SmemLayout(int ring, int MP, int gpc, int BB, int NT, int S, int M) {
+        bar = ring * kTileBytes;                                 // ring of 8-tile slots first
+        x = (bar + (2 * (ring / kChunk) + 4) * 8 + 15) & ~15;    // full/empty per slot, cfull[2], cempty[2]
+        xsum = x + dec::x_bytes(MP, gpc);                        // x slice in fragment order
+        red = xsum + dec::xsum_bytes(gpc);                       // per group and token: sum of x
+        cpart = red + 2 * dec::red_floats(BB, NT) * 4;           // per-warp block partials, 2 buffers
+        total = cpart + 2 * (S > 1 ? S - 1 : 0) * BB * 16 * M * 4;  // leader's receive buffers
     }
 };
 
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-    return v;
-}
-
-template <int NT, int BB>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(GemvParams p) {
+// MP: token count padded to 1, 2, 4, 8 or 16 (x rows beyond M are zero).
+template <int MP>
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
+    constexpr int NT = (MP + 7) / 8;  // n8 token tiles of the MMA
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = gridDim.y, rank = blockIdx.y;  // cluster (1, S, 1): rank = K split
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -114,16 +101,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(GemvParams p) {
     const int g_hi = (int)(((long long)p.G * (rank + 1)) / S);
     const int Gs = g_hi - g_lo;
     const int gpc = (p.G + S - 1) / S;
-    const int M = p.M, ring = p.ring;
-    const SmemLayout L(ring, M, gpc, BB, NT, S);
+    const int M = p.M, BB = p.BB, nslots = p.ring / kChunk;
+    const SmemLayout L(p.ring, MP, gpc, BB, NT, S, M);
     const uint32_t sbase = tc::smem_addr(smem);
-    const uint32_t full0 = sbase + L.bar, empty0 = full0 + 8 * ring, cfull0 = empty0 + 8 * ring,
+    const uint32_t full0 = sbase + L.bar, empty0 = full0 + 8 * nslots, cfull0 = empty0 + 8 * nslots,
                    cempty0 = cfull0 + 16;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < ring; ++s) {
+        for (int s = 0; s < nslots; ++s) {
             tc::mbar_init(full0 + 8 * s, 1);
-            tc::mbar_init(empty0 + 8 * s, 1);
+            tc::mbar_init(empty0 + 8 * s, kConsumerWarps);
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(cfull0 + 8 * b, S > 1 ? S - 1 : 1);
@@ -133,181 +120,169 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(GemvParams p) {
     }
     __syncthreads();
     if (S > 1) tc::cluster_sync_all();  // every CTA's barriers exist before any remote access
-    // The next kernel on the stream may start now: it only streams its own
-    // weights until it, too, waits for this grid to finish.
-    pdl_launch_dependents();
+    if (p.early_trigger) pdl_launch_dependents();
 
     const int P = gridDim.x;
     if (warp == kConsumerWarps) {
-        // ---- producer: stream this CTA's tiles into the ring ------------------
+        // ---- producer: stream this CTA's tiles, 8 per chunk slot -----------------
         if (lane == 0) {
-            int seq = 0;
+            int slot = 0;
+            uint32_t use = 0, issued = 0;
             bool ok = true;
             for (int blk = blockIdx.x; blk < p.nblocks && ok; blk += P) {
                 const int band0 = blk * BB;
                 const int T = min(BB, p.bands - band0) * Gs;
-                for (int t = 0; t < T; ++t, ++seq) {
-                    const int slot = seq % ring, use = seq / ring;
+                int bb = 0, gl = 0;  // position of tile t0 within the block
+                for (int t0 = 0; t0 < T; t0 += kChunk) {
                     if (use > 0 && !tc::mbar_wait(empty0 + 8 * slot, (use - 1) & 1)) {
                         ok = false;
                         break;
                     }
-                    const int bb = t / Gs, g = g_lo + (t - bb * Gs);
-                    const uint8_t* src = p.w + ((size_t)(band0 + bb) * p.G + g) * kTileBytes;
-                    tc::mbar_arrive_expect_tx(full0 + 8 * slot, kTileBytes);
-                    tc::bulk_load(sbase + slot * kTileBytes, src, kTileBytes, full0 + 8 * slot);
+                    const int n = min(kChunk, T - t0);
+                    const uint32_t bar = full0 + 8 * slot;
+                    tc::mbar_arrive_expect_tx(bar, (uint32_t)n * kTileBytes);
+                    // copy tiles t0 .. t0+n-1 as runs that stay inside one band's K range
+                    uint32_t dst = sbase + (uint32_t)slot * (kChunk * kTileBytes);
+                    for (int left = n; left > 0;) {
+                        const int run = min(left, Gs - gl);
+                        const uint8_t* src = p.w + ((size_t)(band0 + bb) * p.G + g_lo + gl) * kTileBytes;
+                        tc::bulk_load(dst, src, (uint32_t)run * kTileBytes, bar);
+                        dst += run * kTileBytes;
+                        left -= run;
+                        gl += run;
+                        if (gl == Gs) {
+                            gl = 0;
+                            ++bb;
+                        }
+                    }
+                    ++issued;
+                    if (++slot == nslots) {
+                        slot = 0;
+                        ++use;
+                    }
                 }
             }
-            // every copy has landed before the CTA may exit
-            for (int sq = seq - 1; sq >= 0 && sq >= seq - ring; --sq)
-                tc::mbar_wait(full0 + 8 * (sq % ring), (sq / ring) & 1);
+            // Everything this CTA reads is in flight: the next kernel on the
+            // stream may start (it streams its own weights until it, too,
+            // waits for this grid to finish).
+            pdl_launch_dependents();
+            // every copy has landed before the CTA may exit: wait for the
+            // latest phase of each slot that was filled
+            for (uint32_t k = 0; k < (uint32_t)nslots && k < issued; ++k) {
+                const uint32_t c = issued - 1 - k;
+                tc::mbar_wait(full0 + 8 * (c % nslots), (c / nslots) & 1);
+            }
         }
         __syncwarp();
     } else {
         // ---- consumers -----------------------------------------------------------
         // x may be produced by the previous kernel on the stream: read it only now.
         pdl_wait();
-        uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L.x);
-        {
-            const int per_row = Gs * 64;  // fp16 pairs of this split's K range
-            const uint32_t* xg = p.x + (size_t)g_lo * 64;
-            const int kp = p.K / 2;
-            for (int idx = threadIdx.x; idx < M * per_row; idx += kConsumers) {
-                const int m = idx / per_row, r = idx - m * per_row;
-                const uint32_t v = __ldcg(xg + (size_t)m * kp + r);
-                // pair kk2 of the group = k 2*kk2, 2*kk2+1; lane class c owns
-                // k 4c..4c+3 of each k16 step (the lower pair is b0, the upper b1)
-                const int gl = r >> 6, kk2 = r & 63;
-                const int j = kk2 >> 3, c = (kk2 >> 1) & 3, hi = kk2 & 1;
-                xs[gl * (M * 64) + (j >> 1) * (M * 16) + (m * 4 + c) * 4 + (j & 1) * 2 + hi] = v;
-            }
-        }
-        tc::named_barrier(1, kConsumers);
+        dec::stage_x<MP>(p.x, M, p.K, g_lo, Gs, reinterpret_cast<uint32_t*>(smem + L.x),
+                         reinterpret_cast<float*>(smem + L.xsum));
+        // everything this CTA's consumers read from the previous grid is read
+        pdl_launch_dependents();
 
-        const uint4* xs4 = reinterpret_cast<const uint4*>(smem + L.x);
-        const int tok = lane >> 2, cl4 = lane & 3;
+        dec::TileMac<MP> mac(sbase + L.x, sbase + L.xsum, lane);
         float* red_base = reinterpret_cast<float*>(smem + L.red);
-        const int red_buf = kConsumerWarps * BB * NT * 4 * 32;
+        const int red_buf = dec::red_floats(BB, NT);
         const int part_buf = (S > 1 ? S - 1 : 0) * BB * 16 * M;
-        int seq = 0, kblk = 0;
+        int slot = 0;
+        uint32_t use = 0;
+        int kblk = 0;
+        bool ok = true;
         for (int blk = blockIdx.x; blk < p.nblocks; blk += P, ++kblk) {
             const int band0 = blk * BB;
             const int nb = min(BB, p.bands - band0);
             const int T = nb * Gs;
-            bool ok = true;
-            float acc[BB][NT][4];
+            const bool blk_ok0 = ok;
+            // this warp's partial of band cur_bb; bands it has no tile of stay 0
+            float* red = red_base + (kblk & 1) * red_buf;
+            float4* myred = reinterpret_cast<float4*>(red) + warp * BB * NT * 32 + lane;
+            for (int i = 0; i < BB * NT; ++i) myred[i * 32] = make_float4(0.f, 0.f, 0.f, 0.f);
+            float acc[NT][4];
 #pragma unroll
-            for (int bb = 0; bb < BB; ++bb)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) acc[bb][nt][r] = 0.f;
+                for (int r = 0; r < 4; ++r) acc[nt][r] = 0.f;
+            int cur_bb = 0, band_end = Gs;
 
-            for (int t = warp; t < T; t += kConsumerWarps) {
-                const int sq = seq + t;
-                const int slot = sq % ring;
-                if (!tc::mbar_wait(full0 + 8 * slot, (sq / ring) & 1)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t ta = sbase + slot * kTileBytes;
-                const uint4 lo = lds128(ta + 16 * lane), hi = lds128(ta + 512 + 16 * lane);
-                const uint32_t sc = lds32(ta + kScaleOffset + 4 * (lane >> 2));
-                const int bb = t / Gs, gl = t - bb * Gs;
-                uint4 xb[NT][4];
+            for (int t0 = 0; t0 < T; t0 += kChunk) {
+                if (ok && !tc::mbar_wait(full0 + 8 * slot, use & 1)) ok = false;
+                const int t = t0 + warp;  // this warp's tile in the chunk
+                if (ok && t < T) {
+                    while (t >= band_end) {  // entering a new band: park the finished one
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int m = nt * 8 + tok;
+                        for (int nt = 0; nt < NT; ++nt)
+                            myred[(cur_bb * NT + nt) * 32] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        xb[nt][q] = (m < M) ? xs4[gl * (M * 16) + q * (M * 4) + m * 4 + cl4] : make_uint4(0, 0, 0, 0);
-                }
-                float part[NT][4];
+                        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) part[nt][r] = 0.f;
-                const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t a[4];
-                    unpack_word(wd[j], a);
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const uint4& v = xb[nt][j >> 1];
-                        mma16816(part[nt], a, (j & 1) ? v.z : v.x, (j & 1) ? v.w : v.y);
+                            for (int r = 0; r < 4; ++r) acc[nt][r] = 0.f;
+                        ++cur_bb;
+                        band_end += Gs;
                     }
+                    mac.run(sbase + (uint32_t)slot * (kChunk * kTileBytes) + (uint32_t)warp * kTileBytes,
+                            t - cur_bb * Gs, lane, acc);
                 }
-                // the tile's words are consumed: hand the slot back
+                // the chunk is consumed by this warp (its words are in registers
+                // and used): hand the slot back
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(empty0 + 8 * slot);
-                const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sc));
-#pragma unroll
-                for (int b2 = 0; b2 < BB; ++b2) {
-                    if (b2 == bb) {
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            acc[b2][nt][0] = fmaf(sf.x, part[nt][0], acc[b2][nt][0]);
-                            acc[b2][nt][1] = fmaf(sf.x, part[nt][1], acc[b2][nt][1]);
-                            acc[b2][nt][2] = fmaf(sf.y, part[nt][2], acc[b2][nt][2]);
-                            acc[b2][nt][3] = fmaf(sf.y, part[nt][3], acc[b2][nt][3]);
-                        }
-                    }
+                if (++slot == nslots) {
+                    slot = 0;
+                    ++use;
                 }
             }
-            seq += T;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                myred[(cur_bb * NT + nt) * 32] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
 
             // ---- fixed-order reduction of the block over the warps --------------
-            float* red = red_base + (kblk & 1) * red_buf;
-#pragma unroll
-            for (int bb = 0; bb < BB; ++bb)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int r = 0; r < 4; ++r)
-                        red[(((warp * BB + bb) * NT + nt) * 4 + r) * 32 + lane] = ok ? acc[bb][nt][r] : __int_as_float(0x7FC00000);
             tc::named_barrier(1, kConsumers);
             const int Tout = nb * 16 * M;  // outputs of this block: [m][band row]
-            float v[4];                    // <= 4 outputs per thread (BB * 16 * 16 <= 1024)
-            int cnt = 0;
-            for (int t = threadIdx.x; t < Tout; t += kConsumers, ++cnt) {
-                const int m = t / (nb * 16), rl = t - m * (nb * 16);
-                const int bb = rl >> 4, rr = rl & 15;
-                const int nt = m >> 3, col = m & 7;
-                const int ln = (rr & 7) * 4 + (col >> 1), r = (rr >> 3) * 2 + (col & 1);
-                float sum = 0.f;
+            float v[4];
+            dec::block_sums<NT>(red, BB, nb, M, blk_ok0 && ok, v);
+            if (S == 1) {
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) sum += red[(((w * BB + bb) * NT + nt) * 4 + r) * 32 + ln];
-                v[cnt & 3] = sum;
-                if (S == 1) {
-                    const int n = band0 * 16 + rl;
-                    if (n < p.N) p.y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(sum));
+                for (int i = 0; i < 4; ++i) {
+                    const int t = threadIdx.x + i * kConsumers;
+                    if (t < Tout) {
+                        const int m = t / (nb * 16), rl = t - m * (nb * 16);
+                        const int n = band0 * 16 + rl;
+                        if (n < p.N) p.y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(v[i]));
+                    }
                 }
-            }
-            if (S > 1) {
+            } else {
                 const int buf = kblk & 1;
-                const uint32_t use = (uint32_t)(kblk >> 1);
+                const uint32_t cuse = (uint32_t)(kblk >> 1);
                 float* cpart = reinterpret_cast<float*>(smem + L.cpart) + buf * part_buf;
                 if (rank != 0) {
                     // wait until the leader has read this buffer's previous contents
-                    bool got = tc::mbar_wait_cluster(cempty0 + 8 * buf, (use & 1) ^ 1);
-                    const uint32_t remote = tc::map_rank(tc::smem_addr(cpart), 0) + (uint32_t)(rank - 1) * BB * 16 * M * 4;
-                    cnt = 0;
-                    for (int t = threadIdx.x; t < Tout; t += kConsumers, ++cnt)
-                        tc::st_cluster_f32(remote + 4u * t, got ? v[cnt & 3] : __int_as_float(0x7FC00000));
+                    const bool got = tc::mbar_wait_cluster(cempty0 + 8 * buf, (cuse & 1) ^ 1);
+                    const uint32_t remote =
+                        tc::map_rank(tc::smem_addr(cpart), 0) + (uint32_t)(rank - 1) * BB * 16 * M * 4;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int t = threadIdx.x + i * kConsumers;
+                        if (t < Tout) tc::st_cluster_f32(remote + 4u * t, got ? v[i] : __int_as_float(0x7FC00000));
+                    }
                     tc::fence_acq_rel_cluster();
                     tc::named_barrier(1, kConsumers);
                     if (threadIdx.x == 0) tc::mbar_arrive_remote(tc::map_rank(cfull0 + 8 * buf, 0));
                 } else {
-                    const bool got = tc::mbar_wait_cluster(cfull0 + 8 * buf, use & 1);
-                    cnt = 0;
-                    for (int t = threadIdx.x; t < Tout; t += kConsumers, ++cnt) {
-                        float sum = v[cnt & 3];
-                        for (int r2 = 1; r2 < S; ++r2) sum += cpart[(r2 - 1) * BB * 16 * M + t];
-                        if (!got) sum = __int_as_float(0x7FC00000);
-                        const int m = t / (nb * 16), rl = t - m * (nb * 16);
-                        const int n = band0 * 16 + rl;
-                        if (n < p.N) p.y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(sum));
+                    const bool got = tc::mbar_wait_cluster(cfull0 + 8 * buf, cuse & 1);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int t = threadIdx.x + i * kConsumers;
+                        if (t < Tout) {
+                            float sum = v[i];
+                            for (int r2 = 1; r2 < S; ++r2) sum += cpart[(r2 - 1) * BB * 16 * M + t];
+                            if (!got) sum = __int_as_float(0x7FC00000);
+                            const int m = t / (nb * 16), rl = t - m * (nb * 16);
+                            const int n = band0 * 16 + rl;
+                            if (n < p.N) p.y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(sum));
+                        }
                     }
                     tc::named_barrier(1, kConsumers);
                     if (threadIdx.x == 0)
@@ -324,31 +299,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(GemvParams p) {
 // ---- host side -------------------------------------------------------------
 using KernelFn = void (*)(GemvParams);
 
-template <int NT, int BB>
-static KernelFn kernel_ptr() {
-    return gemv_kernel<NT, BB>;
-}
+static int padded_tokens(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
 
-static KernelFn pick_kernel(int NT, int BB) {
-    if (NT == 1 && BB == 1) return kernel_ptr<1, 1>();
-    if (NT == 1 && BB == 2) return kernel_ptr<1, 2>();
-    if (NT == 1 && BB == 4) return kernel_ptr<1, 4>();
-    if (NT == 2 && BB == 1) return kernel_ptr<2, 1>();
-    if (NT == 2 && BB == 2) return kernel_ptr<2, 2>();
-    if (NT == 2 && BB == 4) return kernel_ptr<2, 4>();
-    return nullptr;
+static KernelFn pick_kernel(int M) {
+    switch (padded_tokens(M)) {
+        case 1: return gemv_kernel<1>;
+        case 2: return gemv_kernel<2>;
+        case 4: return gemv_kernel<4>;
+        case 8: return gemv_kernel<8>;
+        default: return gemv_kernel<16>;
+    }
 }
 
 static int gemv_smem_bytes(int M, int G, int BB, int S, int ring) {
-    const int NT = M <= 8 ? 1 : 2;
-    return SmemLayout(ring, M, (G + S - 1) / S, BB, NT, S).total;
+    const int MP = padded_tokens(M);
+    return SmemLayout(ring, MP, (G + S - 1) / S, BB, (MP + 7) / 8, S, M).total;
 }
 
 // Critical-path tiles per consumer warp of a launch shape (lower is better):
 // waves of blocks over the persistent clusters x tiles per warp per block.
-static double shape_cost(int64_t bands, int G, int BB, int S, int sms) {
+static double shape_cost(int64_t bands, int G, int BB, int S, int slots) {
     const int64_t nblocks = (bands + BB - 1) / BB;
-    const int64_t clusters = sms / S;
+    const int64_t clusters = slots / S;
     const int64_t P = nblocks < clusters ? nblocks : clusters;
     const int64_t waves = (nblocks + P - 1) / P;
     const int Gs = (G + S - 1) / S;
@@ -365,8 +337,8 @@ void default_gemv_config(int M, int64_t N, int64_t K, w4_gemv_config* c) {
     for (int S = 1; S <= 8; S *= 2) {
         if (S > G) break;
         for (int BB = 1; BB <= 4; BB *= 2) {
-            if (gemv_smem_bytes(M, G, BB, S, kDefaultRing) > 128 * 1024) continue;
-            const double cost = shape_cost(bands, G, BB, S, sms);
+            if (gemv_smem_bytes(M, G, BB, S, kDefaultRing) > 110 * 1024) continue;  // two CTAs per SM
+            const double cost = shape_cost(bands, G, BB, S, 2 * sms);
             if (cost < best - 1e-9) {
                 best = cost;
                 c->bands_per_cta = BB;
@@ -376,6 +348,7 @@ void default_gemv_config(int M, int64_t N, int64_t K, w4_gemv_config* c) {
     }
     c->depth = kDefaultRing;
     c->pdl = 1;
+    c->ctas_per_sm = 2;
 }
 
 // Raise a kernel's dynamic shared-memory limit once per (device, kernel).  Not
@@ -397,10 +370,10 @@ static w4_status allow_large_smem(KernelFn fn) {
 }
 
 static w4_status resolve(const w4_weight* w, int M, const w4_gemv_config& c, KernelFn* fn, int* smem) {
-    const int NT = M <= 8 ? 1 : 2;
-    *fn = pick_kernel(NT, c.bands_per_cta);
+    *fn = (c.bands_per_cta == 1 || c.bands_per_cta == 2 || c.bands_per_cta == 4) ? pick_kernel(M) : nullptr;
     const int G = (int)num_groups(w->K);
-    if (!*fn || c.splits < 1 || c.splits > 8 || c.splits > G || c.depth < 2 || c.depth > kMaxRing) {
+    if (!*fn || c.splits < 1 || c.splits > 8 || c.splits > G || c.depth < kChunk || c.depth > kMaxRing ||
+        c.depth % kChunk != 0 || c.ctas_per_sm < 1 || c.ctas_per_sm > 2) {
         set_error("no decode kernel for M=%d bands_per_cta=%d splits=%d depth=%d", M, c.bands_per_cta, c.splits,
                   c.depth);
         return W4_ERR_UNSUPPORTED;
@@ -444,9 +417,11 @@ w4_status launch_gemv(const void* x, const w4_weight* w, void* y, int M, const w
     p.K = (int)w->K;
     p.G = (int)num_groups(w->K);
     p.bands = (int)num_bands(w->N);
+    p.BB = c.bands_per_cta;
     p.nblocks = (p.bands + c.bands_per_cta - 1) / c.bands_per_cta;
     p.ring = c.depth;
-    const int clusters = sm_count() / c.splits;
+    p.early_trigger = c.pdl == 2 ? 1 : 0;
+    const int clusters = c.ctas_per_sm * sm_count() / c.splits;
     const int P = p.nblocks < clusters ? p.nblocks : clusters;
 
     cudaLaunchConfig_t cfg = {};
@@ -535,6 +510,7 @@ extern "C" w4_status w4a16_gemv_config(const void* x, const w4_weight* w, void* 
         if (cfg->splits) c.splits = cfg->splits;
         if (cfg->depth) c.depth = cfg->depth;
         if (cfg->pdl >= 0) c.pdl = cfg->pdl;
+        if (cfg->ctas_per_sm) c.ctas_per_sm = cfg->ctas_per_sm;
     }
     return launch_gemv(x, w, y, M, c, static_cast<cudaStream_t>(stream));
 }

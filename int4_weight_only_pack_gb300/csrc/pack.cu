@@ -3,7 +3,7 @@
 //
 // The pages call their layout "ValueShuffle": INT4 nibbles interleaved even
 // with odd so that the byte-permute datapath unpacks them cheaply ("Building a
-// Custom LLM Inference Runtime ...", ".nanoqwen File Format and Safety
+// Custom LLM Inference Runtime ...", "The .nanoqwen File Format and Safety
 // Protocols").  Here the shuffle is chosen so that one 32-bit word per lane
 // and k16-step becomes, after two masks and one shift, the four f16x2
 // registers of an m16n8k16 tensor-core A fragment; the tile's 16 scales sit

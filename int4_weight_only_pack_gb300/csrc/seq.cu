@@ -21,14 +21,23 @@ w4_status launch_gemv(const void* x, const w4_weight* w, void* y, int M, const w
                       cudaStream_t stream);
 w4_status check_gemv_args(const void* x, const w4_weight* w, const void* y, int M);
 w4_status prepare_gemv(const w4_weight* w, int M, const w4_gemv_config& c);
+
+// persistent decode-step kernel (step.cu)
+struct StepParams;
+struct StepLaunch;
+size_t step_workspace_bytes(const w4_weight* w, int n, int M);
 }  // namespace w4
+
+#include "step_launch.h"
 
 struct w4_seq {
     int n = 0, M = 0;
+    bool persistent = false;
     std::vector<w4_weight> w;
     std::vector<const void*> x;
     std::vector<void*> y;
     std::vector<w4_gemv_config> cfg;
+    w4::StepLaunch step;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
 };
@@ -36,6 +45,7 @@ struct w4_seq {
 using namespace w4;
 
 static w4_status enqueue_all(w4_seq* s, cudaStream_t stream) {
+    if (s->persistent) return step_launch(s->step, stream);
     for (int i = 0; i < s->n; ++i) {
         w4_status st = launch_gemv(s->x[i], &s->w[i], s->y[i], s->M, s->cfg[i], stream);
         if (st != W4_OK) return st;
@@ -117,10 +127,11 @@ extern "C" w4_status w4_decode_seq_create(const w4_weight* w, const void* const*
 }
 
 extern "C" w4_status w4_decode_seq_replay(w4_seq* seq, void* stream) {
-    if (!seq || !seq->exec) {
+    if (!seq || (!seq->exec && !seq->persistent)) {
         set_error("sequence is NULL or not instantiated");
         return W4_ERR_ARG;
     }
+    if (!seq->exec) return enqueue_all(seq, static_cast<cudaStream_t>(stream));
     cudaError_t e = cudaGraphLaunch(seq->exec, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch");
     return W4_OK;
@@ -136,16 +147,77 @@ extern "C" w4_status w4_decode_seq_eager(w4_seq* seq, void* stream) {
 
 extern "C" w4_status w4_decode_seq_run_host(w4_seq* seq, const void* x_host, void* x_dev, size_t x_bytes,
                                             void* y_dev, void* y_host, size_t y_bytes, void* stream) {
-    if (!seq || !seq->exec || (x_bytes && (!x_host || !x_dev)) || (y_bytes && (!y_host || !y_dev))) {
+    if (!seq || (!seq->exec && !seq->persistent) || (x_bytes && (!x_host || !x_dev)) ||
+        (y_bytes && (!y_host || !y_dev))) {
         set_error("NULL argument");
         return W4_ERR_ARG;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (x_bytes) W4_CUDA_TRY(cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, s));
-    W4_CUDA_TRY(cudaGraphLaunch(seq->exec, s));
+    w4_status st = w4_decode_seq_replay(seq, stream);
+    if (st != W4_OK) return st;
     if (y_bytes) W4_CUDA_TRY(cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, s));
     W4_CUDA_TRY(cudaStreamSynchronize(s));
     return W4_OK;
 }
 
-extern "C" int w4_decode_seq_kernels(const w4_seq* seq) { return seq ? seq->n : 0; }
+extern "C" int w4_decode_seq_kernels(const w4_seq* seq) { return seq ? (seq->persistent ? 1 : seq->n) : 0; }
+
+extern "C" size_t w4_decode_seq_workspace_bytes(const w4_weight* w, int n, int M) {
+    if (!w || n < 1 || M < 1 || M > 16) return 0;
+    for (int i = 0; i < n; ++i)
+        if (check_weight(&w[i]) != W4_OK) return 0;
+    return step_workspace_bytes(w, n, M);
+}
+
+extern "C" w4_status w4_decode_seq_create_persistent(const w4_weight* w, const void* const* x, void* const* y, int n,
+                                                     int M, void* workspace, size_t workspace_bytes, void* stream,
+                                                     w4_seq** out) {
+    clear_error();
+    if (!w || !x || !y || !out || n < 1) {
+        set_error("NULL argument or n < 1");
+        return W4_ERR_ARG;
+    }
+    *out = nullptr;
+    for (int i = 0; i < n; ++i) {
+        w4_status st = check_gemv_args(x[i], &w[i], y[i], M);
+        if (st != W4_OK) return st;
+    }
+    w4_seq* s = new w4_seq();
+    s->n = n;
+    s->M = M;
+    s->persistent = true;
+    cudaStream_t user = static_cast<cudaStream_t>(stream);
+    w4_status st = step_prepare(w, x, y, n, M, workspace, workspace_bytes, user, &s->step);
+    if (st != W4_OK) {
+        delete s;
+        return st;
+    }
+    // capture the single cooperative launch as a one-node graph
+    cudaStream_t cap = nullptr;
+    cudaError_t e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+        st = step_launch(s->step, cap);
+        cudaError_t e2 = cudaStreamEndCapture(cap, &s->graph);
+        if (st == W4_OK && e2 == cudaSuccess) e2 = cudaGraphInstantiateWithFlags(&s->exec, s->graph, 0);
+        if (st != W4_OK || e2 != cudaSuccess) {
+            // graphs without this launch: replay issues it directly
+            if (s->graph) cudaGraphDestroy(s->graph);
+            s->graph = nullptr;
+            s->exec = nullptr;
+            (void)cudaGetLastError();
+            clear_error();
+        }
+    } else {
+        (void)cudaGetLastError();
+    }
+    if (cap) cudaStreamDestroy(cap);
+    *out = s;
+    return W4_OK;
+}
+
+extern "C" int w4_decode_seq_status(const w4_seq* seq) {
+    if (!seq) return -1;
+    return seq->persistent ? step_status(seq->step) : 0;
+}

@@ -48,4 +48,17 @@ __device__ __forceinline__ void unpack_word(uint32_t v, uint32_t (&a)[4]) {
     asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(a[3]) : "r"(t3), "r"(k1_16), "r"(km72));
 }
 
+// Eight nibbles u of lane (r, c) -> four f16x2 registers holding u itself
+// as fp16 subnormals: a[0] = u * 2^-24 of row r, k 4c..4c+1; a[1] = u * 2^-20
+// (16u * 2^-24) of row r+8; a[2], a[3] the same for k 4c+2..4c+3.  Every
+// value is exact; the caller rescales rows r and r+8 by 2^24 and 2^20 and
+// subtracts 8 * sum(x) to turn u into q = u - 8.
+__device__ __forceinline__ void unpack_word_biased(uint32_t v, uint32_t (&a)[4]) {
+    const uint32_t v8 = v >> 8;
+    a[0] = v & 0x000F000Fu;
+    a[1] = v & 0x00F000F0u;
+    a[2] = v8 & 0x000F000Fu;
+    a[3] = v8 & 0x00F000F0u;
+}
+
 }  // namespace w4

@@ -9,8 +9,8 @@
  *    scale per group; model dimensions 3584 / 18944, 28 layers.
  *  - same page, "The INT8 vs. FP16 Activation Trade-off": activations stay
  *    FP16 (Path B).
- *  - "The Architecture of Modern Inference ...", ".nanoqwen Format":
- *    symmetric INT4, group 128.
+ *  - "The Architecture of Modern Inference ...", "Data Integrity and
+ *    Serialization: The .nanoqwen Format": symmetric INT4, group 128.
  * Readings where the pages are silent: q is two's-complement 4-bit, [-8, 7];
  * w = q * s; groups run along K within one output row; scales are stored
  * [N, K/128]; the sum is formed in FP64 with k ascending and rounded once

@@ -119,4 +119,5 @@ def test_default_configs_of_the_layer_shapes():
     for M in (1, 2, 4, 8, 16):
         for N, K in [(4608, 3584), (3584, 3584), (37888, 3584), (3584, 18944)]:
             c = w4.w4a16_gemv_default_config(M, N, K)
-            assert c.bands_per_cta in (1, 2, 4) and 1 <= c.splits <= 8 and 2 <= c.depth <= 96
+            assert c.bands_per_cta in (1, 2, 4) and 1 <= c.splits <= 8 and 8 <= c.depth <= 96 and c.depth % 8 == 0
+            assert c.ctas_per_sm in (1, 2)

@@ -47,7 +47,7 @@ def test_parity_default_config(M, N, K):
     assert_close(y, oracle.linear(x, q, s), "M=%d N=%d K=%d" % (M, N, K))
 
 
-CONFIGS = [(bb, sp, d) for bb, d in [(1, 2), (1, 48), (2, 5), (2, 96), (4, 16), (4, 48)]
+CONFIGS = [(bb, sp, d) for bb, d in [(1, 8), (1, 48), (2, 16), (2, 96), (4, 8), (4, 48)]
            for sp in (1, 2, 3, 5, 8)]
 
 
@@ -65,15 +65,16 @@ def test_unsupported_launch_shapes_are_rejected():
     rng = np.random.default_rng(1)
     x, q, s = rand_problem(rng, 1, 32, 256)
     packed, w = pack_on_device(q, s)
-    for cfg in [w4.GemvConfig(3, 1, 8, 1), w4.GemvConfig(1, 3, 8, 1), w4.GemvConfig(1, 1, 1, 1),
-                w4.GemvConfig(1, 9, 8, 1), w4.GemvConfig(1, 1, 200, 1)]:
+    for cfg in [w4.GemvConfig(3, 1, 8, 1), w4.GemvConfig(1, 3, 8, 1), w4.GemvConfig(1, 1, 4, 1),
+                w4.GemvConfig(1, 9, 8, 1), w4.GemvConfig(1, 1, 200, 1), w4.GemvConfig(1, 1, 12, 1),
+                w4.GemvConfig(1, 1, 8, 1, 3)]:
         with pytest.raises(w4.W4Error) as e:
             run(x, w, 32, 1, cfg)
         assert e.value.status == 7
 
 
-@pytest.mark.parametrize("bb,splits,depth", [(1, 1, 3), (1, 2, 48), (1, 8, 7), (2, 1, 48), (2, 3, 16),
-                                             (4, 1, 48), (4, 5, 8), (4, 8, 2)])
+@pytest.mark.parametrize("bb,splits,depth", [(1, 1, 8), (1, 2, 48), (1, 8, 24), (2, 1, 48), (2, 3, 16),
+                                             (4, 1, 48), (4, 5, 8), (4, 8, 48)])
 def test_every_instantiation_and_split_nt2(bb, splits, depth):
     M, N, K = 14, 72, 2304
     rng = np.random.default_rng(bb * 100 + splits * 10 + depth + 5000)
@@ -81,6 +82,16 @@ def test_every_instantiation_and_split_nt2(bb, splits, depth):
     packed, w = pack_on_device(q, s)
     cfg = w4.GemvConfig(bb, splits, depth, 0)
     assert_close(run(x, w, N, M, cfg), oracle.linear(x, q, s), "cfg %s" % ((bb, splits, depth),))
+
+
+@pytest.mark.parametrize("ctas,pdl", [(1, 1), (2, 0), (1, 0)])
+def test_launch_variants(ctas, pdl):
+    M, N, K = 5, 300, 1536
+    rng = np.random.default_rng(ctas * 10 + pdl)
+    x, q, s = rand_problem(rng, M, N, K)
+    packed, w = pack_on_device(q, s)
+    cfg = w4.GemvConfig(0, 0, 0, pdl, ctas)
+    assert_close(run(x, w, N, M, cfg), oracle.linear(x, q, s), "ctas %d pdl %d" % (ctas, pdl))
 
 
 def test_runs_are_bit_identical():

@@ -39,12 +39,26 @@ def build_chain(M, layers, rng):
     return probs, keep, ws, xs, ys
 
 
-@pytest.mark.parametrize("M,pdl", [(1, True), (1, False), (5, True), (16, True)])
-def test_replay_matches_oracle_and_single_calls(M, pdl):
-    rng = np.random.default_rng(M * 10 + pdl)
+def make_seq(ws, xs, ys, M, mode):
+    """mode: 'pdl' / 'nopdl' graph of kernels, or 'persistent' step kernel."""
+    if mode == "persistent":
+        nb = w4.w4_decode_seq_workspace_bytes(ws, M)
+        buf = torch.zeros(nb + 256, dtype=torch.uint8, device="cuda")
+        off = (-buf.data_ptr()) % 256
+        wsbuf = buf[off:off + nb]
+        seq = w4.DecodeSeq(ws, xs, ys, M, workspace=wsbuf)
+        seq._keep = buf
+        return seq
+    return w4.DecodeSeq(ws, xs, ys, M, use_pdl=(mode == "pdl"))
+
+
+@pytest.mark.parametrize("M,mode", [(1, "pdl"), (1, "nopdl"), (5, "pdl"), (16, "pdl"), (1, "persistent"),
+                                    (3, "persistent"), (8, "persistent"), (16, "persistent")])
+def test_replay_matches_oracle_and_single_calls(M, mode):
+    rng = np.random.default_rng(M * 10 + len(mode))
     probs, keep, ws, xs, ys = build_chain(M, 3, rng)
-    seq = w4.DecodeSeq(ws, xs, ys, M, use_pdl=pdl)
-    assert seq.kernels() == len(ws)
+    seq = make_seq(ws, xs, ys, M, mode)
+    assert seq.kernels() == (1 if mode == "persistent" else len(ws))
     for y in ys:
         y.fill_(0)
     seq.replay()
@@ -67,10 +81,12 @@ def test_replay_matches_oracle_and_single_calls(M, pdl):
     torch.cuda.synchronize()
     for i in range(len(ys)):
         assert np.array_equal(host(ys[i]), got[i])
+    assert seq.status() == 0
     seq.close()
 
 
-def test_run_host_copies_in_replays_and_copies_out():
+@pytest.mark.parametrize("mode", ["pdl", "persistent"])
+def test_run_host_copies_in_replays_and_copies_out(mode):
     M = 2
     rng = np.random.default_rng(3)
     shapes = MINI * 2
@@ -90,7 +106,7 @@ def test_run_host_copies_in_replays_and_copies_out():
         probs.append((x, q, s))
         xo += nx
         yo += ny
-    seq = w4.DecodeSeq(ws, xs, ys, M)
+    seq = make_seq(ws, xs, ys, M, mode)
     x_host = torch.from_numpy(np.concatenate([p[0].ravel() for p in probs]).view(np.int16)).pin_memory()
     y_host = torch.zeros(sum(ysz), dtype=torch.int16).pin_memory()
     stream = torch.cuda.current_stream()
@@ -105,9 +121,10 @@ def test_run_host_copies_in_replays_and_copies_out():
 
 def test_full_decode_step_sampled():
     """28 layers x 4 projections at M = 1 with distinct seeded weights (the
-    benchmark's workload and launch configuration), one graph replay; every
-    projection of layers 0 and 27 and one projection of every other layer is
-    checked on sampled rows."""
+    benchmark's workload), as a graph of per-projection kernels and as the
+    persistent step kernel (the benchmark's launch configuration), each
+    replayed twice; every projection of layers 0 and 27 and one projection of
+    every other layer is checked on sampled rows."""
     M, CONFIG = 1, 3
     keep, ws, xs, ys, meta = [], [], [], [], []
     for layer in range(28):
@@ -120,9 +137,19 @@ def test_full_decode_step_sampled():
             xs.append(dev(x))
             ys.append(torch.zeros((M, N), dtype=torch.int16, device="cuda"))
             meta.append((layer, pid, N, K, x))
-    seq = w4.DecodeSeq(ws, xs, ys, M, use_pdl=True)
-    seq.replay()
-    torch.cuda.synchronize()
+    for mode in ("pdl", "persistent"):
+        for y in ys:
+            y.zero_()
+        seq = make_seq(ws, xs, ys, M, mode)
+        seq.replay()
+        seq.replay()
+        torch.cuda.synchronize()
+        assert seq.status() == 0
+        check_step(meta, ys, CONFIG, M)
+        seq.close()
+
+
+def check_step(meta, ys, CONFIG, M):
     rng = np.random.default_rng(11)
     for i, (layer, pid, N, K, x) in enumerate(meta):
         if layer not in (0, 27) and pid != layer % 4:
@@ -130,4 +157,3 @@ def test_full_decode_step_sampled():
         rows = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 24)]))
         ref, _ = oracle_rows(CONFIG, layer, pid, M, N, K, rows, x_bits=x)
         assert_close(host(ys[i])[:, rows], ref, "layer %d proj %d" % (layer, pid))
-    seq.close()
