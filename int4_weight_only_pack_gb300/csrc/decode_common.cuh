@@ -60,9 +60,10 @@ __host__ __device__ constexpr int xsum_bytes(int Gs) { return Gs * 16 * 4; }
 // gl, k 4c + 2(e & 1) .. +1 -- with rows M..MP-1 zero, and the sum of x over
 // every group and token into xsum[gl*16 + m] (0 for m >= M).  Called by the
 // consumer threads only; returns with all of them synchronised.
-template <int MP>
+template <int MP, int NCONS = kConsumers>
 __device__ __forceinline__ void stage_x(const uint32_t* x, int M, int K, int g_lo, int Gs, uint32_t* xs,
                                         float* xsum) {
+    constexpr int kConsumers = NCONS, kConsumerWarps = NCONS / 32;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int per_row = Gs * 64;  // fp16 pairs of this K range
     const uint32_t* xg = x + (size_t)g_lo * 64;
@@ -109,6 +110,49 @@ __device__ __forceinline__ void stage_x(const uint32_t* x, int M, int K, int g_l
         if (lane == 0) xsum[gl * 16 + m] = sum;
     }
     tc::named_barrier(1, kConsumers);
+}
+
+// The same staging as stage_x, with every word copied from global memory
+// straight into its fragment slot by a 4-byte cp.async, all issued before any
+// is waited for: one memory round trip whatever the slice size.
+template <int MP, int NCONS>
+__device__ __forceinline__ void stage_x_async(const uint32_t* x, int M, int K, int g_lo, int Gs, uint32_t* xs,
+                                              float* xsum) {
+    constexpr int kWarps = NCONS / 32;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int per_row = Gs * 64;
+    const uint32_t* xg = x + (size_t)g_lo * 64;
+    const int kp = K / 2;
+    const uint32_t xs_s = tc::smem_addr(xs);
+    for (int m = 0; m < MP; ++m) {
+        for (int r = tid; r < per_row; r += NCONS) {
+            const int gl = r >> 6, kk2 = r & 63;
+            const int j = kk2 >> 3, c = (kk2 >> 1) & 3, hi = kk2 & 1;
+            const int dst = gl * (MP * 64) + (j >> 1) * (MP * 16) + (m * 4 + c) * 4 + (j & 1) * 2 + hi;
+            if (m < M)
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(xs_s + 4u * dst),
+                             "l"(xg + (size_t)m * kp + r)
+                             : "memory");
+            else
+                xs[dst] = 0;
+        }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    for (int idx = tid; idx < Gs * 16; idx += NCONS)
+        if ((idx & 15) >= M) xsum[idx] = 0.f;
+    tc::named_barrier(1, NCONS);
+    for (int idx = warp; idx < Gs * M; idx += kWarps) {
+        const int gl = idx / M, m = idx - gl * M;
+        const int q = lane >> 3, c = (lane >> 1) & 3, e = (lane & 1) * 2;
+        const uint32_t* src = xs + gl * (MP * 64) + q * (MP * 16) + (m * 4 + c) * 4 + e;
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(src));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(src + 1));
+        float sum = (f0.x + f0.y) + (f1.x + f1.y);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+        if (lane == 0) xsum[gl * 16 + m] = sum;
+    }
+    tc::named_barrier(1, NCONS);
 }
 
 // Per-lane state of the tile multiply-accumulate.
@@ -180,13 +224,16 @@ struct TileMac {
 
 // Shared-memory floats of one buffer of per-warp block partials:
 // [warp][band][nt][lane][4].
-__host__ __device__ constexpr int red_floats(int BB, int NT) { return kConsumerWarps * BB * NT * 128; }
+__host__ __device__ constexpr int red_floats(int BB, int NT, int warps = kConsumerWarps) {
+    return warps * BB * NT * 128;
+}
 
 // Fixed-order sum over the consumer warps of the block partials for the
 // outputs t = tid + i * kConsumers < nb*16*M (t = m * nb*16 + band row);
 // NaN where !ok.
-template <int NT>
+template <int NT, int NCONS = kConsumers>
 __device__ __forceinline__ void block_sums(const float* red, int BB, int nb, int M, bool ok, float (&v)[4]) {
+    constexpr int kConsumers = NCONS, kConsumerWarps = NCONS / 32;
     const int Tout = nb * 16 * M;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {

@@ -51,24 +51,25 @@ struct StepOp {
 
 namespace {
 
-using dec::kChunk;
-using dec::kConsumers;
-using dec::kConsumerWarps;
-constexpr int kThreads = kConsumers + 32;
-constexpr int kRing = 48;  // tiles in flight per CTA
-
-
+constexpr int kWarps = 16;              // consumer warps
+constexpr int kCons = kWarps * 32;      // consumer threads
+constexpr int kSlot = kWarps;           // tiles per ring slot: one per consumer warp
+constexpr int kThreads = kCons + 32;    // + one producer warp
+constexpr int kQueue = 32;              // block-queue entries
+constexpr int kSmemBudget = 225 * 1024; // one CTA per SM
 
 struct StepSmem {
-    int bar, flag, x, xsum, red, total;
-    __host__ __device__ StepSmem(int MP, int gpc_max, int bb_max) {
-        const int nslots = kRing / kChunk;
-        bar = kRing * kTileBytes;
-        flag = bar + 2 * nslots * 8;
+    int ring, nslots, bar, queue, flag, x, xsum, red, total;
+    __host__ __device__ StepSmem(int ring_tiles, int MP, int gpc_max, int bb_max) {
+        ring = ring_tiles;
+        nslots = ring_tiles / kSlot;
+        bar = ring_tiles * kTileBytes;                        // ring of 16-tile slots first
+        queue = bar + (2 * nslots + 2 * kQueue) * 8;          // full/empty per slot, queue full/empty
+        flag = queue + kQueue * 4;
         x = (flag + 16 + 127) & ~127;
         xsum = x + dec::x_bytes(MP, gpc_max);
         red = xsum + dec::xsum_bytes(gpc_max);
-        total = red + 2 * dec::red_floats(bb_max, (MP + 7) / 8) * 4;
+        total = red + 2 * dec::red_floats(bb_max, (MP + 7) / 8, kWarps) * 4;
     }
 };
 
@@ -78,53 +79,80 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
     return v;
 }
 
+// The share of projection `o` that CTA c takes without contention: blocks
+// g, g + cps, ... (g = c / S) up to floor(nblocks / cps) of them; the rest are
+// handed out by the per-split counter.
+__device__ __forceinline__ int static_blocks(const StepOp& o, int cps) { return o.nblocks / cps; }
+
 template <int MP>
-__global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
+__global__ void __launch_bounds__(kThreads, 1) step_kernel(StepParams p) {
     constexpr int NT = (MP + 7) / 8;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NC = gridDim.x, c = blockIdx.x;
     const int M = p.M;
-    constexpr int nslots = kRing / kChunk;
-    const StepSmem L(MP, p.gpc_max, p.bb_max);
+    const StepSmem L(p.ring, MP, p.gpc_max, p.bb_max);
+    const int nslots = L.nslots;
     const uint32_t sbase = tc::smem_addr(smem);
-    const uint32_t full0 = sbase + L.bar, empty0 = full0 + 8 * nslots;
+    const uint32_t full0 = sbase + L.bar, empty0 = full0 + 8 * nslots, qfull0 = empty0 + 8 * nslots,
+                   qempty0 = qfull0 + 8 * kQueue;
+    volatile int* queue = reinterpret_cast<volatile int*>(smem + L.queue);
     volatile int* flag = reinterpret_cast<volatile int*>(smem + L.flag);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nslots; ++s) {
             tc::mbar_init(full0 + 8 * s, 1);
-            tc::mbar_init(empty0 + 8 * s, kConsumerWarps);
+            tc::mbar_init(empty0 + 8 * s, kWarps);
+        }
+        for (int q = 0; q < kQueue; ++q) {
+            tc::mbar_init(qfull0 + 8 * q, 1);
+            tc::mbar_init(qempty0 + 8 * q, 1);
         }
         tc::mbar_init_fence();
     }
     __syncthreads();
 
-    if (warp == kConsumerWarps) {
-        // ---- producer: every projection's tiles, back to back --------------------
+    if (warp == kWarps) {
+        // ---- producer: pick blocks, publish them, stream their tiles ---------------
         if (lane == 0) {
-            int slot = 0;
-            uint32_t use = 0, issued = 0;
+            int slot = 0, qs = 0;
+            uint32_t use = 0, quse = 0, issued = 0;
             bool ok = true;
             for (int i = 0; i < p.nops && ok; ++i) {
                 const StepOp o = p.ops[i];
-                const int r = c % o.S, cps = NC / o.S;
+                const int r = c % o.S, cps = NC / o.S, g = c / o.S;
                 const int g_lo = (int)(((long long)o.G * r) / o.S);
                 const int Gs = (int)(((long long)o.G * (r + 1)) / o.S) - g_lo;
-                for (int blk = c / o.S; blk < o.nblocks && ok; blk += cps) {
+                const int nstatic = static_blocks(o, cps);
+                for (int k = 0; ok; ++k) {
+                    int blk = k < nstatic ? g + k * cps
+                                          : nstatic * cps + (int)atomicAdd(p.sched + i * 8 + r, 1u);
+                    if (blk >= o.nblocks) blk = -1;
+                    if (quse > 0 && !tc::mbar_wait(qempty0 + 8 * qs, (quse - 1) & 1)) {
+                        atomicOr(p.status, 1);
+                        ok = false;
+                        break;
+                    }
+                    queue[qs] = blk;
+                    tc::mbar_arrive(qfull0 + 8 * qs);  // release: the entry is visible to the waiters
+                    if (++qs == kQueue) {
+                        qs = 0;
+                        ++quse;
+                    }
+                    if (blk < 0) break;
                     const int band0 = blk * o.BB;
                     const int T = min(o.BB, o.bands - band0) * Gs;
                     int bb = 0, gl = 0;
-                    for (int t0 = 0; t0 < T; t0 += kChunk) {
+                    for (int t0 = 0; t0 < T; t0 += kSlot) {
                         if (use > 0 && !tc::mbar_wait(empty0 + 8 * slot, (use - 1) & 1)) {
                             atomicOr(p.status, 1);
                             ok = false;
                             break;
                         }
-                        const int n = min(kChunk, T - t0);
+                        const int n = min(kSlot, T - t0);
                         const uint32_t bar = full0 + 8 * slot;
                         tc::mbar_arrive_expect_tx(bar, (uint32_t)n * kTileBytes);
-                        uint32_t dst = sbase + (uint32_t)slot * (kChunk * kTileBytes);
+                        uint32_t dst = sbase + (uint32_t)slot * (kSlot * kTileBytes);
                         for (int left = n; left > 0;) {
                             const int run = min(left, Gs - gl);
                             const uint8_t* src = o.w + ((size_t)(band0 + bb) * o.G + g_lo + gl) * kTileBytes;
@@ -153,8 +181,8 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
         __syncwarp();
     } else {
         // ---- consumers ----------------------------------------------------------------
-        int slot = 0;
-        uint32_t use = 0;
+        int slot = 0, qs = 0;
+        uint32_t use = 0, quse = 0;
         int kblk = 0;
         bool ok = true;
         uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L.x);
@@ -162,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
         float* red_base = reinterpret_cast<float*>(smem + L.red);
         for (int i = 0; i < p.nops; ++i) {
             const StepOp o = p.ops[i];
-            const int r = c % o.S, cps = NC / o.S;
+            const int r = c % o.S;
             const int g_lo = (int)(((long long)o.G * r) / o.S);
             const int Gs = (int)(((long long)o.G * (r + 1)) / o.S) - g_lo;
             const int BB = o.BB;
@@ -177,13 +205,27 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
                         }
                     }
                 }
-                tc::named_barrier(1, kConsumers);
+                tc::named_barrier(1, kCons);
             }
-            dec::stage_x<MP>(o.x, M, o.K, g_lo, Gs, xs, xsum);
+            dec::stage_x_async<MP, kCons>(o.x, M, o.K, g_lo, Gs, xs, xsum);
             dec::TileMac<MP> mac(sbase + L.x, sbase + L.xsum, lane);
-            const int red_buf = dec::red_floats(BB, NT);
+            const int red_buf = dec::red_floats(BB, NT, kWarps);
 
-            for (int blk = c / o.S; blk < o.nblocks; blk += cps, ++kblk) {
+            while (true) {
+                if (!tc::mbar_wait(qfull0 + 8 * qs, quse & 1)) {
+                    atomicOr(p.status, 8);
+                    ok = false;
+                }
+                const int blk = ok ? queue[qs] : -1;
+                if (blk < 0) {
+                    tc::named_barrier(1, kCons);  // everyone has read the entry
+                    if (threadIdx.x == 0) tc::mbar_arrive(qempty0 + 8 * qs);
+                    if (++qs == kQueue) {
+                        qs = 0;
+                        ++quse;
+                    }
+                    break;
+                }
                 const int band0 = blk * BB;
                 const int nb = min(BB, o.bands - band0);
                 const int T = nb * Gs;
@@ -197,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
                 int cur_bb = 0, band_end = Gs;
-                for (int t0 = 0; t0 < T; t0 += kChunk) {
+                for (int t0 = 0; t0 < T; t0 += kSlot) {
                     if (ok && !tc::mbar_wait(full0 + 8 * slot, use & 1)) {
                         atomicOr(p.status, 4);
                         ok = false;
@@ -216,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
                             ++cur_bb;
                             band_end += Gs;
                         }
-                        mac.run(sbase + (uint32_t)slot * (kChunk * kTileBytes) + (uint32_t)warp * kTileBytes,
+                        mac.run(sbase + (uint32_t)slot * (kSlot * kTileBytes) + (uint32_t)warp * kTileBytes,
                                 t - cur_bb * Gs, lane, acc);
                     }
                     __syncwarp();
@@ -229,14 +271,20 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
                     myred[(cur_bb * NT + nt) * 32] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-                tc::named_barrier(1, kConsumers);
+                tc::named_barrier(1, kCons);
+                // every consumer has read this block's queue entry: free it
+                if (threadIdx.x == 0) tc::mbar_arrive(qempty0 + 8 * qs);
+                if (++qs == kQueue) {
+                    qs = 0;
+                    ++quse;
+                }
                 const int Tout = nb * 16 * M;
                 float v[4];
-                dec::block_sums<NT>(red, BB, nb, M, blk_ok0 && ok, v);
+                dec::block_sums<NT, kCons>(red, BB, nb, M, blk_ok0 && ok, v);
                 if (o.S == 1) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int t = threadIdx.x + q * kConsumers;
+                        const int t = threadIdx.x + q * kCons;
                         if (t < Tout) {
                             const int m = t / (nb * 16), rl = t - m * (nb * 16);
                             const int n = band0 * 16 + rl;
@@ -250,22 +298,22 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
                     float* mine = o.part + ((size_t)blk * o.S + r) * pb;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int t = threadIdx.x + q * kConsumers;
+                        const int t = threadIdx.x + q * kCons;
                         if (t < Tout) mine[t] = v[q];
                     }
                     __threadfence();
-                    tc::named_barrier(1, kConsumers);
+                    tc::named_barrier(1, kCons);
                     if (threadIdx.x == 0) *flag = (atomicAdd(o.cnt + blk, 1u) == (unsigned)(o.S - 1));
-                    tc::named_barrier(1, kConsumers);
+                    tc::named_barrier(1, kCons);
                     if (*flag) {
                         __threadfence();
                         const float* base = o.part + (size_t)blk * o.S * pb;
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const int t = threadIdx.x + q * kConsumers;
+                            const int t = threadIdx.x + q * kCons;
                             if (t < Tout) {
                                 float sum = 0.f;
-                                for (int s = 0; s < o.S; ++s) sum += __ldcg(base + (size_t)s * pb + t);
+                                for (int s2 = 0; s2 < o.S; ++s2) sum += __ldcg(base + (size_t)s2 * pb + t);
                                 const int m = t / (nb * 16), rl = t - m * (nb * 16);
                                 const int n = band0 * 16 + rl;
                                 if (n < o.N) o.y[(size_t)m * o.N + n] = __half_as_ushort(__float2half_rn(sum));
@@ -274,17 +322,19 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p) {
                         if (threadIdx.x == 0) o.cnt[blk] = 0;  // ready for the next step
                     }
                 }
+                ++kblk;
             }
             // this CTA is done with projection i: its y (and partials) are visible
             __threadfence();
-            tc::named_barrier(1, kConsumers);
+            tc::named_barrier(1, kCons);
             if (threadIdx.x == 0) atomicAdd(p.done + i, 1u);
         }
-        // the last CTA out resets the completion counters for the next step
+        // the last CTA out resets the counters for the next step
         if (threadIdx.x == 0) {
             __threadfence();
             if (atomicAdd(p.exit_cnt, 1u) == (unsigned)(NC - 1)) {
                 for (int i = 0; i < p.nops; ++i) p.done[i] = 0;
+                for (int i = 0; i < 8 * p.nops; ++i) p.sched[i] = 0;
                 *p.exit_cnt = 0;
                 __threadfence();
             }
@@ -311,53 +361,43 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 // ---- host-side plan ---------------------------------------------------------------
 struct StepPlan {
-    int MP = 1, NC = 0, gpc_max = 1, bb_max = 1, smem = 0;
+    int MP = 1, NC = 0, gpc_max = 1, bb_max = 1, ring = 0, smem = 0;
     std::vector<StepOp> ops;  // device pointers filled against a workspace base
-    size_t table_off = 0, done_off = 0, exit_off = 0, status_off = 0, total = 0;
+    size_t table_off = 0, done_off = 0, exit_off = 0, status_off = 0, sched_off = 0, total = 0;
     std::vector<size_t> cnt_off, part_off;
 };
 
-// Choose each projection's K split and block size for a persistent grid of
-// NC CTAs (S must divide NC) and lay out the workspace.
+// Per projection: one band per block (the block queue balances the tail) and
+// the smallest K split (dividing NC) whose x slice fits 48 KB; the ring takes
+// the rest of the shared memory.  Lays out the workspace.
 static void plan_step(const w4_weight* w, int n, int M, int NC, StepPlan* pl) {
     pl->MP = padded(M);
     pl->NC = NC;
     pl->ops.assign(n, StepOp{});
     pl->cnt_off.assign(n, 0);
     pl->part_off.assign(n, 0);
-    const int budget = 110 * 1024;  // two CTAs per SM
-    // first pass: per projection, the lowest-cost (S, BB) whose x slice fits
-    std::vector<int> S_of(n), BB_of(n);
+    std::vector<int> S_of(n);
     for (int i = 0; i < n; ++i) {
-        const int G = (int)(w[i].K / kGroupK), bands = (int)num_bands(w[i].N);
-        double best = 1e30;
-        int bS = 8, bBB = 1;
-        for (int S = 1; S <= 8; S *= 2) {
-            if (S > G || NC % S) break;
-            const int Gs = (G + S - 1) / S, cps = NC / S;
-            for (int BB = 1; BB <= 4; BB *= 2) {
-                if (StepSmem(pl->MP, Gs, BB).total > budget) continue;
-                const int nblocks = (bands + BB - 1) / BB;
-                const double waves = (double)((nblocks + cps - 1) / cps);
-                const double cost = waves * (double)((BB * Gs + kChunk - 1) / kChunk + 2) * (S > 1 ? 1.15 : 1.0);
-                if (cost < best - 1e-9) {
-                    best = cost;
-                    bS = S;
-                    bBB = BB;
-                }
-            }
-        }
-        S_of[i] = bS;
-        BB_of[i] = bBB;
-        pl->gpc_max = std::max(pl->gpc_max, (G + bS - 1) / bS);
-        pl->bb_max = std::max(pl->bb_max, bBB);
+        const int G = (int)(w[i].K / kGroupK);
+        int S = 1;
+        while (S < 8 && 2 * S <= G && NC % (2 * S) == 0 &&
+               dec::x_bytes(pl->MP, (G + S - 1) / S) + dec::xsum_bytes((G + S - 1) / S) > 48 * 1024)
+            S *= 2;
+        S_of[i] = S;
+        pl->gpc_max = std::max(pl->gpc_max, (G + S - 1) / S);
     }
-    pl->smem = StepSmem(pl->MP, pl->gpc_max, pl->bb_max).total;
+    pl->bb_max = 1;
+    int ring = 192;
+    while (ring > kSlot && StepSmem(ring, pl->MP, pl->gpc_max, pl->bb_max).total > kSmemBudget) ring -= kSlot;
+    pl->ring = ring;
+    pl->smem = StepSmem(ring, pl->MP, pl->gpc_max, pl->bb_max).total;
     size_t off = 0;
     pl->table_off = off;
     off = align_up(off + sizeof(StepOp) * n);
     pl->done_off = off;
     off = align_up(off + sizeof(unsigned) * n);
+    pl->sched_off = off;
+    off = align_up(off + sizeof(unsigned) * 8 * n);
     pl->exit_off = off;
     pl->status_off = off + 16;
     off = align_up(off + 32);
@@ -368,8 +408,8 @@ static void plan_step(const w4_weight* w, int n, int M, int NC, StepPlan* pl) {
         o.G = (int)(w[i].K / kGroupK);
         o.bands = (int)num_bands(w[i].N);
         o.S = S_of[i];
-        o.BB = BB_of[i];
-        o.nblocks = (o.bands + o.BB - 1) / o.BB;
+        o.BB = 1;
+        o.nblocks = o.bands;
         if (o.S > 1) {
             pl->cnt_off[i] = off;
             off = align_up(off + sizeof(unsigned) * o.nblocks);
@@ -380,17 +420,6 @@ static void plan_step(const w4_weight* w, int n, int M, int NC, StepPlan* pl) {
     pl->total = off;
 }
 
-static int step_grid(int MP, int smem) {
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    StepFn fn = step_fn(MP);
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess) return 0;
-    if (per_sm < 1) return 0;
-    return sms * std::min(per_sm, 2);
-}
-
 static int sm_count_now() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -399,31 +428,30 @@ static int sm_count_now() {
     return sms;
 }
 
-// Workspace bytes for either grid size the launcher may pick (one or two
-// CTAs per SM).
+// One resident CTA per SM, or 0 if the kernel cannot be resident.
+static int step_grid(int MP, int smem) {
+    int per_sm = 0;
+    StepFn fn = step_fn(MP);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess) return 0;
+    return per_sm >= 1 ? sm_count_now() : 0;
+}
+
 size_t step_workspace_bytes(const w4_weight* w, int n, int M) {
-    const int sms = sm_count_now();
-    StepPlan a, b;
-    plan_step(w, n, M, sms, &a);
-    plan_step(w, n, M, 2 * sms, &b);
-    return std::max(a.total, b.total);
+    StepPlan pl;
+    plan_step(w, n, M, sm_count_now(), &pl);
+    return pl.total;
 }
 
 w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y, int n, int M, void* ws,
                        size_t ws_bytes, cudaStream_t stream, StepLaunch* out) {
     const int MP = padded(M);
-    // grid: two CTAs per SM when the worst shared-memory need allows it
-    StepPlan probe;
-    plan_step(w, n, M, 2 * sm_count_now(), &probe);
-    const int NC = step_grid(MP, probe.smem);
-    if (NC <= 0) {
-        set_error("the persistent step kernel cannot be resident (shared memory %d bytes)", probe.smem);
-        return W4_ERR_UNSUPPORTED;
-    }
     StepPlan pl;
-    plan_step(w, n, M, NC, &pl);
-    if (step_grid(MP, pl.smem) < NC) {
-        set_error("the persistent step kernel cannot keep %d CTAs resident", NC);
+    plan_step(w, n, M, sm_count_now(), &pl);
+    const int NC = step_grid(MP, pl.smem);
+    if (NC <= 0 || NC != pl.NC || pl.ring < 2 * kSlot) {
+        set_error("the persistent step kernel cannot be resident (shared memory %d bytes, ring %d tiles)",
+                  pl.smem, pl.ring);
         return W4_ERR_UNSUPPORTED;
     }
     if (!ws || ws_bytes < pl.total) {
@@ -456,9 +484,11 @@ w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y,
     p.M = M;
     p.done = reinterpret_cast<unsigned*>(base + pl.done_off);
     p.exit_cnt = reinterpret_cast<unsigned*>(base + pl.exit_off);
+    p.sched = reinterpret_cast<unsigned*>(base + pl.sched_off);
     p.status = reinterpret_cast<int*>(base + pl.status_off);
     p.gpc_max = pl.gpc_max;
     p.bb_max = pl.bb_max;
+    p.ring = pl.ring;
     return W4_OK;
 }
 
@@ -471,7 +501,7 @@ int step_status(const StepLaunch& s) {
 w4_status step_launch(const StepLaunch& s, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)s.NC, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);  // 16 consumer warps + the producer warp
     cfg.dynamicSmemBytes = (size_t)s.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr;

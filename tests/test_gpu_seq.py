@@ -66,10 +66,14 @@ def test_replay_matches_oracle_and_single_calls(M, mode):
     got = [host(y).copy() for y in ys]
     for i, (x, q, s) in enumerate(probs):
         assert_close(got[i], oracle.linear(x, q, s), "projection %d" % i)
-        single = torch.zeros_like(ys[i])
-        w4.w4a16_gemv(xs[i], ws[i], single, M)
-        torch.cuda.synchronize()
-        assert np.array_equal(host(single), got[i])
+        if mode != "persistent":
+            # same kernel and launch shape as a single call: same bits.  (The
+            # persistent kernel may split K differently, so only the oracle
+            # tolerance and its own run-to-run identity apply to it.)
+            single = torch.zeros_like(ys[i])
+            w4.w4a16_gemv(xs[i], ws[i], single, M)
+            torch.cuda.synchronize()
+            assert np.array_equal(host(single), got[i])
     for y in ys:
         y.fill_(0)
     seq.eager()
