@@ -108,13 +108,13 @@ class ClockSampler:
 
 
 # ---- workload -----------------------------------------------------------------
-def build_step(torch, w4, synth, M: int):
-    """Packed weights of 28 layers (device-generated, device-packed), x and y
-    arenas, and the captured sequence."""
+def build_step(torch, w4, synth, M: int, layers: int = LAYERS):
+    """Packed weights of `layers` layers (device-generated, device-packed), x
+    and y arenas, and the captured sequence."""
     dev = torch.device("cuda")
     ws, keep, meta = [], [], []
     x_host_parts, xsz, ysz = [], [], []
-    for layer in range(LAYERS):
+    for layer in range(layers):
         for pid, (_, N, K) in enumerate(LAYER):
             G = K // 128
             q = torch.empty((N, K), dtype=torch.int8, device=dev)
@@ -156,7 +156,7 @@ def time_replays(torch, fn, reps: int) -> float:
 
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
-    for name in ("gemv.cu", "w4_internal.cuh", "w4_device.cuh", "tc_ptx.cuh"):
+    for name in ("step.cu", "step_launch.h", "decode_common.cuh", "w4_internal.cuh", "w4_device.cuh", "tc_ptx.cuh"):
         with open(os.path.join(ROOT, "int4_weight_only_pack_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -337,6 +337,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-extras", action="store_true",
                     help="time the step only (no clock soak, e2e, side measurements or CPU baseline): for profilers")
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="with --no-extras: a step of the first L layers only (a small case for a profiler; "
+                         "prints a profiler line, not the benchmark line)")
     ap.add_argument("--profile-projection", choices=[n for n, _, _ in LAYER], default=None,
                     help="launch one projection of layer 0 (M=1, library launch shape) --steps times: a small "
                          "case for a profiler")
@@ -364,7 +367,8 @@ def main():
         dist.barrier()
     torch.cuda.set_device(local)
     M = 1
-    st = build_step(torch, w4, synth, M)
+    layers = max(1, min(args.layers, LAYERS)) if args.no_extras else LAYERS
+    st = build_step(torch, w4, synth, M, layers)
     nbw = w4.w4_decode_seq_workspace_bytes(st["ws"], M)
     ws_buf = torch.zeros(nbw + 256, dtype=torch.uint8, device="cuda")
     ws_off = (-ws_buf.data_ptr()) % 256
@@ -398,6 +402,14 @@ def main():
         t = torch.tensor([ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
+    if layers != LAYERS:
+        nb = BYTES_PER_STEP // LAYERS * layers
+        if rank == 0:
+            print(json.dumps({"profile_case": "decode step of the first %d layers, M=1" % layers,
+                              "bytes_per_step": nb, "us_per_step": ms * 1e3, "GB/s": nb / (ms * 1e-3) / 1e9,
+                              "status_word": seq.status()}), flush=True)
+        seq.close()
+        return 0
     value = world * BYTES_PER_STEP / (ms * 1e-3) / 1e9
     per_gpu = BYTES_PER_STEP / (ms * 1e-3) / 1e9
     launches = seq.kernels()
@@ -474,7 +486,7 @@ def main():
                            "bytes_per_step": BYTES_PER_STEP, "accumulate": "f32",
                            "l2": "inputs larger than L2: 3.36 GB of weights per step vs 129 MB L2",
                            "launch": "one cudaGraphLaunch per step of a one-node graph: the persistent "
-                                     "cooperative decode-step kernel (2 CTAs/SM)",
+                                     "cooperative decode-step kernel (one CTA per SM)",
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "roofline": roof,
                 "cpu_baseline": cpu,

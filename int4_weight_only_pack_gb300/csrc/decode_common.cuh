@@ -220,6 +220,65 @@ struct TileMac {
             acc[nt][3] = fmaf(cb, X.y, fmaf(sb, pe[nt][3] + po[nt][3], acc[nt][3]));
         }
     }
+
+    // The same for NTL consecutive tiles at ta, ta + 1056, ... (groups gl,
+    // gl + 1, ... of one band), their MMA chains interleaved.  The tiles are
+    // added to acc in order, so the result equals NTL calls of run().
+    template <int NTL>
+    __device__ __forceinline__ void run_tiles(uint32_t ta, int gl, int lane, float (&acc)[NT][4]) {
+        uint32_t wd[NTL][8], sc[NTL];
+#pragma unroll
+        for (int n = 0; n < NTL; ++n) {
+            const uint32_t tn = ta + (uint32_t)(n * kTileBytes);
+            const uint4 lo = lds128(tn + 16 * lane), hi = lds128(tn + 512 + 16 * lane);
+            wd[n][0] = lo.x, wd[n][1] = lo.y, wd[n][2] = lo.z, wd[n][3] = lo.w;
+            wd[n][4] = hi.x, wd[n][5] = hi.y, wd[n][6] = hi.z, wd[n][7] = hi.w;
+            sc[n] = lds32(tn + kScaleOffset + 4 * (lane >> 2));
+        }
+        const uint32_t xa0 = xfrag + (uint32_t)gl * (MP * 256);
+        float pe[NTL][NT][4], po[NTL][NT][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // k16 steps 2q (even chain) and 2q + 1 (odd chain)
+#pragma unroll
+            for (int n = 0; n < NTL; ++n) {
+                uint4 v[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    v[nt] = xlane ? lds128(xa0 + (uint32_t)(n * MP * 256 + q * MP * 64 + nt * 512))
+                                  : make_uint4(0, 0, 0, 0);
+                uint32_t a[4], b[4];
+                unpack_word_biased(wd[n][2 * q], a);
+                unpack_word_biased(wd[n][2 * q + 1], b);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (q == 0) {
+                        mma16816_zero(pe[n][nt], a, v[nt].x, v[nt].y);
+                        mma16816_zero(po[n][nt], b, v[nt].z, v[nt].w);
+                    } else {
+                        mma16816(pe[n][nt], a, v[nt].x, v[nt].y);
+                        mma16816(po[n][nt], b, v[nt].z, v[nt].w);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < NTL; ++n) {
+            const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sc[n]));
+            const float sa = sf.x * 16777216.f, sb = sf.y * 1048576.f;
+            const float ca = -8.f * sf.x, cb = -8.f * sf.y;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float2 X;
+                asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];"
+                             : "=f"(X.x), "=f"(X.y)
+                             : "r"(xsum + (uint32_t)(((gl + n) * 16 + nt * 8) * 4)));
+                acc[nt][0] = fmaf(ca, X.x, fmaf(sa, pe[n][nt][0] + po[n][nt][0], acc[nt][0]));
+                acc[nt][1] = fmaf(ca, X.y, fmaf(sa, pe[n][nt][1] + po[n][nt][1], acc[nt][1]));
+                acc[nt][2] = fmaf(cb, X.x, fmaf(sb, pe[n][nt][2] + po[n][nt][2], acc[nt][2]));
+                acc[nt][3] = fmaf(cb, X.y, fmaf(sb, pe[n][nt][3] + po[n][nt][3], acc[nt][3]));
+            }
+        }
+    }
 };
 
 // Shared-memory floats of one buffer of per-warp block partials:

@@ -6,31 +6,41 @@
 // CUDA Graphs").  On GB300 each separate projection kernel still pays a ramp
 // up (first bytes in flight), a drain (the last CTA) and a grid completion at
 // every boundary; over 112 projections of 1 to 10 microseconds of streaming
-// that is most of the step.  Here one persistent grid (two CTAs per SM)
-// streams the weights of every projection back to back:
+// that is most of the step.  Here one persistent grid (one CTA per SM)
+// streams the weights of every projection back to back.
 //
-//  * The producer lane of each CTA walks the projections in order and streams
-//    the tiles of its work blocks into a shared-memory ring (cp.async.bulk,
-//    8 tiles per slot) without ever waiting on the dependency chain: weights
-//    do not depend on activations, so the ring fills with the next
-//    projection's weights while the consumers finish the current one.
-//  * Consumers of projection i wait until every CTA has finished projection
-//    i - 1 (a completion counter in the workspace, read with acquire
-//    semantics), then stage x_i and compute exactly as the single-projection
-//    kernel does (same tile arithmetic, same fixed-order block reduction).
-//    This honours the data dependency of a real decode step, where x_i is
-//    computed from y_(i-1).
-//  * A K split (when a projection has too few bands to balance) writes FP32
-//    block partials to the workspace; the CTA whose arrival completes a block
-//    adds the partials in split order (deterministic) and writes y.
-//  * Counters reset themselves (the last arriver of a block, the last CTA of
+// Work split.  Projection i is cut into units: (16-row band, K split) pairs.
+// The CTAs of K split r (c % S == r) share its bands in contiguous runs, and
+// the tiles of a CTA's run (band-major, then group) are cut into 16 equal
+// contiguous ranges, one per warp.  So every warp streams one contiguous run
+// of tiles per projection and sums its bands in registers:
+//
+//  * Each warp owns a ring of R slots of up to 4 tiles in shared memory and
+//    issues its own bulk copies (one cp.async.bulk and one mbarrier per slot;
+//    a slot never crosses the end of a band's run of tiles).  Its copy
+//    cursor walks its ranges of all projections in order and never waits on
+//    the dependency chain (weights do not depend on activations), so while a
+//    warp waits for projection i's input, the copies of its next tiles,
+//    of projection i+1 onwards, are already in flight.  A slot is refilled
+//    as soon as the warp has consumed it: no cross-warp handshake per tile.
+//  * Before projection i the CTA waits until every CTA has finished
+//    projection i - 1 (a completion counter, read with acquire semantics),
+//    then stages x_i: x_i may be computed from y_(i-1) in a real decode step.
+//  * A band whose tiles all fall in one warp's range is finished by that warp
+//    straight from its accumulators.  A band cut between warps is parked in
+//    shared memory by each and summed, in warp order, by one warp after a CTA
+//    barrier.  A band split in K (S > 1) goes through FP32 partials in the
+//    workspace; the arrival that completes the band adds the S partials in
+//    split order and writes y.  Every sum has a fixed order, so results are
+//    identical from run to run.
+//  * Counters reset themselves (the last arrival of a band, the last CTA of
 //    the step), so the launch can be replayed from a graph.
-//  * Every wait is bounded (about a second); a timeout sets the status word
-//    and the CTA moves on instead of hanging.
-#include <cooperative_groups.h>
-
+//  * Every wait is bounded (about a second); a timeout sets the status word,
+//    the warp stops issuing copies and, before it exits, waits (bounded
+//    again) for the copies it still has in flight.
 #include <algorithm>
-#include <mutex>
+#include <climits>
+#include <cstring>
 #include <vector>
 
 #include "decode_common.cuh"
@@ -42,34 +52,34 @@ struct StepOp {
     const uint8_t* w;
     const uint32_t* x;
     uint16_t* y;
-    float* part;    // K split: partials [nblocks][S][BB*16*M]
-    unsigned* cnt;  // K split: arrivals per block
+    float* part;    // K split: partials [bands][S][16*M]
+    unsigned* cnt;  // K split: arrivals per band
     int N, K, G, bands;
-    int S, BB, nblocks;
-    int pad;
+    int S, pad;
 };
+static_assert(sizeof(StepOp) == 64, "the projection table is copied in 16-byte pieces");
 
 namespace {
 
-constexpr int kWarps = 16;              // consumer warps
-constexpr int kCons = kWarps * 32;      // consumer threads
-constexpr int kSlot = kWarps;           // tiles per ring slot: one per consumer warp
-constexpr int kThreads = kCons + 32;    // + one producer warp
-constexpr int kQueue = 32;              // block-queue entries
-constexpr int kSmemBudget = 225 * 1024; // one CTA per SM
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSmemBudget = 227 * 1024;  // one CTA per SM
+constexpr int kSlotTiles = 4;            // tiles per ring slot (one bulk copy)
+constexpr int kMaxRing = 32;             // slots per warp (one mbarrier per lane at most)
+// x slice + its group sums: small for few tokens so that the rings keep three slots per warp
+__host__ __device__ constexpr int x_budget(int MP) { return MP <= 4 ? 14 * 1024 : 48 * 1024; }
+constexpr int kSplitPenalty = 16;        // tiles: the cost of combining K-split partials
 
 struct StepSmem {
-    int ring, nslots, bar, queue, flag, x, xsum, red, total;
-    __host__ __device__ StepSmem(int ring_tiles, int MP, int gpc_max, int bb_max) {
-        ring = ring_tiles;
-        nslots = ring_tiles / kSlot;
-        bar = ring_tiles * kTileBytes;                        // ring of 16-tile slots first
-        queue = bar + (2 * nslots + 2 * kQueue) * 8;          // full/empty per slot, queue full/empty
-        flag = queue + kQueue * 4;
-        x = (flag + 16 + 127) & ~127;
+    int R, bar, ops, x, xsum, park, total;
+    __host__ __device__ StepSmem(int R_, int MP, int gpc_max, int nops) {
+        R = R_;
+        bar = kWarps * R * kSlotTiles * kTileBytes;  // rings first: warp w's at w*R*4*1056
+        ops = (bar + kWarps * R * 8 + 63) & ~63;
+        x = (ops + nops * (int)sizeof(StepOp) + 127) & ~127;
         xsum = x + dec::x_bytes(MP, gpc_max);
-        red = xsum + dec::xsum_bytes(gpc_max);
-        total = red + 2 * dec::red_floats(bb_max, (MP + 7) / 8, kWarps) * 4;
+        park = xsum + dec::xsum_bytes(gpc_max);
+        total = park + kWarps * 2 * 16 * MP * 4;
     }
 };
 
@@ -79,265 +89,273 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
     return v;
 }
 
-// The share of projection `o` that CTA c takes without contention: blocks
-// g, g + cps, ... (g = c / S) up to floor(nblocks / cps) of them; the rest are
-// handed out by the per-split counter.
-__device__ __forceinline__ int static_blocks(const StepOp& o, int cps) { return o.nblocks / cps; }
+// This CTA's and this warp's share of a projection.
+struct Geo {
+    int r, g_lo, Gs;  // K split and its group range
+    int ub, nu;       // the CTA's first band and band count
+    int Tc;           // the CTA's tiles (nu * Gs)
+};
+__device__ __forceinline__ Geo geometry(const StepOp& o, int c, int NC) {
+    Geo q;
+    const int S = o.S, cps = NC / S, g = c / S;
+    q.r = c - g * S;
+    q.g_lo = o.G * q.r / S;
+    q.Gs = o.G * (q.r + 1) / S - q.g_lo;
+    q.ub = (int)((long long)o.bands * g / cps);
+    q.nu = (int)((long long)o.bands * (g + 1) / cps) - q.ub;
+    q.Tc = q.nu * q.Gs;
+    return q;
+}
+__device__ __forceinline__ int warp_lo(int Tc, int w) { return Tc * w / kWarps; }
+
+// The copy cursor of one warp: the next tile of its ranges, over all projections.
+struct Cursor {
+    int i, t, t1, gl, Gs, G;
+    const uint8_t* src;
+
+    __device__ __forceinline__ void seek(const StepOp* ops, int nops, int c, int NC, int w) {
+        for (; i < nops; ++i) {
+            const StepOp& o = ops[i];
+            const Geo q = geometry(o, c, NC);
+            const int t0 = warp_lo(q.Tc, w), te = warp_lo(q.Tc, w + 1);
+            if (t0 < te) {
+                t = t0;
+                t1 = te;
+                Gs = q.Gs;
+                G = o.G;
+                gl = t0 % q.Gs;
+                src = o.w + ((size_t)(q.ub + t0 / q.Gs) * o.G + q.g_lo + gl) * kTileBytes;
+                return;
+            }
+        }
+    }
+    // Copy the cursor's next chunk -- up to 4 tiles, not past the end of the
+    // band's run nor of the range -- into dst (lane 0), completing on bar;
+    // advance.  False (nothing issued) at the end of the stream.
+    __device__ __forceinline__ bool issue(const StepOp* ops, int nops, int c, int NC, int w, int lane, uint32_t dst,
+                                          uint32_t bar) {
+        if (i >= nops) return false;
+        const int n = min(kSlotTiles, min(Gs - gl, t1 - t));
+        if (lane == 0) {
+            tc::mbar_arrive_expect_tx(bar, (uint32_t)(n * kTileBytes));
+            tc::bulk_load(dst, src, (uint32_t)(n * kTileBytes), bar);
+        }
+        src += (size_t)n * kTileBytes;
+        gl += n;
+        if (gl == Gs) {
+            gl = 0;
+            src += (size_t)(G - Gs) * kTileBytes;
+        }
+        t += n;
+        if (t == t1) {
+            ++i;
+            seek(ops, nops, c, NC, w);
+        }
+        return true;
+    }
+};
+
+// The outputs a lane holds in MMA fragment layout: rows g8 and g8 + 8 of the
+// band, tokens nt*8 + 2*(lane%4) + {0, 1}; f(row, m, value) for m < M.
+template <int MP, typename F>
+__device__ __forceinline__ void for_frag(const float (&acc)[(MP + 7) / 8][4], int lane, int M, F&& f) {
+    constexpr int NT = (MP + 7) / 8;
+    const int g8 = lane >> 2, cl4 = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int m0 = nt * 8 + 2 * cl4;
+        if (m0 < M) {
+            f(g8, m0, acc[nt][0]);
+            f(g8 + 8, m0, acc[nt][2]);
+        }
+        if (m0 + 1 < M) {
+            f(g8, m0 + 1, acc[nt][1]);
+            f(g8 + 8, m0 + 1, acc[nt][3]);
+        }
+    }
+}
+
+// Finish band `band` of projection o from per-lane outputs (visit(f) calls
+// f(row, m, value) for each output this lane holds; every output of the band
+// is held by exactly one lane of the warp).  S == 1: write y.  S > 1: publish
+// this split's partial; the arrival that completes the band adds the S
+// partials in split order and writes y.
+template <typename V>
+__device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, int M, int lane, V&& visit) {
+    const int n0 = band * 16;
+    if (o.S == 1) {
+        visit([&](int row, int m, float v) {
+            if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = __half_as_ushort(__float2half_rn(v));
+        });
+        return;
+    }
+    const int pb = 16 * M;
+    float* mine = o.part + ((size_t)band * o.S + r) * pb;
+    visit([&](int row, int m, float v) { mine[row * M + m] = v; });
+    __threadfence();
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0) last = atomicAdd(o.cnt + band, 1u) == (unsigned)(o.S - 1);
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    if (!last) return;
+    __threadfence();
+    const float* base = o.part + (size_t)band * o.S * pb;
+    visit([&](int row, int m, float) {
+        float sum = 0.f;
+        for (int s = 0; s < o.S; ++s) sum += __ldcg(base + (size_t)s * pb + row * M + m);
+        if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = __half_as_ushort(__float2half_rn(sum));
+    });
+    if (lane == 0) o.cnt[band] = 0;  // ready for the next replay
+}
 
 template <int MP>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(StepParams p) {
     constexpr int NT = (MP + 7) / 8;
+    constexpr int PB = 16 * MP;  // floats of one parked band partial
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NC = gridDim.x, c = blockIdx.x;
-    const int M = p.M;
-    const StepSmem L(p.ring, MP, p.gpc_max, p.bb_max);
-    const int nslots = L.nslots;
+    const int NC = gridDim.x, c = blockIdx.x, M = p.M, nops = p.nops;
+    const StepSmem L(p.ring, MP, p.gpc_max, nops);
+    const int R = L.R;
     const uint32_t sbase = tc::smem_addr(smem);
-    const uint32_t full0 = sbase + L.bar, empty0 = full0 + 8 * nslots, qfull0 = empty0 + 8 * nslots,
-                   qempty0 = qfull0 + 8 * kQueue;
-    volatile int* queue = reinterpret_cast<volatile int*>(smem + L.queue);
-    volatile int* flag = reinterpret_cast<volatile int*>(smem + L.flag);
+    const uint32_t ring_w = sbase + (uint32_t)(warp * R * kSlotTiles * kTileBytes);
+    const uint32_t bar_w = sbase + (uint32_t)(L.bar + warp * R * 8);
+    StepOp* ops = reinterpret_cast<StepOp*>(smem + L.ops);
+    uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L.x);
+    float* xsum = reinterpret_cast<float*>(smem + L.xsum);
+    float* park = reinterpret_cast<float*>(smem + L.park);
+    float* park_w = park + warp * 2 * PB;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < nslots; ++s) {
-            tc::mbar_init(full0 + 8 * s, 1);
-            tc::mbar_init(empty0 + 8 * s, kWarps);
-        }
-        for (int q = 0; q < kQueue; ++q) {
-            tc::mbar_init(qfull0 + 8 * q, 1);
-            tc::mbar_init(qempty0 + 8 * q, 1);
-        }
-        tc::mbar_init_fence();
-    }
+    for (int k = threadIdx.x; k < nops * 4; k += kThreads)
+        reinterpret_cast<uint4*>(ops)[k] = __ldg(reinterpret_cast<const uint4*>(p.ops) + k);
+    if (lane < R) tc::mbar_init(bar_w + 8 * lane, 1);
+    tc::mbar_init_fence();
     __syncthreads();
 
-    if (warp == kWarps) {
-        // ---- producer: pick blocks, publish them, stream their tiles ---------------
-        if (lane == 0) {
-            int slot = 0, qs = 0;
-            uint32_t use = 0, quse = 0, issued = 0;
-            bool ok = true;
-            for (int i = 0; i < p.nops && ok; ++i) {
-                const StepOp o = p.ops[i];
-                const int r = c % o.S, cps = NC / o.S, g = c / o.S;
-                const int g_lo = (int)(((long long)o.G * r) / o.S);
-                const int Gs = (int)(((long long)o.G * (r + 1)) / o.S) - g_lo;
-                const int nstatic = static_blocks(o, cps);
-                for (int k = 0; ok; ++k) {
-                    int blk = k < nstatic ? g + k * cps
-                                          : nstatic * cps + (int)atomicAdd(p.sched + i * 8 + r, 1u);
-                    if (blk >= o.nblocks) blk = -1;
-                    if (quse > 0 && !tc::mbar_wait(qempty0 + 8 * qs, (quse - 1) & 1)) {
-                        atomicOr(p.status, 1);
-                        ok = false;
+    // fill this warp's ring
+    Cursor cur;
+    cur.i = 0;
+    cur.seek(ops, nops, c, NC, warp);
+    uint32_t n_iss = 0, n_con = 0, n_obs = 0;  // issued, consumed, observed complete
+    for (int s = 0; s < R; ++s) {
+        if (!cur.issue(ops, nops, c, NC, warp, lane, ring_w + (uint32_t)(s * kSlotTiles * kTileBytes), bar_w + 8 * s))
+            break;
+        ++n_iss;
+    }
+    bool ok = true;
+
+    for (int i = 0; i < nops; ++i) {
+        const StepOp& o = ops[i];
+        if (i > 0) {
+            // x_i may be computed from y_(i-1): wait until every CTA is done with it
+            if (threadIdx.x == 0) {
+                const long long t0 = clock64();
+                while (ld_acquire(p.done + (i - 1)) < (unsigned)NC) {
+                    if (clock64() - t0 > (1ll << 31)) {
+                        atomicOr(p.status, 2);
                         break;
                     }
-                    queue[qs] = blk;
-                    tc::mbar_arrive(qfull0 + 8 * qs);  // release: the entry is visible to the waiters
-                    if (++qs == kQueue) {
-                        qs = 0;
-                        ++quse;
-                    }
-                    if (blk < 0) break;
-                    const int band0 = blk * o.BB;
-                    const int T = min(o.BB, o.bands - band0) * Gs;
-                    int bb = 0, gl = 0;
-                    for (int t0 = 0; t0 < T; t0 += kSlot) {
-                        if (use > 0 && !tc::mbar_wait(empty0 + 8 * slot, (use - 1) & 1)) {
-                            atomicOr(p.status, 1);
-                            ok = false;
-                            break;
-                        }
-                        const int n = min(kSlot, T - t0);
-                        const uint32_t bar = full0 + 8 * slot;
-                        tc::mbar_arrive_expect_tx(bar, (uint32_t)n * kTileBytes);
-                        uint32_t dst = sbase + (uint32_t)slot * (kSlot * kTileBytes);
-                        for (int left = n; left > 0;) {
-                            const int run = min(left, Gs - gl);
-                            const uint8_t* src = o.w + ((size_t)(band0 + bb) * o.G + g_lo + gl) * kTileBytes;
-                            tc::bulk_load(dst, src, (uint32_t)run * kTileBytes, bar);
-                            dst += run * kTileBytes;
-                            left -= run;
-                            gl += run;
-                            if (gl == Gs) {
-                                gl = 0;
-                                ++bb;
-                            }
-                        }
-                        ++issued;
-                        if (++slot == nslots) {
-                            slot = 0;
-                            ++use;
-                        }
-                    }
                 }
             }
-            for (uint32_t k = 0; k < (uint32_t)nslots && k < issued; ++k) {
-                const uint32_t cc = issued - 1 - k;
-                tc::mbar_wait(full0 + 8 * (cc % nslots), (cc / nslots) & 1);
-            }
+            __syncthreads();
         }
-        __syncwarp();
-    } else {
-        // ---- consumers ----------------------------------------------------------------
-        int slot = 0, qs = 0;
-        uint32_t use = 0, quse = 0;
-        int kblk = 0;
-        bool ok = true;
-        uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L.x);
-        float* xsum = reinterpret_cast<float*>(smem + L.xsum);
-        float* red_base = reinterpret_cast<float*>(smem + L.red);
-        for (int i = 0; i < p.nops; ++i) {
-            const StepOp o = p.ops[i];
-            const int r = c % o.S;
-            const int g_lo = (int)(((long long)o.G * r) / o.S);
-            const int Gs = (int)(((long long)o.G * (r + 1)) / o.S) - g_lo;
-            const int BB = o.BB;
-            if (i > 0) {
-                // x_i may be computed from y_(i-1): wait until every CTA is done with it
-                if (threadIdx.x == 0) {
-                    const long long t0 = clock64();
-                    while (ld_acquire(p.done + (i - 1)) < (unsigned)NC) {
-                        if (clock64() - t0 > (1ll << 31)) {
-                            atomicOr(p.status, 2);
-                            break;
-                        }
-                    }
-                }
-                tc::named_barrier(1, kCons);
-            }
-            dec::stage_x_async<MP, kCons>(o.x, M, o.K, g_lo, Gs, xs, xsum);
+        const Geo q = geometry(o, c, NC);
+        if (q.nu > 0) {
+            dec::stage_x_async<MP, kThreads>(o.x, M, o.K, q.g_lo, q.Gs, xs, xsum);
             dec::TileMac<MP> mac(sbase + L.x, sbase + L.xsum, lane);
-            const int red_buf = dec::red_floats(BB, NT, kWarps);
-
-            while (true) {
-                if (!tc::mbar_wait(qfull0 + 8 * qs, quse & 1)) {
-                    atomicOr(p.status, 8);
-                    ok = false;
-                }
-                const int blk = ok ? queue[qs] : -1;
-                if (blk < 0) {
-                    tc::named_barrier(1, kCons);  // everyone has read the entry
-                    if (threadIdx.x == 0) tc::mbar_arrive(qempty0 + 8 * qs);
-                    if (++qs == kQueue) {
-                        qs = 0;
-                        ++quse;
-                    }
-                    break;
-                }
-                const int band0 = blk * BB;
-                const int nb = min(BB, o.bands - band0);
-                const int T = nb * Gs;
-                const bool blk_ok0 = ok;
-                float* red = red_base + (kblk & 1) * red_buf;
-                float4* myred = reinterpret_cast<float4*>(red) + warp * BB * NT * 32 + lane;
-                for (int q = 0; q < BB * NT; ++q) myred[q * 32] = make_float4(0.f, 0.f, 0.f, 0.f);
-                float acc[NT][4];
+            const int t0 = warp_lo(q.Tc, warp), t1 = warp_lo(q.Tc, warp + 1);
+            const int u_first = t0 / q.Gs;
+            int t = t0, gl = t0 % q.Gs, u = u_first;
+            float acc[NT][4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-                int cur_bb = 0, band_end = Gs;
-                for (int t0 = 0; t0 < T; t0 += kSlot) {
-                    if (ok && !tc::mbar_wait(full0 + 8 * slot, use & 1)) {
-                        atomicOr(p.status, 4);
+                for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+            while (t < t1) {
+                const int n = min(kSlotTiles, min(q.Gs - gl, t1 - t));  // the chunk the cursor copied
+                const uint32_t slot = n_con % (uint32_t)R;
+                const uint32_t ta = ring_w + slot * (kSlotTiles * kTileBytes), bar = bar_w + 8 * slot;
+                if (ok) {
+                    const bool got = tc::mbar_wait(bar, (n_con / (uint32_t)R) & 1);
+                    if (__all_sync(0xFFFFFFFFu, got)) {
+                        ++n_obs;
+                    } else {
+                        if (lane == 0) atomicOr(p.status, 4);
                         ok = false;
                     }
-                    const int t = t0 + warp;
-                    if (ok && t < T) {
-                        while (t >= band_end) {
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt)
-                                myred[(cur_bb * NT + nt) * 32] =
-                                    make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-                            ++cur_bb;
-                            band_end += Gs;
+                }
+                if (ok) {
+                    if (n == kSlotTiles) {
+                        if constexpr (MP >= 8) {  // register budget: two pairs
+                            mac.template run_tiles<2>(ta, gl, lane, acc);
+                            mac.template run_tiles<2>(ta + 2 * kTileBytes, gl + 2, lane, acc);
+                        } else {
+                            mac.template run_tiles<kSlotTiles>(ta, gl, lane, acc);
                         }
-                        mac.run(sbase + (uint32_t)slot * (kSlot * kTileBytes) + (uint32_t)warp * kTileBytes,
-                                t - cur_bb * Gs, lane, acc);
-                    }
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(empty0 + 8 * slot);
-                    if (++slot == nslots) {
-                        slot = 0;
-                        ++use;
+                    } else {
+                        for (int j = 0; j < n; ++j) mac.run(ta + (uint32_t)(j * kTileBytes), gl + j, lane, acc);
                     }
                 }
+                __syncwarp();
+                ++n_con;
+                if (ok && cur.issue(ops, nops, c, NC, warp, lane, ta, bar)) ++n_iss;
+                t += n;
+                gl += n;
+                if (gl == q.Gs || t == t1) {
+                    const int us = u * q.Gs;
+                    if (us >= t0 && us + q.Gs <= t1) {
+                        // the whole band is this warp's: finish it from the accumulators
+                        finish_band(o, q.ub + u, q.r, M, lane, [&](auto&& f) { for_frag<MP>(acc, lane, M, f); });
+                    } else {
+                        // cut between warps: park this warp's share
+                        float* dst = park_w + (u == u_first ? 0 : PB);
+                        for_frag<MP>(acc, lane, M, [&](int row, int m, float v) { dst[row * MP + m] = v; });
+                    }
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    myred[(cur_bb * NT + nt) * 32] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-                tc::named_barrier(1, kCons);
-                // every consumer has read this block's queue entry: free it
-                if (threadIdx.x == 0) tc::mbar_arrive(qempty0 + 8 * qs);
-                if (++qs == kQueue) {
-                    qs = 0;
-                    ++quse;
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+                    ++u;
+                    gl = 0;
                 }
-                const int Tout = nb * 16 * M;
-                float v[4];
-                dec::block_sums<NT, kCons>(red, BB, nb, M, blk_ok0 && ok, v);
-                if (o.S == 1) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int t = threadIdx.x + q * kCons;
-                        if (t < Tout) {
-                            const int m = t / (nb * 16), rl = t - m * (nb * 16);
-                            const int n = band0 * 16 + rl;
-                            if (n < o.N) o.y[(size_t)m * o.N + n] = __half_as_ushort(__float2half_rn(v[q]));
-                        }
-                    }
-                } else {
-                    // K split: publish this split's partial; the last arrival adds all
-                    // splits in order and writes y
-                    const int pb = BB * 16 * M;
-                    float* mine = o.part + ((size_t)blk * o.S + r) * pb;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int t = threadIdx.x + q * kCons;
-                        if (t < Tout) mine[t] = v[q];
-                    }
-                    __threadfence();
-                    tc::named_barrier(1, kCons);
-                    if (threadIdx.x == 0) *flag = (atomicAdd(o.cnt + blk, 1u) == (unsigned)(o.S - 1));
-                    tc::named_barrier(1, kCons);
-                    if (*flag) {
-                        __threadfence();
-                        const float* base = o.part + (size_t)blk * o.S * pb;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int t = threadIdx.x + q * kCons;
-                            if (t < Tout) {
-                                float sum = 0.f;
-                                for (int s2 = 0; s2 < o.S; ++s2) sum += __ldcg(base + (size_t)s2 * pb + t);
-                                const int m = t / (nb * 16), rl = t - m * (nb * 16);
-                                const int n = band0 * 16 + rl;
-                                if (n < o.N) o.y[(size_t)m * o.N + n] = __half_as_ushort(__float2half_rn(sum));
-                            }
-                        }
-                        if (threadIdx.x == 0) o.cnt[blk] = 0;  // ready for the next step
-                    }
-                }
-                ++kblk;
             }
-            // this CTA is done with projection i: its y (and partials) are visible
-            __threadfence();
-            tc::named_barrier(1, kCons);
-            if (threadIdx.x == 0) atomicAdd(p.done + i, 1u);
+            __syncthreads();
+            // bands cut between warps: the lowest warp whose range starts
+            // strictly inside the band adds the parked shares in warp order
+            const int tw = t0 % q.Gs;
+            if (warp > 0 && t0 < q.Tc && tw != 0 && warp_lo(q.Tc, warp - 1) <= t0 - tw) {
+                const int bs = u_first * q.Gs, be = bs + q.Gs;  // the band's tiles
+                finish_band(o, q.ub + u_first, q.r, M, lane, [&](auto&& f) {
+                    for (int oi = lane; oi < 16 * M; oi += 32) {
+                        const int row = oi / M, m = oi - row * M;
+                        float sum = 0.f;
+                        for (int w2 = 0; w2 < kWarps; ++w2) {
+                            const int a = warp_lo(q.Tc, w2), b = warp_lo(q.Tc, w2 + 1);
+                            if (a < b && a < be && b > bs)
+                                sum += park[(w2 * 2 + (a >= bs ? 0 : 1)) * PB + row * MP + m];
+                        }
+                        f(row, m, sum);
+                    }
+                });
+            }
         }
-        // the last CTA out resets the counters for the next step
-        if (threadIdx.x == 0) {
+        // this CTA is done with projection i: its y (and partials) are visible
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) atomicAdd(p.done + i, 1u);
+    }
+
+    // copies still in flight after a timeout
+    for (; n_obs < n_iss; ++n_obs)
+        if (!tc::mbar_wait(bar_w + 8 * (n_obs % (uint32_t)R), (n_obs / (uint32_t)R) & 1)) break;
+
+    // the last CTA out resets the counters for the next step
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.exit_cnt, 1u) == (unsigned)(NC - 1)) {
+            for (int i = 0; i < nops; ++i) p.done[i] = 0;
+            *p.exit_cnt = 0;
             __threadfence();
-            if (atomicAdd(p.exit_cnt, 1u) == (unsigned)(NC - 1)) {
-                for (int i = 0; i < p.nops; ++i) p.done[i] = 0;
-                for (int i = 0; i < 8 * p.nops; ++i) p.sched[i] = 0;
-                *p.exit_cnt = 0;
-                __threadfence();
-            }
         }
     }
 }
@@ -361,63 +379,78 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 // ---- host-side plan ---------------------------------------------------------------
 struct StepPlan {
-    int MP = 1, NC = 0, gpc_max = 1, bb_max = 1, ring = 0, smem = 0;
+    int MP = 1, NC = 0, gpc_max = 1, R = 0, smem = 0;
     std::vector<StepOp> ops;  // device pointers filled against a workspace base
-    size_t table_off = 0, done_off = 0, exit_off = 0, status_off = 0, sched_off = 0, total = 0;
+    size_t table_off = 0, done_off = 0, exit_off = 0, status_off = 0, total = 0;
     std::vector<size_t> cnt_off, part_off;
 };
 
-// Per projection: one band per block (the block queue balances the tail) and
-// the smallest K split (dividing NC) whose x slice fits 48 KB; the ring takes
-// the rest of the shared memory.  Lays out the workspace.
-static void plan_step(const w4_weight* w, int n, int M, int NC, StepPlan* pl) {
+// K split of one projection: S divides NC (the CTAs of a split are c % S),
+// the x slice fits its budget, and the largest per-CTA share of tiles (plus a
+// fixed cost for combining partials when S > 1) is smallest.  0 if no split fits.
+static int choose_split(int bands, int G, int MP, int NC) {
+    int best = 0;
+    long best_cost = LONG_MAX;
+    for (int S = 1; S <= std::min(G, NC); ++S) {
+        if (NC % S) continue;
+        const int Gs = (G + S - 1) / S;
+        if (dec::x_bytes(MP, Gs) + dec::xsum_bytes(Gs) > x_budget(MP)) continue;
+        const int cps = NC / S;
+        const long cost = (long)((bands + cps - 1) / cps) * Gs + (S > 1 ? kSplitPenalty : 0);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = S;
+        }
+    }
+    return best;
+}
+
+// Splits, shared-memory sizing (the rings take what the rest leaves) and the
+// workspace layout.  False if some projection cannot be planned.
+static bool plan_step(const w4_weight* w, int n, int M, int NC, StepPlan* pl) {
     pl->MP = padded(M);
     pl->NC = NC;
     pl->ops.assign(n, StepOp{});
     pl->cnt_off.assign(n, 0);
     pl->part_off.assign(n, 0);
-    std::vector<int> S_of(n);
-    for (int i = 0; i < n; ++i) {
-        const int G = (int)(w[i].K / kGroupK);
-        int S = 1;
-        while (S < 8 && 2 * S <= G && NC % (2 * S) == 0 &&
-               dec::x_bytes(pl->MP, (G + S - 1) / S) + dec::xsum_bytes((G + S - 1) / S) > 48 * 1024)
-            S *= 2;
-        S_of[i] = S;
-        pl->gpc_max = std::max(pl->gpc_max, (G + S - 1) / S);
-    }
-    pl->bb_max = 1;
-    int ring = 192;
-    while (ring > kSlot && StepSmem(ring, pl->MP, pl->gpc_max, pl->bb_max).total > kSmemBudget) ring -= kSlot;
-    pl->ring = ring;
-    pl->smem = StepSmem(ring, pl->MP, pl->gpc_max, pl->bb_max).total;
-    size_t off = 0;
-    pl->table_off = off;
-    off = align_up(off + sizeof(StepOp) * n);
-    pl->done_off = off;
-    off = align_up(off + sizeof(unsigned) * n);
-    pl->sched_off = off;
-    off = align_up(off + sizeof(unsigned) * 8 * n);
-    pl->exit_off = off;
-    pl->status_off = off + 16;
-    off = align_up(off + 32);
-    for (int i = 0; i < n; ++i) {
+    pl->gpc_max = 1;
+    bool fits = NC > 0;
+    for (int i = 0; i < n && fits; ++i) {
         StepOp& o = pl->ops[i];
         o.N = (int)w[i].N;
         o.K = (int)w[i].K;
         o.G = (int)(w[i].K / kGroupK);
         o.bands = (int)num_bands(w[i].N);
-        o.S = S_of[i];
-        o.BB = 1;
-        o.nblocks = o.bands;
+        o.S = choose_split(o.bands, o.G, pl->MP, NC);
+        if (o.S == 0) {
+            fits = false;
+            o.S = 1;
+        }
+        pl->gpc_max = std::max(pl->gpc_max, (o.G + o.S - 1) / o.S);
+    }
+    const int fixed = StepSmem(0, pl->MP, pl->gpc_max, n).total;
+    pl->R = std::min(kMaxRing, (kSmemBudget - fixed) / (kWarps * (kSlotTiles * kTileBytes + 8)));
+    while (pl->R > 0 && StepSmem(pl->R, pl->MP, pl->gpc_max, n).total > kSmemBudget) --pl->R;
+    pl->smem = StepSmem(pl->R, pl->MP, pl->gpc_max, n).total;
+    size_t off = 0;
+    pl->table_off = off;
+    off = align_up(off + sizeof(StepOp) * n);
+    pl->done_off = off;
+    off = align_up(off + sizeof(unsigned) * n);
+    pl->exit_off = off;
+    pl->status_off = off + 16;
+    off = align_up(off + 32);
+    for (int i = 0; i < n; ++i) {
+        const StepOp& o = pl->ops[i];
         if (o.S > 1) {
             pl->cnt_off[i] = off;
-            off = align_up(off + sizeof(unsigned) * o.nblocks);
+            off = align_up(off + sizeof(unsigned) * o.bands);
             pl->part_off[i] = off;
-            off = align_up(off + sizeof(float) * (size_t)o.nblocks * o.S * o.BB * 16 * M);
+            off = align_up(off + sizeof(float) * (size_t)o.bands * o.S * 16 * M);
         }
     }
     pl->total = off;
+    return fits && pl->R >= 2;
 }
 
 static int sm_count_now() {
@@ -447,11 +480,13 @@ w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y,
                        size_t ws_bytes, cudaStream_t stream, StepLaunch* out) {
     const int MP = padded(M);
     StepPlan pl;
-    plan_step(w, n, M, sm_count_now(), &pl);
+    if (!plan_step(w, n, M, sm_count_now(), &pl)) {
+        set_error("the persistent step kernel cannot hold this sequence in shared memory (%d projections)", n);
+        return W4_ERR_UNSUPPORTED;
+    }
     const int NC = step_grid(MP, pl.smem);
-    if (NC <= 0 || NC != pl.NC || pl.ring < 2 * kSlot) {
-        set_error("the persistent step kernel cannot be resident (shared memory %d bytes, ring %d tiles)",
-                  pl.smem, pl.ring);
+    if (NC <= 0 || NC != pl.NC) {
+        set_error("the persistent step kernel cannot be resident (shared memory %d bytes)", pl.smem);
         return W4_ERR_UNSUPPORTED;
     }
     if (!ws || ws_bytes < pl.total) {
@@ -484,11 +519,9 @@ w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y,
     p.M = M;
     p.done = reinterpret_cast<unsigned*>(base + pl.done_off);
     p.exit_cnt = reinterpret_cast<unsigned*>(base + pl.exit_off);
-    p.sched = reinterpret_cast<unsigned*>(base + pl.sched_off);
     p.status = reinterpret_cast<int*>(base + pl.status_off);
     p.gpc_max = pl.gpc_max;
-    p.bb_max = pl.bb_max;
-    p.ring = pl.ring;
+    p.ring = pl.R;
     return W4_OK;
 }
 
@@ -501,7 +534,7 @@ int step_status(const StepLaunch& s) {
 w4_status step_launch(const StepLaunch& s, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)s.NC, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);  // 16 consumer warps + the producer warp
+    cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)s.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr;

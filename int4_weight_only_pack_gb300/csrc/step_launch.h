@@ -15,10 +15,9 @@ struct StepParams {
     int nops, M;
     unsigned* done;      // [nops] CTAs finished with each projection
     unsigned* exit_cnt;  // CTAs finished with the step
-    unsigned* sched;     // [nops][8] next dynamic block per K split
     int* status;         // set non-zero when a wait gives up
-    int gpc_max, bb_max; // shared-memory sizing
-    int ring;            // ring tiles (a multiple of 16)
+    int gpc_max;         // largest x slice (groups): shared-memory sizing
+    int ring;            // ring slots (tiles) per warp
 };
 
 using StepFn = void (*)(StepParams);
