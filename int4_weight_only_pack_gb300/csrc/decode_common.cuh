@@ -112,9 +112,10 @@ __device__ __forceinline__ void stage_x(const uint32_t* x, int M, int K, int g_l
     tc::named_barrier(1, kConsumers);
 }
 
-// The same staging as stage_x, with every word copied from global memory
-// straight into its fragment slot by a 4-byte cp.async, all issued before any
-// is waited for: one memory round trip whatever the slice size.
+// The same staging as stage_x, with every 8-byte piece (the b0, b1 words of
+// one lane class and k16 step) copied from global memory straight into its
+// fragment slot by a cp.async, all issued before any is waited for: one
+// memory round trip whatever the slice size.  x must be 8-byte aligned.
 template <int MP, int NCONS>
 __device__ __forceinline__ void stage_x_async(const uint32_t* x, int M, int K, int g_lo, int Gs, uint32_t* xs,
                                               float* xsum) {
@@ -124,17 +125,19 @@ __device__ __forceinline__ void stage_x_async(const uint32_t* x, int M, int K, i
     const uint32_t* xg = x + (size_t)g_lo * 64;
     const int kp = K / 2;
     const uint32_t xs_s = tc::smem_addr(xs);
+    // 8-byte pieces: k 4c .. 4c+3 of one k16 step (its b0 and b1 words)
+    const int per_row8 = per_row / 2;
     for (int m = 0; m < MP; ++m) {
-        for (int r = tid; r < per_row; r += NCONS) {
-            const int gl = r >> 6, kk2 = r & 63;
-            const int j = kk2 >> 3, c = (kk2 >> 1) & 3, hi = kk2 & 1;
-            const int dst = gl * (MP * 64) + (j >> 1) * (MP * 16) + (m * 4 + c) * 4 + (j & 1) * 2 + hi;
+        for (int r = tid; r < per_row8; r += NCONS) {
+            const int gl = r >> 5, kq = r & 31;
+            const int j = kq >> 2, c = kq & 3;
+            const int dst = gl * (MP * 64) + (j >> 1) * (MP * 16) + (m * 4 + c) * 4 + (j & 1) * 2;
             if (m < M)
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(xs_s + 4u * dst),
-                             "l"(xg + (size_t)m * kp + r)
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(xs_s + 4u * dst),
+                             "l"(xg + (size_t)m * kp + 2 * r)
                              : "memory");
             else
-                xs[dst] = 0;
+                *reinterpret_cast<uint2*>(xs + dst) = make_uint2(0, 0);
         }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -161,25 +164,22 @@ struct TileMac {
     static constexpr int NT = (MP + 7) / 8;  // n8 token tiles of the MMA
     uint32_t xfrag;                          // this lane's B-fragment words of group 0
     uint32_t xsum;                           // this lane's token pair's sums of group 0
-    bool xlane;                              // lanes of padding tokens keep zero fragments
     uint4 xb[NT][4];
 
+    // Lanes of the MMA's padding token columns (tok >= MP) read the fragment
+    // of token tok % MP: those output columns are never written, and a real
+    // token's (finite) values keep them finite.
     __device__ __forceinline__ TileMac(uint32_t x_smem, uint32_t xsum_smem, int lane) {
         const int tok = lane >> 2, cl4 = lane & 3;
-        xfrag = x_smem + (uint32_t)((tok * 4 + cl4) * 16);
+        xfrag = x_smem + (uint32_t)(((tok % MP) * 4 + cl4) * 16);
         xsum = xsum_smem + (uint32_t)(2 * cl4 * 4);
-        xlane = tok < MP;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) xb[nt][q] = make_uint4(0, 0, 0, 0);
     }
 
     // acc += s * sum_{k in group gl} x * q for the tile at shared address ta.
     __device__ __forceinline__ void run(uint32_t ta, int gl, int lane, float (&acc)[NT][4]) {
         const uint4 lo = lds128(ta + 16 * lane), hi = lds128(ta + 512 + 16 * lane);
         const uint32_t sc = lds32(ta + kScaleOffset + 4 * (lane >> 2));
-        if (xlane) {
+        {
             const uint32_t xa = xfrag + (uint32_t)gl * (MP * 256);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -244,8 +244,7 @@ struct TileMac {
                 uint4 v[NT];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
-                    v[nt] = xlane ? lds128(xa0 + (uint32_t)(n * MP * 256 + q * MP * 64 + nt * 512))
-                                  : make_uint4(0, 0, 0, 0);
+                    v[nt] = lds128(xa0 + (uint32_t)(n * MP * 256 + q * MP * 64 + nt * 512));
                 uint32_t a[4], b[4];
                 unpack_word_biased(wd[n][2 * q], a);
                 unpack_word_biased(wd[n][2 * q + 1], b);

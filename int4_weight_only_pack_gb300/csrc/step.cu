@@ -55,7 +55,7 @@ struct StepOp {
     float* part;    // K split: partials [bands][S][16*M]
     unsigned* cnt;  // K split: arrivals per band
     int N, K, G, bands;
-    int S, pad;
+    int S, cps;  // K splits; CTAs per split (grid / S)
 };
 static_assert(sizeof(StepOp) == 64, "the projection table is copied in 16-byte pieces");
 
@@ -97,12 +97,12 @@ struct Geo {
 };
 __device__ __forceinline__ Geo geometry(const StepOp& o, int c, int NC) {
     Geo q;
-    const int S = o.S, cps = NC / S, g = c / S;
+    const int S = o.S, cps = o.cps, g = c / S;  // 32-bit: bands * grid < 2^31
     q.r = c - g * S;
     q.g_lo = o.G * q.r / S;
     q.Gs = o.G * (q.r + 1) / S - q.g_lo;
-    q.ub = (int)((long long)o.bands * g / cps);
-    q.nu = (int)((long long)o.bands * (g + 1) / cps) - q.ub;
+    q.ub = o.bands * g / cps;
+    q.nu = o.bands * (g + 1) / cps - q.ub;
     q.Tc = q.nu * q.Gs;
     return q;
 }
@@ -192,13 +192,16 @@ __device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, in
     const int pb = 16 * M;
     float* mine = o.part + ((size_t)band * o.S + r) * pb;
     visit([&](int row, int m, float v) { mine[row * M + m] = v; });
-    __threadfence();
+    // the warp's stores are ordered before lane 0's fence by the warp barrier
     __syncwarp();
     unsigned last = 0;
-    if (lane == 0) last = atomicAdd(o.cnt + band, 1u) == (unsigned)(o.S - 1);
+    if (lane == 0) {
+        __threadfence();
+        last = atomicAdd(o.cnt + band, 1u) == (unsigned)(o.S - 1);
+        if (last) __threadfence();
+    }
     last = __shfl_sync(0xFFFFFFFFu, last, 0);
     if (!last) return;
-    __threadfence();
     const float* base = o.part + (size_t)band * o.S * pb;
     visit([&](int row, int m, float) {
         float sum = 0.f;
@@ -339,10 +342,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(StepParams p) {
                 });
             }
         }
-        // this CTA is done with projection i: its y (and partials) are visible
-        __threadfence();
+        // this CTA is done with projection i: the barrier orders every
+        // thread's y stores before thread 0's fence, which makes them visible
+        // before the completion count
         __syncthreads();
-        if (threadIdx.x == 0) atomicAdd(p.done + i, 1u);
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicAdd(p.done + i, 1u);
+        }
     }
 
     // copies still in flight after a timeout
@@ -422,10 +429,11 @@ static bool plan_step(const w4_weight* w, int n, int M, int NC, StepPlan* pl) {
         o.G = (int)(w[i].K / kGroupK);
         o.bands = (int)num_bands(w[i].N);
         o.S = choose_split(o.bands, o.G, pl->MP, NC);
-        if (o.S == 0) {
+        if (o.S == 0 || (long long)o.bands * NC >= INT_MAX) {
             fits = false;
             o.S = 1;
         }
+        o.cps = NC / o.S;
         pl->gpc_max = std::max(pl->gpc_max, (o.G + o.S - 1) / o.S);
     }
     const int fixed = StepSmem(0, pl->MP, pl->gpc_max, n).total;
