@@ -23,7 +23,6 @@ w4_status check_gemv_args(const void* x, const w4_weight* w, const void* y, int 
 w4_status prepare_gemv(const w4_weight* w, int M, const w4_gemv_config& c);
 
 // persistent decode-step kernel (step.cu)
-struct StepParams;
 struct StepLaunch;
 size_t step_workspace_bytes(const w4_weight* w, int n, int M);
 }  // namespace w4

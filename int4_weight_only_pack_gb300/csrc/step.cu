@@ -57,7 +57,20 @@ struct StepOp {
     int N, K, G, bands;
     int S, cps;  // K splits; CTAs per split (grid / S)
 };
-static_assert(sizeof(StepOp) == 64, "the projection table is copied in 16-byte pieces");
+static_assert(sizeof(StepOp) == 64, "one projection record");
+
+// The kernel's only parameter: the projection table travels in the launch's
+// parameter space (read through the constant cache; at most 32 KB).
+struct StepArgs {
+    int nops, M;
+    unsigned* done;      // [nops] CTAs finished with each projection
+    unsigned* exit_cnt;  // CTAs finished with the step
+    int* status;         // set non-zero when a wait gives up
+    int gpc_max;         // largest x slice (groups): shared-memory sizing
+    int ring;            // ring slots per warp
+    StepOp ops[kMaxStepOps];
+};
+static_assert(sizeof(StepArgs) <= 32000, "kernel parameter space");
 
 namespace {
 
@@ -66,17 +79,18 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kSmemBudget = 227 * 1024;  // one CTA per SM
 constexpr int kSlotTiles = 4;            // tiles per ring slot (one bulk copy)
 constexpr int kMaxRing = 32;             // slots per warp (one mbarrier per lane at most)
+constexpr int kSplitPenalty = 16;        // tiles: the cost of combining K-split partials
+constexpr int kMaxCtaTiles = 1 << 22;    // per-CTA tiles of one projection (float division below)
 // x slice + its group sums: small for few tokens so that the rings keep three slots per warp
 __host__ __device__ constexpr int x_budget(int MP) { return MP <= 4 ? 14 * 1024 : 48 * 1024; }
-constexpr int kSplitPenalty = 16;        // tiles: the cost of combining K-split partials
 
 struct StepSmem {
-    int R, bar, ops, x, xsum, park, total;
+    int R, bar, geo, x, xsum, park, total;
     __host__ __device__ StepSmem(int R_, int MP, int gpc_max, int nops) {
         R = R_;
         bar = kWarps * R * kSlotTiles * kTileBytes;  // rings first: warp w's at w*R*4*1056
-        ops = (bar + kWarps * R * 8 + 63) & ~63;
-        x = (ops + nops * (int)sizeof(StepOp) + 127) & ~127;
+        geo = bar + kWarps * R * 8;
+        x = (geo + nops * 16 + 127) & ~127;
         xsum = x + dec::x_bytes(MP, gpc_max);
         park = xsum + dec::xsum_bytes(gpc_max);
         total = park + kWarps * 2 * 16 * MP * 4;
@@ -89,42 +103,59 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
     return v;
 }
 
-// This CTA's and this warp's share of a projection.
+// This CTA's share of one projection, computed once per launch.
 struct Geo {
-    int r, g_lo, Gs;  // K split and its group range
-    int ub, nu;       // the CTA's first band and band count
-    int Tc;           // the CTA's tiles (nu * Gs)
+    int g_lo, Gs;  // the K split's group range
+    int ub, nu;    // the CTA's first band and band count
+    int r;         // K split
+    float inv_gs;  // 1 / Gs
+    __device__ __forceinline__ int Tc() const { return nu * Gs; }
 };
-__device__ __forceinline__ Geo geometry(const StepOp& o, int c, int NC) {
+__device__ __forceinline__ void put_geo(uint4* tab, const StepOp& o, int c) {
+    const int S = o.S, g = c / S, r = c - g * S;
+    const int g_lo = o.G * r / S, Gs = o.G * (r + 1) / S - g_lo;
+    const int ub = o.bands * g / o.cps, nu = o.bands * (g + 1) / o.cps - ub;
+    *tab = make_uint4((uint32_t)g_lo | ((uint32_t)Gs << 16), (uint32_t)ub | ((uint32_t)nu << 16), (uint32_t)r,
+                      __float_as_uint(1.0f / (float)Gs));
+}
+__device__ __forceinline__ Geo get_geo(const uint4* tab) {
+    const uint4 v = *tab;
     Geo q;
-    const int S = o.S, cps = o.cps, g = c / S;  // 32-bit: bands * grid < 2^31
-    q.r = c - g * S;
-    q.g_lo = o.G * q.r / S;
-    q.Gs = o.G * (q.r + 1) / S - q.g_lo;
-    q.ub = o.bands * g / cps;
-    q.nu = o.bands * (g + 1) / cps - q.ub;
-    q.Tc = q.nu * q.Gs;
+    q.g_lo = (int)(v.x & 0xFFFF);
+    q.Gs = (int)(v.x >> 16);
+    q.ub = (int)(v.y & 0xFFFF);
+    q.nu = (int)(v.y >> 16);
+    q.r = (int)v.z;
+    q.inv_gs = __uint_as_float(v.w);
     return q;
 }
 __device__ __forceinline__ int warp_lo(int Tc, int w) { return Tc * w / kWarps; }
+// t / d for 0 <= t < 2^22, with inv = 1/d: the float estimate is off by at most one.
+__device__ __forceinline__ int div_small(int t, int d, float inv) {
+    int q = __float2int_rz((float)t * inv);
+    const int rem = t - q * d;
+    if (rem < 0) --q;
+    else if (rem >= d) ++q;
+    return q;
+}
 
-// The copy cursor of one warp: the next tile of its ranges, over all projections.
+// The copy cursor of one warp: the next chunk of its ranges, over all projections.
 struct Cursor {
     int i, t, t1, gl, Gs, G;
     const uint8_t* src;
 
-    __device__ __forceinline__ void seek(const StepOp* ops, int nops, int c, int NC, int w) {
-        for (; i < nops; ++i) {
-            const StepOp& o = ops[i];
-            const Geo q = geometry(o, c, NC);
-            const int t0 = warp_lo(q.Tc, w), te = warp_lo(q.Tc, w + 1);
+    __device__ __forceinline__ void seek(const StepArgs& a, const uint4* geo, int w) {
+        for (; i < a.nops; ++i) {
+            const Geo q = get_geo(geo + i);
+            const int t0 = warp_lo(q.Tc(), w), te = warp_lo(q.Tc(), w + 1);
             if (t0 < te) {
+                const int u = div_small(t0, q.Gs, q.inv_gs);
                 t = t0;
                 t1 = te;
                 Gs = q.Gs;
-                G = o.G;
-                gl = t0 % q.Gs;
-                src = o.w + ((size_t)(q.ub + t0 / q.Gs) * o.G + q.g_lo + gl) * kTileBytes;
+                G = a.ops[i].G;
+                gl = t0 - u * q.Gs;
+                src = a.ops[i].w + ((size_t)(q.ub + u) * G + q.g_lo + gl) * kTileBytes;
                 return;
             }
         }
@@ -132,9 +163,9 @@ struct Cursor {
     // Copy the cursor's next chunk -- up to 4 tiles, not past the end of the
     // band's run nor of the range -- into dst (lane 0), completing on bar;
     // advance.  False (nothing issued) at the end of the stream.
-    __device__ __forceinline__ bool issue(const StepOp* ops, int nops, int c, int NC, int w, int lane, uint32_t dst,
+    __device__ __forceinline__ bool issue(const StepArgs& a, const uint4* geo, int w, int lane, uint32_t dst,
                                           uint32_t bar) {
-        if (i >= nops) return false;
+        if (i >= a.nops) return false;
         const int n = min(kSlotTiles, min(Gs - gl, t1 - t));
         if (lane == 0) {
             tc::mbar_arrive_expect_tx(bar, (uint32_t)(n * kTileBytes));
@@ -149,7 +180,7 @@ struct Cursor {
         t += n;
         if (t == t1) {
             ++i;
-            seek(ops, nops, c, NC, w);
+            seek(a, geo, w);
         }
         return true;
     }
@@ -212,25 +243,24 @@ __device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, in
 }
 
 template <int MP>
-__global__ void __launch_bounds__(kThreads, 1) step_kernel(StepParams p) {
+__global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepArgs a) {
     constexpr int NT = (MP + 7) / 8;
     constexpr int PB = 16 * MP;  // floats of one parked band partial
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NC = gridDim.x, c = blockIdx.x, M = p.M, nops = p.nops;
-    const StepSmem L(p.ring, MP, p.gpc_max, nops);
+    const int NC = gridDim.x, c = blockIdx.x, M = a.M, nops = a.nops;
+    const StepSmem L(a.ring, MP, a.gpc_max, nops);
     const int R = L.R;
     const uint32_t sbase = tc::smem_addr(smem);
     const uint32_t ring_w = sbase + (uint32_t)(warp * R * kSlotTiles * kTileBytes);
     const uint32_t bar_w = sbase + (uint32_t)(L.bar + warp * R * 8);
-    StepOp* ops = reinterpret_cast<StepOp*>(smem + L.ops);
+    uint4* geo = reinterpret_cast<uint4*>(smem + L.geo);
     uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L.x);
     float* xsum = reinterpret_cast<float*>(smem + L.xsum);
     float* park = reinterpret_cast<float*>(smem + L.park);
     float* park_w = park + warp * 2 * PB;
 
-    for (int k = threadIdx.x; k < nops * 4; k += kThreads)
-        reinterpret_cast<uint4*>(ops)[k] = __ldg(reinterpret_cast<const uint4*>(p.ops) + k);
+    for (int i = threadIdx.x; i < nops; i += kThreads) put_geo(geo + i, a.ops[i], c);
     if (lane < R) tc::mbar_init(bar_w + 8 * lane, 1);
     tc::mbar_init_fence();
     __syncthreads();
@@ -238,37 +268,39 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(StepParams p) {
     // fill this warp's ring
     Cursor cur;
     cur.i = 0;
-    cur.seek(ops, nops, c, NC, warp);
-    uint32_t n_iss = 0, n_con = 0, n_obs = 0;  // issued, consumed, observed complete
+    cur.seek(a, geo, warp);
+    int inflight = 0;
     for (int s = 0; s < R; ++s) {
-        if (!cur.issue(ops, nops, c, NC, warp, lane, ring_w + (uint32_t)(s * kSlotTiles * kTileBytes), bar_w + 8 * s))
-            break;
-        ++n_iss;
+        if (!cur.issue(a, geo, warp, lane, ring_w + (uint32_t)(s * kSlotTiles * kTileBytes), bar_w + 8 * s)) break;
+        ++inflight;
     }
+    int slot = 0;           // next slot to consume
+    uint32_t phase = 0;     // its expected completion parity
     bool ok = true;
 
     for (int i = 0; i < nops; ++i) {
-        const StepOp& o = ops[i];
+        const StepOp& o = a.ops[i];
         if (i > 0) {
             // x_i may be computed from y_(i-1): wait until every CTA is done with it
             if (threadIdx.x == 0) {
                 const long long t0 = clock64();
-                while (ld_acquire(p.done + (i - 1)) < (unsigned)NC) {
+                while (ld_acquire(a.done + (i - 1)) < (unsigned)NC) {
                     if (clock64() - t0 > (1ll << 31)) {
-                        atomicOr(p.status, 2);
+                        atomicOr(a.status, 2);
                         break;
                     }
                 }
             }
             __syncthreads();
         }
-        const Geo q = geometry(o, c, NC);
+        const Geo q = get_geo(geo + i);
         if (q.nu > 0) {
             dec::stage_x_async<MP, kThreads>(o.x, M, o.K, q.g_lo, q.Gs, xs, xsum);
             dec::TileMac<MP> mac(sbase + L.x, sbase + L.xsum, lane);
-            const int t0 = warp_lo(q.Tc, warp), t1 = warp_lo(q.Tc, warp + 1);
-            const int u_first = t0 / q.Gs;
-            int t = t0, gl = t0 % q.Gs, u = u_first;
+            const int Tc = q.Tc();
+            const int t0 = warp_lo(Tc, warp), t1 = warp_lo(Tc, warp + 1);
+            const int u_first = div_small(t0, q.Gs, q.inv_gs);
+            int t = t0, gl = t0 - u_first * q.Gs, u = u_first;
             float acc[NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -276,32 +308,32 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(StepParams p) {
                 for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
             while (t < t1) {
                 const int n = min(kSlotTiles, min(q.Gs - gl, t1 - t));  // the chunk the cursor copied
-                const uint32_t slot = n_con % (uint32_t)R;
-                const uint32_t ta = ring_w + slot * (kSlotTiles * kTileBytes), bar = bar_w + 8 * slot;
                 if (ok) {
-                    const bool got = tc::mbar_wait(bar, (n_con / (uint32_t)R) & 1);
+                    const uint32_t ta = ring_w + (uint32_t)(slot * kSlotTiles * kTileBytes), bar = bar_w + 8 * slot;
+                    const bool got = tc::mbar_wait(bar, phase);
                     if (__all_sync(0xFFFFFFFFu, got)) {
-                        ++n_obs;
+                        --inflight;
+                        if (n == kSlotTiles) {
+                            if constexpr (MP >= 8) {  // register budget: two pairs
+                                mac.template run_tiles<2>(ta, gl, lane, acc);
+                                mac.template run_tiles<2>(ta + 2 * kTileBytes, gl + 2, lane, acc);
+                            } else {
+                                mac.template run_tiles<kSlotTiles>(ta, gl, lane, acc);
+                            }
+                        } else {
+                            for (int j = 0; j < n; ++j) mac.run(ta + (uint32_t)(j * kTileBytes), gl + j, lane, acc);
+                        }
+                        __syncwarp();  // every lane is done reading the slot
+                        if (cur.issue(a, geo, warp, lane, ta, bar)) ++inflight;
+                        if (++slot == R) {
+                            slot = 0;
+                            phase ^= 1;
+                        }
                     } else {
-                        if (lane == 0) atomicOr(p.status, 4);
+                        if (lane == 0) atomicOr(a.status, 4);
                         ok = false;
                     }
                 }
-                if (ok) {
-                    if (n == kSlotTiles) {
-                        if constexpr (MP >= 8) {  // register budget: two pairs
-                            mac.template run_tiles<2>(ta, gl, lane, acc);
-                            mac.template run_tiles<2>(ta + 2 * kTileBytes, gl + 2, lane, acc);
-                        } else {
-                            mac.template run_tiles<kSlotTiles>(ta, gl, lane, acc);
-                        }
-                    } else {
-                        for (int j = 0; j < n; ++j) mac.run(ta + (uint32_t)(j * kTileBytes), gl + j, lane, acc);
-                    }
-                }
-                __syncwarp();
-                ++n_con;
-                if (ok && cur.issue(ops, nops, c, NC, warp, lane, ta, bar)) ++n_iss;
                 t += n;
                 gl += n;
                 if (gl == q.Gs || t == t1) {
@@ -323,19 +355,19 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(StepParams p) {
                 }
             }
             __syncthreads();
-            // bands cut between warps: the lowest warp whose range starts
-            // strictly inside the band adds the parked shares in warp order
-            const int tw = t0 % q.Gs;
-            if (warp > 0 && t0 < q.Tc && tw != 0 && warp_lo(q.Tc, warp - 1) <= t0 - tw) {
-                const int bs = u_first * q.Gs, be = bs + q.Gs;  // the band's tiles
+            // a band cut between warps is added up, in warp order, by the
+            // lowest warp whose range starts strictly inside it (warp - 1
+            // then holds the band's first tile)
+            const int bs = u_first * q.Gs, be = bs + q.Gs;
+            if (warp > 0 && t0 < Tc && t0 != bs && warp_lo(Tc, warp - 1) <= bs) {
                 finish_band(o, q.ub + u_first, q.r, M, lane, [&](auto&& f) {
                     for (int oi = lane; oi < 16 * M; oi += 32) {
                         const int row = oi / M, m = oi - row * M;
                         float sum = 0.f;
-                        for (int w2 = 0; w2 < kWarps; ++w2) {
-                            const int a = warp_lo(q.Tc, w2), b = warp_lo(q.Tc, w2 + 1);
-                            if (a < b && a < be && b > bs)
-                                sum += park[(w2 * 2 + (a >= bs ? 0 : 1)) * PB + row * MP + m];
+                        for (int w2 = warp - 1; w2 < kWarps; ++w2) {
+                            const int lo = warp_lo(Tc, w2), hi = warp_lo(Tc, w2 + 1);
+                            if (lo >= be) break;
+                            if (lo < hi) sum += park[(w2 * 2 + (lo >= bs ? 0 : 1)) * PB + row * MP + m];
                         }
                         f(row, m, sum);
                     }
@@ -348,26 +380,33 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(StepParams p) {
         __syncthreads();
         if (threadIdx.x == 0) {
             __threadfence();
-            atomicAdd(p.done + i, 1u);
+            atomicAdd(a.done + i, 1u);
         }
     }
 
     // copies still in flight after a timeout
-    for (; n_obs < n_iss; ++n_obs)
-        if (!tc::mbar_wait(bar_w + 8 * (n_obs % (uint32_t)R), (n_obs / (uint32_t)R) & 1)) break;
+    for (; inflight > 0; --inflight) {
+        if (!tc::mbar_wait(bar_w + 8 * slot, phase)) break;
+        if (++slot == R) {
+            slot = 0;
+            phase ^= 1;
+        }
+    }
 
     // the last CTA out resets the counters for the next step
     if (threadIdx.x == 0) {
         __threadfence();
-        if (atomicAdd(p.exit_cnt, 1u) == (unsigned)(NC - 1)) {
-            for (int i = 0; i < nops; ++i) p.done[i] = 0;
-            *p.exit_cnt = 0;
+        if (atomicAdd(a.exit_cnt, 1u) == (unsigned)(NC - 1)) {
+            for (int i = 0; i < nops; ++i) a.done[i] = 0;
+            *a.exit_cnt = 0;
             __threadfence();
         }
     }
 }
 
-StepFn step_fn(int MP) {
+using StepKernel = void (*)(StepArgs);
+
+StepKernel step_fn(int MP) {
     switch (MP) {
         case 1: return step_kernel<1>;
         case 2: return step_kernel<2>;
@@ -388,7 +427,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 struct StepPlan {
     int MP = 1, NC = 0, gpc_max = 1, R = 0, smem = 0;
     std::vector<StepOp> ops;  // device pointers filled against a workspace base
-    size_t table_off = 0, done_off = 0, exit_off = 0, status_off = 0, total = 0;
+    size_t done_off = 0, exit_off = 0, status_off = 0, total = 0;
     std::vector<size_t> cnt_off, part_off;
 };
 
@@ -421,7 +460,7 @@ static bool plan_step(const w4_weight* w, int n, int M, int NC, StepPlan* pl) {
     pl->cnt_off.assign(n, 0);
     pl->part_off.assign(n, 0);
     pl->gpc_max = 1;
-    bool fits = NC > 0;
+    bool fits = NC > 0 && n <= kMaxStepOps;
     for (int i = 0; i < n && fits; ++i) {
         StepOp& o = pl->ops[i];
         o.N = (int)w[i].N;
@@ -429,11 +468,16 @@ static bool plan_step(const w4_weight* w, int n, int M, int NC, StepPlan* pl) {
         o.G = (int)(w[i].K / kGroupK);
         o.bands = (int)num_bands(w[i].N);
         o.S = choose_split(o.bands, o.G, pl->MP, NC);
-        if (o.S == 0 || (long long)o.bands * NC >= INT_MAX) {
+        if (o.S == 0) {
             fits = false;
             o.S = 1;
         }
         o.cps = NC / o.S;
+        // 16-bit fields of the per-CTA share table, 32-bit share arithmetic
+        const long long cta_tiles = (long long)((o.bands + o.cps - 1) / o.cps) * ((o.G + o.S - 1) / o.S);
+        if (o.bands >= 65536 || o.G >= 65536 || (long long)o.bands * NC >= INT_MAX ||
+            (long long)o.G * o.S >= INT_MAX || cta_tiles >= kMaxCtaTiles)
+            fits = false;
         pl->gpc_max = std::max(pl->gpc_max, (o.G + o.S - 1) / o.S);
     }
     const int fixed = StepSmem(0, pl->MP, pl->gpc_max, n).total;
@@ -441,8 +485,6 @@ static bool plan_step(const w4_weight* w, int n, int M, int NC, StepPlan* pl) {
     while (pl->R > 0 && StepSmem(pl->R, pl->MP, pl->gpc_max, n).total > kSmemBudget) --pl->R;
     pl->smem = StepSmem(pl->R, pl->MP, pl->gpc_max, n).total;
     size_t off = 0;
-    pl->table_off = off;
-    off = align_up(off + sizeof(StepOp) * n);
     pl->done_off = off;
     off = align_up(off + sizeof(unsigned) * n);
     pl->exit_off = off;
@@ -472,7 +514,7 @@ static int sm_count_now() {
 // One resident CTA per SM, or 0 if the kernel cannot be resident.
 static int step_grid(int MP, int smem) {
     int per_sm = 0;
-    StepFn fn = step_fn(MP);
+    StepKernel fn = step_fn(MP);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess) return 0;
     return per_sm >= 1 ? sm_count_now() : 0;
@@ -489,7 +531,9 @@ w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y,
     const int MP = padded(M);
     StepPlan pl;
     if (!plan_step(w, n, M, sm_count_now(), &pl)) {
-        set_error("the persistent step kernel cannot hold this sequence in shared memory (%d projections)", n);
+        set_error("the persistent step kernel cannot take this sequence (%d projections; at most %d, and each "
+                  "must fit its shared-memory and index limits)",
+                  n, kMaxStepOps);
         return W4_ERR_UNSUPPORTED;
     }
     const int NC = step_grid(MP, pl.smem);
@@ -515,27 +559,27 @@ w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y,
         o.part = o.S > 1 ? reinterpret_cast<float*>(base + pl.part_off[i]) : nullptr;
     }
     W4_CUDA_TRY(cudaMemsetAsync(ws, 0, pl.total, stream));
-    W4_CUDA_TRY(cudaMemcpyAsync(base + pl.table_off, pl.ops.data(), sizeof(StepOp) * n, cudaMemcpyHostToDevice,
-                                stream));
     W4_CUDA_TRY(cudaStreamSynchronize(stream));
-    out->fn = step_fn(MP);
+    out->args.assign(sizeof(StepArgs), 0);
+    StepArgs* a = reinterpret_cast<StepArgs*>(out->args.data());
+    a->nops = n;
+    a->M = M;
+    a->done = reinterpret_cast<unsigned*>(base + pl.done_off);
+    a->exit_cnt = reinterpret_cast<unsigned*>(base + pl.exit_off);
+    a->status = reinterpret_cast<int*>(base + pl.status_off);
+    a->gpc_max = pl.gpc_max;
+    a->ring = pl.R;
+    std::copy(pl.ops.begin(), pl.ops.end(), a->ops);
+    out->fn = reinterpret_cast<const void*>(step_fn(MP));
+    out->status = a->status;
     out->NC = NC;
     out->smem = pl.smem;
-    StepParams& p = out->params;
-    p.ops = reinterpret_cast<const StepOp*>(base + pl.table_off);
-    p.nops = n;
-    p.M = M;
-    p.done = reinterpret_cast<unsigned*>(base + pl.done_off);
-    p.exit_cnt = reinterpret_cast<unsigned*>(base + pl.exit_off);
-    p.status = reinterpret_cast<int*>(base + pl.status_off);
-    p.gpc_max = pl.gpc_max;
-    p.ring = pl.R;
     return W4_OK;
 }
 
 int step_status(const StepLaunch& s) {
     int v = 0;
-    if (cudaMemcpy(&v, s.params.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+    if (!s.status || cudaMemcpy(&v, s.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
     return v;
 }
 
@@ -550,7 +594,8 @@ w4_status step_launch(const StepLaunch& s, cudaStream_t stream) {
     attr.val.cooperative = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, s.fn, s.params);
+    void* params[] = {const_cast<unsigned char*>(s.args.data())};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, s.fn, params);
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(step)");
     return W4_OK;
 }

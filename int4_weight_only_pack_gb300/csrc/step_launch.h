@@ -4,27 +4,20 @@
 
 #include <cuda_runtime.h>
 
+#include <vector>
+
 #include "w4.h"
 
 namespace w4 {
 
-struct StepOp;
-
-struct StepParams {
-    const StepOp* ops;
-    int nops, M;
-    unsigned* done;      // [nops] CTAs finished with each projection
-    unsigned* exit_cnt;  // CTAs finished with the step
-    int* status;         // set non-zero when a wait gives up
-    int gpc_max;         // largest x slice (groups): shared-memory sizing
-    int ring;            // ring slots (tiles) per warp
-};
-
-using StepFn = void (*)(StepParams);
+// Projections one persistent launch can carry (its table travels in the
+// kernel's parameter space).
+constexpr int kMaxStepOps = 448;
 
 struct StepLaunch {
-    StepFn fn = nullptr;
-    StepParams params{};
+    const void* fn = nullptr;
+    std::vector<unsigned char> args;  // the kernel's parameter block
+    int* status = nullptr;            // device status word
     int NC = 0, smem = 0;
 };
 
