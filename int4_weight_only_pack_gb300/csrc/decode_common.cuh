@@ -50,15 +50,21 @@ __device__ __forceinline__ void mma16816_zero(float (&c)[4], const uint32_t (&a)
 }
 
 // Shared-memory bytes of an x slice of Gs groups for MP padded tokens, and of
-// its per-group sums.
+// its per-group sums: xsum[gl * xsum_stride(MP) + m] (the stride is even so
+// that a lane reads its token pair as one float2; eight floats of slack cover
+// the reads of lanes whose MMA columns are padding and never written).  Both
+// sizes are multiples of 16 bytes, so what follows them stays 16-byte aligned.
 __host__ __device__ constexpr int x_bytes(int MP, int Gs) { return MP * Gs * 256; }
-__host__ __device__ constexpr int xsum_bytes(int Gs) { return Gs * 16 * 4; }
+__host__ __device__ constexpr int xsum_stride(int MP) { return MP < 2 ? 2 : MP; }
+__host__ __device__ constexpr int xsum_bytes(int MP, int Gs) {
+    return ((Gs * xsum_stride(MP) + 8) * 4 + 15) & ~15;
+}
 
 // Stage x[0:M, 128*g_lo : 128*(g_lo+Gs)) (fp16 pairs; row stride K/2 words)
 // into `xs` in fragment order -- word (gl, q, m, c, e) at
 // gl*MP*64 + q*MP*16 + (m*4 + c)*4 + e holds k16 step 2q + (e >> 1) of group
 // gl, k 4c + 2(e & 1) .. +1 -- with rows M..MP-1 zero, and the sum of x over
-// every group and token into xsum[gl*16 + m] (0 for m >= M).  Called by the
+// every group and token m < M into xsum[gl*xsum_stride(MP) + m].  Called by the
 // consumer threads only; returns with all of them synchronised.
 template <int MP, int NCONS = kConsumers>
 __device__ __forceinline__ void stage_x(const uint32_t* x, int M, int K, int g_lo, int Gs, uint32_t* xs,
@@ -94,8 +100,6 @@ __device__ __forceinline__ void stage_x(const uint32_t* x, int M, int K, int g_l
             }
         }
     }
-    for (int idx = tid; idx < Gs * 16; idx += kConsumers)
-        if ((idx & 15) >= M) xsum[idx] = 0.f;
     tc::named_barrier(1, kConsumers);
     // FP32 sums in a fixed order: four values per lane, then a butterfly
     for (int idx = warp; idx < Gs * M; idx += kConsumerWarps) {
@@ -107,7 +111,7 @@ __device__ __forceinline__ void stage_x(const uint32_t* x, int M, int K, int g_l
         float sum = (f0.x + f0.y) + (f1.x + f1.y);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-        if (lane == 0) xsum[gl * 16 + m] = sum;
+        if (lane == 0) xsum[gl * xsum_stride(MP) + m] = sum;
     }
     tc::named_barrier(1, kConsumers);
 }
@@ -141,8 +145,6 @@ __device__ __forceinline__ void stage_x_async(const uint32_t* x, int M, int K, i
         }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    for (int idx = tid; idx < Gs * 16; idx += NCONS)
-        if ((idx & 15) >= M) xsum[idx] = 0.f;
     tc::named_barrier(1, NCONS);
     for (int idx = warp; idx < Gs * M; idx += kWarps) {
         const int gl = idx / M, m = idx - gl * M;
@@ -153,7 +155,7 @@ __device__ __forceinline__ void stage_x_async(const uint32_t* x, int M, int K, i
         float sum = (f0.x + f0.y) + (f1.x + f1.y);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-        if (lane == 0) xsum[gl * 16 + m] = sum;
+        if (lane == 0) xsum[gl * xsum_stride(MP) + m] = sum;
     }
     tc::named_barrier(1, NCONS);
 }
@@ -213,7 +215,7 @@ struct TileMac {
             float2 X;
             asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];"
                          : "=f"(X.x), "=f"(X.y)
-                         : "r"(xsum + (uint32_t)((gl * 16 + nt * 8) * 4)));
+                         : "r"(xsum + (uint32_t)((gl * xsum_stride(MP) + nt * 8) * 4)));
             acc[nt][0] = fmaf(ca, X.x, fmaf(sa, pe[nt][0] + po[nt][0], acc[nt][0]));
             acc[nt][1] = fmaf(ca, X.y, fmaf(sa, pe[nt][1] + po[nt][1], acc[nt][1]));
             acc[nt][2] = fmaf(cb, X.x, fmaf(sb, pe[nt][2] + po[nt][2], acc[nt][2]));
@@ -270,7 +272,7 @@ struct TileMac {
                 float2 X;
                 asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];"
                              : "=f"(X.x), "=f"(X.y)
-                             : "r"(xsum + (uint32_t)(((gl + n) * 16 + nt * 8) * 4)));
+                             : "r"(xsum + (uint32_t)(((gl + n) * xsum_stride(MP) + nt * 8) * 4)));
                 acc[nt][0] = fmaf(ca, X.x, fmaf(sa, pe[n][nt][0] + po[n][nt][0], acc[nt][0]));
                 acc[nt][1] = fmaf(ca, X.y, fmaf(sa, pe[n][nt][1] + po[n][nt][1], acc[nt][1]));
                 acc[nt][2] = fmaf(cb, X.x, fmaf(sb, pe[n][nt][2] + po[n][nt][2], acc[nt][2]));

@@ -84,7 +84,7 @@ struct SmemLayout {
         bar = ring * kTileBytes;                                 // ring of 8-tile slots first
         x = (bar + (2 * (ring / kChunk) + 4) * 8 + 15) & ~15;    // full/empty per slot, cfull[2], cempty[2]
         xsum = x + dec::x_bytes(MP, gpc);                        // x slice in fragment order
-        red = xsum + dec::xsum_bytes(gpc);                       // per group and token: sum of x
+        red = xsum + dec::xsum_bytes(MP, gpc);                   // per group and token: sum of x
         cpart = red + 2 * dec::red_floats(BB, NT) * 4;           // per-warp block partials, 2 buffers
         total = cpart + 2 * (S > 1 ? S - 1 : 0) * BB * 16 * M * 4;  // leader's receive buffers
     }

@@ -82,7 +82,7 @@ constexpr int kMaxRing = 32;             // slots per warp (one mbarrier per lan
 constexpr int kSplitPenalty = 16;        // tiles: the cost of combining K-split partials
 constexpr int kMaxCtaTiles = 1 << 22;    // per-CTA tiles of one projection (float division below)
 // x slice + its group sums: small for few tokens so that the rings keep three slots per warp
-__host__ __device__ constexpr int x_budget(int MP) { return MP <= 4 ? 14 * 1024 : 48 * 1024; }
+__host__ __device__ constexpr int x_budget(int MP) { return MP <= 4 ? 20 * 1024 : 48 * 1024; }
 
 struct StepSmem {
     int R, bar, geo, x, xsum, park, total;
@@ -92,7 +92,7 @@ struct StepSmem {
         geo = bar + kWarps * R * 8;
         x = (geo + nops * 16 + 127) & ~127;
         xsum = x + dec::x_bytes(MP, gpc_max);
-        park = xsum + dec::xsum_bytes(gpc_max);
+        park = xsum + dec::xsum_bytes(MP, gpc_max);
         total = park + kWarps * 2 * 16 * MP * 4;
     }
 };
@@ -143,6 +143,7 @@ __device__ __forceinline__ int div_small(int t, int d, float inv) {
 struct Cursor {
     int i, t, t1, gl, Gs, G;
     const uint8_t* src;
+    uint64_t policy;  // weights are read once: first out of L2
 
     __device__ __forceinline__ void seek(const StepArgs& a, const uint4* geo, int w) {
         for (; i < a.nops; ++i) {
@@ -169,7 +170,7 @@ struct Cursor {
         const int n = min(kSlotTiles, min(Gs - gl, t1 - t));
         if (lane == 0) {
             tc::mbar_arrive_expect_tx(bar, (uint32_t)(n * kTileBytes));
-            tc::bulk_load(dst, src, (uint32_t)(n * kTileBytes), bar);
+            tc::bulk_load_hint(dst, src, (uint32_t)(n * kTileBytes), bar, policy);
         }
         src += (size_t)n * kTileBytes;
         gl += n;
@@ -261,13 +262,26 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     float* park_w = park + warp * 2 * PB;
 
     for (int i = threadIdx.x; i < nops; i += kThreads) put_geo(geo + i, a.ops[i], c);
+    // x slices are small and read by every CTA of a split: keep the next one
+    // warm in L2 (as it is when x has just been written)
+    auto prefetch_x = [&](int i) {
+        if (i < nops) {
+            const Geo q = get_geo(geo + i);
+            const StepOp& o = a.ops[i];
+            if (q.nu > 0)
+                for (int m = 0; m < M; ++m)
+                    tc::prefetch_l2(o.x + (size_t)m * (o.K / 2) + (size_t)q.g_lo * 64, (uint32_t)(q.Gs * 256));
+        }
+    };
     if (lane < R) tc::mbar_init(bar_w + 8 * lane, 1);
     tc::mbar_init_fence();
     __syncthreads();
+    if (threadIdx.x == 0) prefetch_x(0);
 
     // fill this warp's ring
     Cursor cur;
     cur.i = 0;
+    cur.policy = tc::policy_evict_first();
     cur.seek(a, geo, warp);
     int inflight = 0;
     for (int s = 0; s < R; ++s) {
@@ -280,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
     for (int i = 0; i < nops; ++i) {
         const StepOp& o = a.ops[i];
+        if (threadIdx.x == 32) prefetch_x(i + 1);
         if (i > 0) {
             // x_i may be computed from y_(i-1): wait until every CTA is done with it
             if (threadIdx.x == 0) {
@@ -313,15 +328,16 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     const bool got = tc::mbar_wait(bar, phase);
                     if (__all_sync(0xFFFFFFFFu, got)) {
                         --inflight;
-                        if (n == kSlotTiles) {
-                            if constexpr (MP >= 8) {  // register budget: two pairs
-                                mac.template run_tiles<2>(ta, gl, lane, acc);
-                                mac.template run_tiles<2>(ta + 2 * kTileBytes, gl + 2, lane, acc);
-                            } else {
-                                mac.template run_tiles<kSlotTiles>(ta, gl, lane, acc);
-                            }
+                        static_assert(kSlotTiles == 4, "chunk cases below");
+                        if constexpr (MP >= 8) {  // register budget: at most two tiles at once
+                            if (n >= 2) mac.template run_tiles<2>(ta, gl, lane, acc);
+                            if (n == 4) mac.template run_tiles<2>(ta + 2 * kTileBytes, gl + 2, lane, acc);
+                            if (n & 1) mac.run(ta + (uint32_t)((n - 1) * kTileBytes), gl + n - 1, lane, acc);
                         } else {
-                            for (int j = 0; j < n; ++j) mac.run(ta + (uint32_t)(j * kTileBytes), gl + j, lane, acc);
+                            if (n == 4) mac.template run_tiles<4>(ta, gl, lane, acc);
+                            else if (n == 3) mac.template run_tiles<3>(ta, gl, lane, acc);
+                            else if (n == 2) mac.template run_tiles<2>(ta, gl, lane, acc);
+                            else mac.run(ta, gl, lane, acc);
                         }
                         __syncwarp();  // every lane is done reading the slot
                         if (cur.issue(a, geo, warp, lane, ta, bar)) ++inflight;
@@ -378,10 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         // thread's y stores before thread 0's fence, which makes them visible
         // before the completion count
         __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            atomicAdd(a.done + i, 1u);
-        }
+        if (threadIdx.x == 0)
+            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.done + i) : "memory");
     }
 
     // copies still in flight after a timeout
@@ -440,7 +454,7 @@ static int choose_split(int bands, int G, int MP, int NC) {
     for (int S = 1; S <= std::min(G, NC); ++S) {
         if (NC % S) continue;
         const int Gs = (G + S - 1) / S;
-        if (dec::x_bytes(MP, Gs) + dec::xsum_bytes(Gs) > x_budget(MP)) continue;
+        if (dec::x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs) > x_budget(MP)) continue;
         const int cps = NC / S;
         const long cost = (long)((bands + cps - 1) / cps) * Gs + (S > 1 ? kSplitPenalty : 0);
         if (cost < best_cost) {
