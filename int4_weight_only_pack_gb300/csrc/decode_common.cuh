@@ -160,72 +160,57 @@ __device__ __forceinline__ void stage_x_async(const uint32_t* x, int M, int K, i
     tc::named_barrier(1, NCONS);
 }
 
+// Predicated shared-memory loads: lanes whose predicate is false issue no
+// access (and cost no bandwidth) and keep the register's previous contents.
+__device__ __forceinline__ void lds128_if(uint4& v, uint32_t a, uint32_t pred) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n @p ld.shared.v4.u32 {%0,%1,%2,%3}, [%5];\n}\n"
+        : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+        : "r"(pred), "r"(a));
+}
+__device__ __forceinline__ void lds64f_if(float2& v, uint32_t a, uint32_t pred) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p ld.shared.v2.f32 {%0,%1}, [%3];\n}\n"
+                 : "+f"(v.x), "+f"(v.y)
+                 : "r"(pred), "r"(a));
+}
+
 // Per-lane state of the tile multiply-accumulate.
+//
+// Lane L = 4*tok + cl4 holds the B fragment of MMA column tok (a token) and
+// the accumulators of tokens nt*8 + 2*cl4 + {0, 1}.  Only lanes of real
+// (padded) tokens, tok < MP, load x fragments and only lanes whose first
+// token is real load group sums: the other lanes' MMA columns are never
+// written out, so whatever their registers hold is harmless, and the loads
+// they skip are shared-memory bandwidth saved.
 template <int MP>
 struct TileMac {
     static constexpr int NT = (MP + 7) / 8;  // n8 token tiles of the MMA
+    static constexpr int NE = MP == 1 ? 1 : 2;  // tokens per lane that can be real (token 2*cl4 + 1 >= MP=1)
     uint32_t xfrag;                          // this lane's B-fragment words of group 0
     uint32_t xsum;                           // this lane's token pair's sums of group 0
-    uint4 xb[NT][4];
+    uint32_t xl, sl;                         // load predicates: x fragments, group sums
+    uint4 xv[4][NT];                         // x fragments of up to four tiles
+    float2 X[4][NT];                         // group sums of up to four tiles
 
-    // Lanes of the MMA's padding token columns (tok >= MP) read the fragment
-    // of token tok % MP: those output columns are never written, and a real
-    // token's (finite) values keep them finite.
     __device__ __forceinline__ TileMac(uint32_t x_smem, uint32_t xsum_smem, int lane) {
         const int tok = lane >> 2, cl4 = lane & 3;
         xfrag = x_smem + (uint32_t)(((tok % MP) * 4 + cl4) * 16);
         xsum = xsum_smem + (uint32_t)(2 * cl4 * 4);
-    }
-
-    // acc += s * sum_{k in group gl} x * q for the tile at shared address ta.
-    __device__ __forceinline__ void run(uint32_t ta, int gl, int lane, float (&acc)[NT][4]) {
-        const uint4 lo = lds128(ta + 16 * lane), hi = lds128(ta + 512 + 16 * lane);
-        const uint32_t sc = lds32(ta + kScaleOffset + 4 * (lane >> 2));
-        {
-            const uint32_t xa = xfrag + (uint32_t)gl * (MP * 256);
+        xl = tok < MP;
+        sl = 2 * cl4 < MP || MP >= 8;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) xb[nt][q] = lds128(xa + (uint32_t)(q * MP * 64 + nt * 512));
-        }
-        float pe[NT][4], po[NT][4];
-        const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            uint32_t a[4];
-            unpack_word_biased(wd[j], a);
+        for (int n = 0; n < 4; ++n)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const uint4& v = xb[nt][j >> 1];
-                if (j == 0)
-                    mma16816_zero(pe[nt], a, v.x, v.y);
-                else if (j == 1)
-                    mma16816_zero(po[nt], a, v.z, v.w);
-                else if (j & 1)
-                    mma16816(po[nt], a, v.z, v.w);
-                else
-                    mma16816(pe[nt], a, v.x, v.y);
+                xv[n][nt] = make_uint4(0, 0, 0, 0);
+                X[n][nt] = make_float2(0.f, 0.f);
             }
-        }
-        const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sc));
-        const float sa = sf.x * 16777216.f, sb = sf.y * 1048576.f;
-        const float ca = -8.f * sf.x, cb = -8.f * sf.y;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            float2 X;
-            asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];"
-                         : "=f"(X.x), "=f"(X.y)
-                         : "r"(xsum + (uint32_t)((gl * xsum_stride(MP) + nt * 8) * 4)));
-            acc[nt][0] = fmaf(ca, X.x, fmaf(sa, pe[nt][0] + po[nt][0], acc[nt][0]));
-            acc[nt][1] = fmaf(ca, X.y, fmaf(sa, pe[nt][1] + po[nt][1], acc[nt][1]));
-            acc[nt][2] = fmaf(cb, X.x, fmaf(sb, pe[nt][2] + po[nt][2], acc[nt][2]));
-            acc[nt][3] = fmaf(cb, X.y, fmaf(sb, pe[nt][3] + po[nt][3], acc[nt][3]));
-        }
     }
 
-    // The same for NTL consecutive tiles at ta, ta + 1056, ... (groups gl,
-    // gl + 1, ... of one band), their MMA chains interleaved.  The tiles are
-    // added to acc in order, so the result equals NTL calls of run().
+    // acc += s * sum_{k in group} x * q for NTL consecutive tiles at ta, ta +
+    // 1056, ... (groups gl, gl + 1, ... of one band), their MMA chains
+    // interleaved; the tiles are added to acc in order.  Per tile and row:
+    //     acc += s * (2^24 * D - 8 * sum_k x)      (2^20 for rows r + 8)
     template <int NTL>
     __device__ __forceinline__ void run_tiles(uint32_t ta, int gl, int lane, float (&acc)[NT][4]) {
         uint32_t wd[NTL][8], sc[NTL];
@@ -236,6 +221,9 @@ struct TileMac {
             wd[n][0] = lo.x, wd[n][1] = lo.y, wd[n][2] = lo.z, wd[n][3] = lo.w;
             wd[n][4] = hi.x, wd[n][5] = hi.y, wd[n][6] = hi.z, wd[n][7] = hi.w;
             sc[n] = lds32(tn + kScaleOffset + 4 * (lane >> 2));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                lds64f_if(X[n][nt], xsum + (uint32_t)(((gl + n) * xsum_stride(MP) + nt * 8) * 4), sl);
         }
         const uint32_t xa0 = xfrag + (uint32_t)gl * (MP * 256);
         float pe[NTL][NT][4], po[NTL][NT][4];
@@ -243,42 +231,43 @@ struct TileMac {
         for (int q = 0; q < 4; ++q) {  // k16 steps 2q (even chain) and 2q + 1 (odd chain)
 #pragma unroll
             for (int n = 0; n < NTL; ++n) {
-                uint4 v[NT];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
-                    v[nt] = lds128(xa0 + (uint32_t)(n * MP * 256 + q * MP * 64 + nt * 512));
+                    lds128_if(xv[n][nt], xa0 + (uint32_t)(n * MP * 256 + q * MP * 64 + nt * 512), xl);
                 uint32_t a[4], b[4];
                 unpack_word_biased(wd[n][2 * q], a);
                 unpack_word_biased(wd[n][2 * q + 1], b);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
+                    const uint4 v = xv[n][nt];
                     if (q == 0) {
-                        mma16816_zero(pe[n][nt], a, v[nt].x, v[nt].y);
-                        mma16816_zero(po[n][nt], b, v[nt].z, v[nt].w);
+                        mma16816_zero(pe[n][nt], a, v.x, v.y);
+                        mma16816_zero(po[n][nt], b, v.z, v.w);
                     } else {
-                        mma16816(pe[n][nt], a, v[nt].x, v[nt].y);
-                        mma16816(po[n][nt], b, v[nt].z, v[nt].w);
+                        mma16816(pe[n][nt], a, v.x, v.y);
+                        mma16816(po[n][nt], b, v.z, v.w);
                     }
                 }
             }
         }
 #pragma unroll
         for (int n = 0; n < NTL; ++n) {
-            const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sc[n]));
-            const float sa = sf.x * 16777216.f, sb = sf.y * 1048576.f;
-            const float ca = -8.f * sf.x, cb = -8.f * sf.y;
+            const float2 s = __half22float2(*reinterpret_cast<const __half2*>(&sc[n]));  // rows r, r + 8
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float2 X;
-                asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];"
-                             : "=f"(X.x), "=f"(X.y)
-                             : "r"(xsum + (uint32_t)(((gl + n) * xsum_stride(MP) + nt * 8) * 4)));
-                acc[nt][0] = fmaf(ca, X.x, fmaf(sa, pe[n][nt][0] + po[n][nt][0], acc[nt][0]));
-                acc[nt][1] = fmaf(ca, X.y, fmaf(sa, pe[n][nt][1] + po[n][nt][1], acc[nt][1]));
-                acc[nt][2] = fmaf(cb, X.x, fmaf(sb, pe[n][nt][2] + po[n][nt][2], acc[nt][2]));
-                acc[nt][3] = fmaf(cb, X.y, fmaf(sb, pe[n][nt][3] + po[n][nt][3], acc[nt][3]));
+#pragma unroll
+                for (int e = 0; e < NE; ++e) {
+                    const float m8x = -8.f * (e ? X[n][nt].y : X[n][nt].x);
+                    acc[nt][e] = fmaf(s.x, fmaf(16777216.f, pe[n][nt][e] + po[n][nt][e], m8x), acc[nt][e]);
+                    acc[nt][2 + e] = fmaf(s.y, fmaf(1048576.f, pe[n][nt][2 + e] + po[n][nt][2 + e], m8x), acc[nt][2 + e]);
+                }
             }
         }
+    }
+
+    // One tile.
+    __device__ __forceinline__ void run(uint32_t ta, int gl, int lane, float (&acc)[NT][4]) {
+        run_tiles<1>(ta, gl, lane, acc);
     }
 };
 

@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     if (__all_sync(0xFFFFFFFFu, got)) {
                         --inflight;
                         static_assert(kSlotTiles == 4, "chunk cases below");
-                        if constexpr (MP >= 8) {  // register budget: at most two tiles at once
+                        if constexpr (MP >= 16) {  // register budget: at most two tiles at once
                             if (n >= 2) mac.template run_tiles<2>(ta, gl, lane, acc);
                             if (n == 4) mac.template run_tiles<2>(ta + 2 * kTileBytes, gl + 2, lane, acc);
                             if (n & 1) mac.run(ta + (uint32_t)((n - 1) * kTileBytes), gl + n - 1, lane, acc);
