@@ -79,10 +79,13 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kSmemBudget = 227 * 1024;  // one CTA per SM
 constexpr int kSlotTiles = 4;            // tiles per ring slot (one bulk copy)
 constexpr int kMaxRing = 32;             // slots per warp (one mbarrier per lane at most)
-constexpr int kSplitPenalty = 16;        // tiles: the cost of combining K-split partials
+constexpr int kSplitPenalty = 64;        // tiles: the cost of combining K-split partials (~2 us of streaming),
+                                         // plus 4 per split
 constexpr int kMaxCtaTiles = 1 << 22;    // per-CTA tiles of one projection (float division below)
-// x slice + its group sums: small for few tokens so that the rings keep three slots per warp
-__host__ __device__ constexpr int x_budget(int MP) { return MP <= 4 ? 20 * 1024 : 48 * 1024; }
+// x slice + its group sums: small for one or two tokens so that the rings keep
+// three slots per warp; larger for more tokens (x grows with them), where
+// fewer K splits are worth a shallower ring
+__host__ __device__ constexpr int x_budget(int MP) { return MP <= 2 ? 20 * 1024 : 40 * 1024; }
 
 struct StepSmem {
     int R, bar, geo, x, xsum, park, total;
@@ -236,8 +239,18 @@ __device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, in
     if (!last) return;
     const float* base = o.part + (size_t)band * o.S * pb;
     visit([&](int row, int m, float) {
+        // eight partials in flight at a time, added in split order
+        const float* pp = base + row * M + m;
         float sum = 0.f;
-        for (int s = 0; s < o.S; ++s) sum += __ldcg(base + (size_t)s * pb + row * M + m);
+        int s = 0;
+        for (; s + 8 <= o.S; s += 8) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = __ldcg(pp + (size_t)(s + e) * pb);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sum += v[e];
+        }
+        for (; s < o.S; ++s) sum += __ldcg(pp + (size_t)s * pb);
         if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = __half_as_ushort(__float2half_rn(sum));
     });
     if (lane == 0) o.cnt[band] = 0;  // ready for the next replay
@@ -456,7 +469,7 @@ static int choose_split(int bands, int G, int MP, int NC) {
         const int Gs = (G + S - 1) / S;
         if (dec::x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs) > x_budget(MP)) continue;
         const int cps = NC / S;
-        const long cost = (long)((bands + cps - 1) / cps) * Gs + (S > 1 ? kSplitPenalty : 0);
+        const long cost = (long)((bands + cps - 1) / cps) * Gs + (S > 1 ? kSplitPenalty + 4 * S : 0);
         if (cost < best_cost) {
             best_cost = cost;
             best = S;
