@@ -327,10 +327,32 @@ static double shape_cost(int64_t bands, int G, int BB, int S, int slots) {
     return (double)waves * (double)((BB * Gs + kConsumerWarps - 1) / kConsumerWarps) * (S > 1 ? 1.05 : 1.0);
 }
 
+// Launch shapes measured best on GB300 (sweeps over bands per CTA, splits,
+// ring depth and CTAs per SM) for the Qwen2.5-7B projection shapes, at one
+// token and at 9-16 tokens.
+struct TunedShape {
+    int64_t N, K;
+    int m_lo, m_hi;
+    w4_gemv_config c;  // bands_per_cta, splits, depth, pdl, ctas_per_sm
+};
+static const TunedShape kTuned[] = {
+    {4608, 3584, 1, 1, {2, 1, 48, 1, 2}},   {3584, 3584, 1, 1, {2, 1, 48, 1, 1}},
+    {37888, 3584, 1, 1, {4, 1, 64, 1, 2}},  {3584, 18944, 1, 1, {4, 4, 48, 1, 2}},
+    {4608, 3584, 9, 16, {4, 2, 64, 1, 1}},  {3584, 3584, 9, 16, {2, 4, 32, 1, 1}},
+    {37888, 3584, 9, 16, {4, 2, 48, 1, 1}}, {3584, 18944, 9, 16, {2, 8, 64, 1, 1}},
+};
+
 void default_gemv_config(int M, int64_t N, int64_t K, w4_gemv_config* c) {
     const int64_t bands = num_bands(N);
     const int G = (int)num_groups(K);
     const int sms = sm_count();
+    for (const TunedShape& t : kTuned)
+        if (t.N == N && t.K == K && M >= t.m_lo && M <= t.m_hi &&
+            gemv_smem_bytes(M, G, t.c.bands_per_cta, t.c.splits, t.c.depth) <=
+                (t.c.ctas_per_sm == 2 ? 110 * 1024 : kMaxSmem)) {
+            *c = t.c;
+            return;
+        }
     double best = 1e30;
     c->bands_per_cta = 1;
     c->splits = 8;
