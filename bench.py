@@ -328,6 +328,40 @@ def prefill_layer(torch, w4, synth, st, M=512, layers=4, reps=5):
     return out
 
 
+def packed_file_load(torch, w4, st):
+    """Layer 0's four packed weights written to packed-weight files and read
+    back (header + checksum validation + one host-to-device copy each) into
+    device buffers: seconds and GB/s of payload, page-cache warm."""
+    import tempfile
+    import shutil
+    d = tempfile.mkdtemp(prefix="w4pk_")
+    try:
+        idx = [i for i, m in enumerate(st["meta"]) if m[0] == 0]
+        paths, nb = [], 0
+        t0 = time.perf_counter()
+        for i in idx:
+            p = os.path.join(d, "l0_p%d.pk" % i)
+            w4.w4_file_write(p, st["ws"][i], src_on_device=True)
+            paths.append(p)
+            nb += w4.w4_packed_bytes(st["meta"][i][2], st["meta"][i][3])
+        t_write = time.perf_counter() - t0
+        bufs = [torch.empty(w4.w4_packed_bytes(st["meta"][i][2], st["meta"][i][3]), dtype=torch.uint8,
+                            device="cuda") for i in idx]
+        for p, b in zip(paths, bufs):  # warm the page cache
+            w4.w4_file_read(p, b)
+        reps = 3
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            for p, b in zip(paths, bufs):
+                w4.w4_file_read(p, b)
+        t_read = (time.perf_counter() - t0) / reps
+        same = all(torch.equal(b, st["keep"][i][:b.numel()]) for i, b in zip(idx, bufs))
+        return {"bytes": nb, "write_s": t_write, "read_s": t_read, "read_GB/s": nb / t_read / 1e9,
+                "bit_exact": bool(same)}
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
+
+
 # ---- main ------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
@@ -460,6 +494,7 @@ def main():
         extras["per_projection_back_to_back_28_layers"] = per
         extras["small_batch_step"] = small_batch_sweep(torch, w4, synth, st)
         extras["prefill_M512"] = prefill_layer(torch, w4, synth, st)
+        extras["packed_file_layer0"] = packed_file_load(torch, w4, st)
 
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))

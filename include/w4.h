@@ -273,6 +273,44 @@ int w4_decode_seq_kernels(const w4_seq* seq);
 
 void w4_decode_seq_destroy(w4_seq* seq);
 
+/* ------------------------------------------------------------------------
+ * Packed-weight file.  The pages keep their quantised weights in a
+ * memory-mappable file that opens with a 256-byte header starting with a
+ * magic string, and refuse to load a file whose magic does not match
+ * ("Building a Custom LLM Inference Runtime ...", "The .nanoqwen File Format
+ * and Safety Protocols"; "The Architecture of Modern Inference ...", "Data
+ * Integrity and Serialization: The .nanoqwen Format").  Here a file holds ONE
+ * packed weight (the layout above) after a 256-byte little-endian header:
+ *   0 magic "W4A16PK1" | 8 u32 version 1 | 12 u32 header bytes 256 |
+ *   16 i64 N | 24 i64 K | 32 u32 group 128 | 36 u32 tile bytes 1056 |
+ *   40 u64 payload bytes | 48 u64 payload offset 256 |
+ *   56 u64 checksum of the payload | 64 u64 checksum of bytes 0..63 |
+ *   72..255 zero.  Checksum: FNV-1a 64 taken over little-endian 64-bit
+ *   words (h = 0xcbf29ce484222325; per word: h ^= w; h *= 0x100000001b3).
+ * Readers check every field, the reserved bytes and both checksums before
+ * copying anything (fail fast): any mismatch is W4_ERR_ARG with the reason in
+ * w4_last_error().  All three calls are synchronous host calls.
+ * ---------------------------------------------------------------------- */
+#define W4_FILE_HEADER_BYTES 256
+
+/* Write w to path (created or truncated).  src_on_device: w->data is device
+ * memory (copied to the host on `stream` first) or host memory. */
+w4_status w4_file_write(const char* path, const w4_weight* w,
+                        int src_on_device, void* stream);
+
+/* Validate path's header and return the weight's shape and payload size
+ * (any of the outputs may be NULL).  Does not read the payload. */
+w4_status w4_file_info(const char* path, int64_t* N, int64_t* K,
+                       size_t* payload_bytes);
+
+/* Validate path (header and payload checksum), then copy the payload into
+ * the caller's buffer dst (dst_bytes >= payload, 16-byte aligned; device
+ * memory when dst_on_device, copied on `stream` and synchronised, else host
+ * memory) and describe it in *out.  W4_ERR_WORKSPACE if dst is too small,
+ * W4_ERR_ALIGN if misaligned; nothing is written to dst on any error. */
+w4_status w4_file_read(const char* path, void* dst, size_t dst_bytes,
+                       int dst_on_device, void* stream, w4_weight* out);
+
 #ifdef __cplusplus
 }
 #endif

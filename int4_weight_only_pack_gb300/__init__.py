@@ -72,6 +72,9 @@ _SIGNATURES = {
                                                _int, _int, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
     "w4_decode_seq_status": (_int, [_vp]),
     "w4_decode_seq_destroy": (None, [_vp]),
+    "w4_file_write": (_int, [ctypes.c_char_p, ctypes.POINTER(Weight), _int, _vp]),
+    "w4_file_info": (_int, [ctypes.c_char_p, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_sz)]),
+    "w4_file_read": (_int, [ctypes.c_char_p, _vp, _sz, _int, _vp, ctypes.POINTER(Weight)]),
 }
 EXPORTED = tuple(_SIGNATURES)
 _lib = None
@@ -132,6 +135,35 @@ def w4_workspace_bytes(M: int, N: int, K: int) -> int:
 def w4_weight_view(packed, N: int, K: int) -> Weight:
     w = Weight()
     _check(lib().w4_weight_view(_addr(packed), N, K, ctypes.byref(w)))
+    return w
+
+
+def _on_device(t) -> bool:
+    return not isinstance(t, np.ndarray) and getattr(t, "is_cuda", False)
+
+
+def w4_file_write(path: str, w: Weight, src_on_device: bool, stream=None):
+    """Write one packed weight (w.data on the device or the host) to a packed-weight file."""
+    _check(lib().w4_file_write(path.encode(), ctypes.byref(w), int(src_on_device),
+                               _stream(stream) if src_on_device else None))
+
+
+def w4_file_info(path: str):
+    """(N, K, payload bytes) from a validated packed-weight file header."""
+    N, K, nb = _i64(), _i64(), _sz()
+    _check(lib().w4_file_info(path.encode(), ctypes.byref(N), ctypes.byref(K), ctypes.byref(nb)))
+    return N.value, K.value, nb.value
+
+
+def w4_file_read(path: str, dst, dst_bytes: int | None = None, stream=None) -> Weight:
+    """Validate a packed-weight file and copy its payload into dst (a CUDA
+    tensor or a host numpy array); returns the descriptor of dst."""
+    dev = _on_device(dst)
+    nb = dst_bytes if dst_bytes is not None else (dst.nbytes if isinstance(dst, np.ndarray)
+                                                  else dst.numel() * dst.element_size())
+    w = Weight()
+    _check(lib().w4_file_read(path.encode(), _addr(dst), nb, int(dev), _stream(stream) if dev else None,
+                              ctypes.byref(w)))
     return w
 
 
