@@ -328,6 +328,28 @@ def prefill_layer(torch, w4, synth, st, M=512, layers=4, reps=5):
     return out
 
 
+def bf16_step(torch, w4, synth, st, reps=100):
+    """The same 28-layer step with bfloat16 activations (same weights, x drawn
+    from the same seeds and rounded to bfloat16): us/step and weight GB/s."""
+    xs, ys = [], []
+    for (layer, pid, N, K) in st["meta"]:
+        xb = synth.x_full_bf16(synth.seed_of(CONFIG_ID, layer, pid, synth.T_X), 1, K)
+        xs.append(torch.from_numpy(xb.view(np.int16)).cuda())
+        ys.append(torch.zeros((1, N), dtype=torch.int16, device="cuda"))
+    nbw = w4.w4_decode_seq_workspace_bytes(st["ws"], 1)
+    buf = torch.zeros(nbw + 256, dtype=torch.uint8, device="cuda")
+    off = (-buf.data_ptr()) % 256
+    seq = w4.DecodeSeq(st["ws"], xs, ys, 1, workspace=buf[off:off + nbw], act="bf16")
+    for _ in range(5):
+        seq.replay()
+    ms = time_replays(torch, seq.replay, reps)
+    peak = measured_peaks()[0].get("hbm_gbs", FALLBACK_HBM_GBS)
+    out = {"us_per_step": ms * 1e3, "GB/s": BYTES_PER_STEP / (ms * 1e-3) / 1e9,
+           "frac_of_hbm": BYTES_PER_STEP / (ms * 1e-3) / 1e9 / peak, "status_word": seq.status()}
+    seq.close()
+    return out
+
+
 def packed_file_load(torch, w4, st):
     """Layer 0's four packed weights written to packed-weight files and read
     back (header + checksum validation + one host-to-device copy each) into
@@ -495,6 +517,7 @@ def main():
         extras["small_batch_step"] = small_batch_sweep(torch, w4, synth, st)
         extras["prefill_M512"] = prefill_layer(torch, w4, synth, st)
         extras["packed_file_layer0"] = packed_file_load(torch, w4, st)
+        extras["bf16_activations_step_M1"] = bf16_step(torch, w4, synth, st)
 
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))

@@ -262,6 +262,22 @@ w4_status w4_decode_seq_create_persistent(const w4_weight* w, const void* const*
                                           void* const* y, int n, int M, void* workspace,
                                           size_t workspace_bytes, void* stream, w4_seq** out);
 
+/* Activation types of the persistent sequence. */
+#define W4_ACT_F16 0  /* x and y IEEE binary16 (the pages' FP16 activations) */
+#define W4_ACT_BF16 1 /* x and y bfloat16; scales stay binary16 */
+
+/* w4_decode_seq_create_persistent with the activation type chosen (act =
+ * W4_ACT_F16 is w4_decode_seq_create_persistent).  With W4_ACT_BF16, x and y
+ * are bfloat16 and y = bf16_rne(sum x * q * s) with FP32 accumulation: the
+ * the benchmark spec's FP16/BF16 activation conversion applied to the pages'
+ * projection ("Building a Custom LLM Inference Runtime ...", "Technical
+ * Specifications and Hardware Alignment").  Same workspace size as the
+ * binary16 sequence.  W4_ERR_ARG for another act. */
+w4_status w4_decode_seq_create_persistent_act(const w4_weight* w, const void* const* x,
+                                              void* const* y, int n, int M, int act,
+                                              void* workspace, size_t workspace_bytes,
+                                              void* stream, w4_seq** out);
+
 /* Status word of a persistent sequence (a synchronous device read): 0 when
  * every wait of its replays so far completed, non-zero when one gave up after
  * about a second (the outputs of that replay are then invalid).  0 for graph

@@ -70,6 +70,9 @@ _SIGNATURES = {
     "w4_decode_seq_workspace_bytes": (_sz, [ctypes.POINTER(Weight), _int, _int]),
     "w4_decode_seq_create_persistent": (_int, [ctypes.POINTER(Weight), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                                _int, _int, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
+    "w4_decode_seq_create_persistent_act": (_int, [ctypes.POINTER(Weight), ctypes.POINTER(_vp),
+                                                   ctypes.POINTER(_vp), _int, _int, _int, _vp, _sz, _vp,
+                                                   ctypes.POINTER(_vp)]),
     "w4_decode_seq_status": (_int, [_vp]),
     "w4_decode_seq_destroy": (None, [_vp]),
     "w4_file_write": (_int, [ctypes.c_char_p, ctypes.POINTER(Weight), _int, _vp]),
@@ -246,8 +249,10 @@ class DecodeSeq:
     (w4_decode_seq_create_persistent); otherwise as a graph of one kernel per
     projection (w4_decode_seq_create)."""
 
+    ACT = {"fp16": 0, "bf16": 1}
+
     def __init__(self, weights, xs, ys, M: int, use_pdl: bool = True, stream=None, workspace=None,
-                 workspace_bytes: int | None = None):
+                 workspace_bytes: int | None = None, act: str = "fp16"):
         n = len(weights)
         self._w = (Weight * n)(*weights)
         self._x = (ctypes.c_void_p * n)(*[_addr(t) for t in xs])
@@ -259,9 +264,12 @@ class DecodeSeq:
             if workspace_bytes is None:
                 workspace_bytes = workspace.numel() * workspace.element_size()
             self._ws = workspace
-            _check(lib().w4_decode_seq_create_persistent(self._w, self._x, self._y, n, M, _addr(workspace),
-                                                         workspace_bytes, _stream(stream), ctypes.byref(self._h)))
+            _check(lib().w4_decode_seq_create_persistent_act(self._w, self._x, self._y, n, M, self.ACT[act],
+                                                             _addr(workspace), workspace_bytes, _stream(stream),
+                                                             ctypes.byref(self._h)))
         else:
+            if act != "fp16":
+                raise ValueError("bfloat16 activations need the persistent sequence (pass a workspace)")
             _check(lib().w4_decode_seq_create(self._w, self._x, self._y, n, M, int(use_pdl), _stream(stream),
                                               ctypes.byref(self._h)))
 

@@ -11,6 +11,7 @@
 // is then scaled by the group's FP32 scale and added in FP32.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "tc_ptx.cuh"
@@ -35,6 +36,9 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
     return v;
 }
 
+// Activation types: binary16 (the pages' FP16 activations) or bfloat16.
+enum : int { kActF16 = 0, kActBF16 = 1 };
+
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
@@ -48,6 +52,71 @@ __device__ __forceinline__ void mma16816_zero(float (&c)[4], const uint32_t (&a)
         : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
 }
+
+__device__ __forceinline__ void mma16816_bf(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma16816_bf_zero(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// What changes with the activation type: how x pairs widen to FP32, how a
+// result rounds, how a nibble word becomes MMA A registers, the MMA itself,
+// and the constants that turn the MMA sum D into the group partial:
+//   sum_k x * q = kLo * D - kBias * sum_k x      (kHi for rows r + 8)
+//  * binary16: nibbles as exact subnormals u * 2^-24 (rows r) and u * 2^-20
+//    (rows r + 8), 5 integer ops per word; kLo = 2^24, kHi = 2^20, kBias = 8.
+//  * bfloat16: a subnormal product would fall below FP32's normal range, so
+//    every nibble is moved to bits 0..3 of its half and OR-ed with the
+//    exponent of 128: the exact bfloat16 value 128 + u = q + 136 (7 integer
+//    ops per word); kLo = kHi = 1, kBias = 136.
+template <int ACT>
+struct ActOps;
+template <>
+struct ActOps<kActF16> {
+    static constexpr float kLo = 16777216.f, kHi = 1048576.f, kBias = 8.f;
+    __device__ static __forceinline__ float2 to_float2(uint32_t v) {
+        return __half22float2(*reinterpret_cast<const __half2*>(&v));
+    }
+    __device__ static __forceinline__ uint16_t round(float v) { return __half_as_ushort(__float2half_rn(v)); }
+    __device__ static __forceinline__ void unpack(uint32_t v, uint32_t (&a)[4]) { unpack_word_biased(v, a); }
+    __device__ static __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                               bool first) {
+        if (first)
+            mma16816_zero(c, a, b0, b1);
+        else
+            mma16816(c, a, b0, b1);
+    }
+};
+template <>
+struct ActOps<kActBF16> {
+    static constexpr float kLo = 1.f, kHi = 1.f, kBias = 136.f;
+    __device__ static __forceinline__ float2 to_float2(uint32_t v) {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+    }
+    __device__ static __forceinline__ uint16_t round(float v) {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
+    __device__ static __forceinline__ void unpack(uint32_t v, uint32_t (&a)[4]) {
+        a[0] = (v & 0x000F000Fu) | 0x43004300u;          // rows r,     k 4c, 4c+1
+        a[1] = ((v >> 4) & 0x000F000Fu) | 0x43004300u;   // rows r + 8, k 4c, 4c+1
+        a[2] = ((v >> 8) & 0x000F000Fu) | 0x43004300u;   // rows r,     k 4c+2, 4c+3
+        a[3] = ((v >> 12) & 0x000F000Fu) | 0x43004300u;  // rows r + 8, k 4c+2, 4c+3
+    }
+    __device__ static __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                               bool first) {
+        if (first)
+            mma16816_bf_zero(c, a, b0, b1);
+        else
+            mma16816_bf(c, a, b0, b1);
+    }
+};
 
 // Shared-memory bytes of an x slice of Gs groups for MP padded tokens, and of
 // its per-group sums: xsum[gl * xsum_stride(MP) + m] (the stride is even so
@@ -120,7 +189,7 @@ __device__ __forceinline__ void stage_x(const uint32_t* x, int M, int K, int g_l
 // one lane class and k16 step) copied from global memory straight into its
 // fragment slot by a cp.async, all issued before any is waited for: one
 // memory round trip whatever the slice size.  x must be 8-byte aligned.
-template <int MP, int NCONS>
+template <int MP, int NCONS, int ACT = kActF16>
 __device__ __forceinline__ void stage_x_async(const uint32_t* x, int M, int K, int g_lo, int Gs, uint32_t* xs,
                                               float* xsum) {
     constexpr int kWarps = NCONS / 32;
@@ -150,8 +219,8 @@ __device__ __forceinline__ void stage_x_async(const uint32_t* x, int M, int K, i
         const int gl = idx / M, m = idx - gl * M;
         const int q = lane >> 3, c = (lane >> 1) & 3, e = (lane & 1) * 2;
         const uint32_t* src = xs + gl * (MP * 64) + q * (MP * 16) + (m * 4 + c) * 4 + e;
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(src));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(src + 1));
+        const float2 f0 = ActOps<ACT>::to_float2(src[0]);
+        const float2 f1 = ActOps<ACT>::to_float2(src[1]);
         float sum = (f0.x + f0.y) + (f1.x + f1.y);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
@@ -182,8 +251,9 @@ __device__ __forceinline__ void lds64f_if(float2& v, uint32_t a, uint32_t pred) 
 // token is real load group sums: the other lanes' MMA columns are never
 // written out, so whatever their registers hold is harmless, and the loads
 // they skip are shared-memory bandwidth saved.
-template <int MP>
+template <int MP, int ACT = kActF16>
 struct TileMac {
+    using Ops = ActOps<ACT>;
     static constexpr int NT = (MP + 7) / 8;  // n8 token tiles of the MMA
     static constexpr int NE = MP == 1 ? 1 : 2;  // tokens per lane that can be real (token 2*cl4 + 1 >= MP=1)
     uint32_t xfrag;                          // this lane's B-fragment words of group 0
@@ -210,7 +280,7 @@ struct TileMac {
     // acc += s * sum_{k in group} x * q for NTL consecutive tiles at ta, ta +
     // 1056, ... (groups gl, gl + 1, ... of one band), their MMA chains
     // interleaved; the tiles are added to acc in order.  Per tile and row:
-    //     acc += s * (2^24 * D - 8 * sum_k x)      (2^20 for rows r + 8)
+    //     acc += s * (kLo * D - kBias * sum_k x)      (kHi for rows r + 8)
     template <int NTL>
     __device__ __forceinline__ void run_tiles(uint32_t ta, int gl, int lane, float (&acc)[NT][4]) {
         uint32_t wd[NTL][8], sc[NTL];
@@ -235,18 +305,13 @@ struct TileMac {
                 for (int nt = 0; nt < NT; ++nt)
                     lds128_if(xv[n][nt], xa0 + (uint32_t)(n * MP * 256 + q * MP * 64 + nt * 512), xl);
                 uint32_t a[4], b[4];
-                unpack_word_biased(wd[n][2 * q], a);
-                unpack_word_biased(wd[n][2 * q + 1], b);
+                Ops::unpack(wd[n][2 * q], a);
+                Ops::unpack(wd[n][2 * q + 1], b);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const uint4 v = xv[n][nt];
-                    if (q == 0) {
-                        mma16816_zero(pe[n][nt], a, v.x, v.y);
-                        mma16816_zero(po[n][nt], b, v.z, v.w);
-                    } else {
-                        mma16816(pe[n][nt], a, v.x, v.y);
-                        mma16816(po[n][nt], b, v.z, v.w);
-                    }
+                    Ops::mma(pe[n][nt], a, v.x, v.y, q == 0);
+                    Ops::mma(po[n][nt], b, v.z, v.w, q == 0);
                 }
             }
         }
@@ -257,9 +322,9 @@ struct TileMac {
             for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
                 for (int e = 0; e < NE; ++e) {
-                    const float m8x = -8.f * (e ? X[n][nt].y : X[n][nt].x);
-                    acc[nt][e] = fmaf(s.x, fmaf(16777216.f, pe[n][nt][e] + po[n][nt][e], m8x), acc[nt][e]);
-                    acc[nt][2 + e] = fmaf(s.y, fmaf(1048576.f, pe[n][nt][2 + e] + po[n][nt][2 + e], m8x), acc[nt][2 + e]);
+                    const float mbx = -Ops::kBias * (e ? X[n][nt].y : X[n][nt].x);
+                    acc[nt][e] = fmaf(s.x, fmaf(Ops::kLo, pe[n][nt][e] + po[n][nt][e], mbx), acc[nt][e]);
+                    acc[nt][2 + e] = fmaf(s.y, fmaf(Ops::kHi, pe[n][nt][2 + e] + po[n][nt][2 + e], mbx), acc[nt][2 + e]);
                 }
             }
         }

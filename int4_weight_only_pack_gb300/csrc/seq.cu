@@ -169,15 +169,29 @@ extern "C" size_t w4_decode_seq_workspace_bytes(const w4_weight* w, int n, int M
     return step_workspace_bytes(w, n, M);
 }
 
+extern "C" w4_status w4_decode_seq_create_persistent_act(const w4_weight* w, const void* const* x,
+                                                         void* const* y, int n, int M, int act, void* workspace,
+                                                         size_t workspace_bytes, void* stream, w4_seq** out);
+
 extern "C" w4_status w4_decode_seq_create_persistent(const w4_weight* w, const void* const* x, void* const* y, int n,
                                                      int M, void* workspace, size_t workspace_bytes, void* stream,
                                                      w4_seq** out) {
+    return w4_decode_seq_create_persistent_act(w, x, y, n, M, W4_ACT_F16, workspace, workspace_bytes, stream, out);
+}
+
+extern "C" w4_status w4_decode_seq_create_persistent_act(const w4_weight* w, const void* const* x,
+                                                         void* const* y, int n, int M, int act, void* workspace,
+                                                         size_t workspace_bytes, void* stream, w4_seq** out) {
     clear_error();
     if (!w || !x || !y || !out || n < 1) {
         set_error("NULL argument or n < 1");
         return W4_ERR_ARG;
     }
     *out = nullptr;
+    if (act != W4_ACT_F16 && act != W4_ACT_BF16) {
+        set_error("unknown activation type %d", act);
+        return W4_ERR_ARG;
+    }
     for (int i = 0; i < n; ++i) {
         w4_status st = check_gemv_args(x[i], &w[i], y[i], M);
         if (st != W4_OK) return st;
@@ -187,7 +201,7 @@ extern "C" w4_status w4_decode_seq_create_persistent(const w4_weight* w, const v
     s->M = M;
     s->persistent = true;
     cudaStream_t user = static_cast<cudaStream_t>(stream);
-    w4_status st = step_prepare(w, x, y, n, M, workspace, workspace_bytes, user, &s->step);
+    w4_status st = step_prepare(w, x, y, n, M, act, workspace, workspace_bytes, user, &s->step);
     if (st != W4_OK) {
         delete s;
         return st;

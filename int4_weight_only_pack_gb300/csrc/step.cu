@@ -215,12 +215,13 @@ __device__ __forceinline__ void for_frag(const float (&acc)[(MP + 7) / 8][4], in
 // is held by exactly one lane of the warp).  S == 1: write y.  S > 1: publish
 // this split's partial; the arrival that completes the band adds the S
 // partials in split order and writes y.
-template <typename V>
+template <int ACT, typename V>
 __device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, int M, int lane, V&& visit) {
+    using Ops = dec::ActOps<ACT>;
     const int n0 = band * 16;
     if (o.S == 1) {
         visit([&](int row, int m, float v) {
-            if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = __half_as_ushort(__float2half_rn(v));
+            if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = Ops::round(v);
         });
         return;
     }
@@ -251,12 +252,12 @@ __device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, in
             for (int e = 0; e < 8; ++e) sum += v[e];
         }
         for (; s < o.S; ++s) sum += __ldcg(pp + (size_t)s * pb);
-        if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = __half_as_ushort(__float2half_rn(sum));
+        if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = Ops::round(sum);
     });
     if (lane == 0) o.cnt[band] = 0;  // ready for the next replay
 }
 
-template <int MP>
+template <int MP, int ACT>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepArgs a) {
     constexpr int NT = (MP + 7) / 8;
     constexpr int PB = 16 * MP;  // floats of one parked band partial
@@ -323,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         }
         const Geo q = get_geo(geo + i);
         if (q.nu > 0) {
-            dec::stage_x_async<MP, kThreads>(o.x, M, o.K, q.g_lo, q.Gs, xs, xsum);
-            dec::TileMac<MP> mac(sbase + L.x, sbase + L.xsum, lane);
+            dec::stage_x_async<MP, kThreads, ACT>(o.x, M, o.K, q.g_lo, q.Gs, xs, xsum);
+            dec::TileMac<MP, ACT> mac(sbase + L.x, sbase + L.xsum, lane);
             const int Tc = q.Tc();
             const int t0 = warp_lo(Tc, warp), t1 = warp_lo(Tc, warp + 1);
             const int u_first = div_small(t0, q.Gs, q.inv_gs);
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     const int us = u * q.Gs;
                     if (us >= t0 && us + q.Gs <= t1) {
                         // the whole band is this warp's: finish it from the accumulators
-                        finish_band(o, q.ub + u, q.r, M, lane, [&](auto&& f) { for_frag<MP>(acc, lane, M, f); });
+                        finish_band<ACT>(o, q.ub + u, q.r, M, lane, [&](auto&& f) { for_frag<MP>(acc, lane, M, f); });
                     } else {
                         // cut between warps: park this warp's share
                         float* dst = park_w + (u == u_first ? 0 : PB);
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             // then holds the band's first tile)
             const int bs = u_first * q.Gs, be = bs + q.Gs;
             if (warp > 0 && t0 < Tc && t0 != bs && warp_lo(Tc, warp - 1) <= bs) {
-                finish_band(o, q.ub + u_first, q.r, M, lane, [&](auto&& f) {
+                finish_band<ACT>(o, q.ub + u_first, q.r, M, lane, [&](auto&& f) {
                     for (int oi = lane; oi < 16 * M; oi += 32) {
                         const int row = oi / M, m = oi - row * M;
                         float sum = 0.f;
@@ -433,14 +434,18 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
 using StepKernel = void (*)(StepArgs);
 
-StepKernel step_fn(int MP) {
+template <int ACT>
+StepKernel step_fn_act(int MP) {
     switch (MP) {
-        case 1: return step_kernel<1>;
-        case 2: return step_kernel<2>;
-        case 4: return step_kernel<4>;
-        case 8: return step_kernel<8>;
-        default: return step_kernel<16>;
+        case 1: return step_kernel<1, ACT>;
+        case 2: return step_kernel<2, ACT>;
+        case 4: return step_kernel<4, ACT>;
+        case 8: return step_kernel<8, ACT>;
+        default: return step_kernel<16, ACT>;
     }
+}
+StepKernel step_fn(int MP, int act) {
+    return act == dec::kActBF16 ? step_fn_act<dec::kActBF16>(MP) : step_fn_act<dec::kActF16>(MP);
 }
 
 int padded(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
@@ -539,9 +544,9 @@ static int sm_count_now() {
 }
 
 // One resident CTA per SM, or 0 if the kernel cannot be resident.
-static int step_grid(int MP, int smem) {
+static int step_grid(int MP, int act, int smem) {
     int per_sm = 0;
-    StepKernel fn = step_fn(MP);
+    StepKernel fn = step_fn(MP, act);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess) return 0;
     return per_sm >= 1 ? sm_count_now() : 0;
@@ -553,7 +558,7 @@ size_t step_workspace_bytes(const w4_weight* w, int n, int M) {
     return pl.total;
 }
 
-w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y, int n, int M, void* ws,
+w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y, int n, int M, int act, void* ws,
                        size_t ws_bytes, cudaStream_t stream, StepLaunch* out) {
     const int MP = padded(M);
     StepPlan pl;
@@ -563,7 +568,7 @@ w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y,
                   n, kMaxStepOps);
         return W4_ERR_UNSUPPORTED;
     }
-    const int NC = step_grid(MP, pl.smem);
+    const int NC = step_grid(MP, act, pl.smem);
     if (NC <= 0 || NC != pl.NC) {
         set_error("the persistent step kernel cannot be resident (shared memory %d bytes)", pl.smem);
         return W4_ERR_UNSUPPORTED;
@@ -597,7 +602,7 @@ w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y,
     a->gpc_max = pl.gpc_max;
     a->ring = pl.R;
     std::copy(pl.ops.begin(), pl.ops.end(), a->ops);
-    out->fn = reinterpret_cast<const void*>(step_fn(MP));
+    out->fn = reinterpret_cast<const void*>(step_fn(MP, act));
     out->status = a->status;
     out->NC = NC;
     out->smem = pl.smem;

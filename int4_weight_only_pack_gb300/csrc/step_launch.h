@@ -21,7 +21,8 @@ struct StepLaunch {
     int NC = 0, smem = 0;
 };
 
-w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y, int n, int M, void* ws,
+// act: 0 binary16 activations, 1 bfloat16.
+w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y, int n, int M, int act, void* ws,
                        size_t ws_bytes, cudaStream_t stream, StepLaunch* out);
 w4_status step_launch(const StepLaunch& s, cudaStream_t stream);
 int step_status(const StepLaunch& s);

@@ -42,6 +42,14 @@ def lib():
         L.w4o_double_from_half.argtypes = [ctypes.c_uint16]
         L.w4o_half_from_double.restype = ctypes.c_uint16
         L.w4o_half_from_double.argtypes = [ctypes.c_double]
+        L.w4o_double_from_bf16.restype = ctypes.c_double
+        L.w4o_double_from_bf16.argtypes = [ctypes.c_uint16]
+        L.w4o_bf16_from_double.restype = ctypes.c_uint16
+        L.w4o_bf16_from_double.argtypes = [ctypes.c_double]
+        L.w4o_linear_act.restype = ctypes.c_int
+        L.w4o_linear_act.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         L.w4o_linear.restype = ctypes.c_int
         L.w4o_linear.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
@@ -61,15 +69,24 @@ def half_from_double(v: float) -> int:
     return int(lib().w4o_half_from_double(float(v)))
 
 
+def double_from_bf16(b: int) -> float:
+    return lib().w4o_double_from_bf16(int(b) & 0xFFFF)
+
+
+def bf16_from_double(v: float) -> int:
+    return int(lib().w4o_bf16_from_double(float(v)))
+
+
 def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
 def linear(x: np.ndarray, q: np.ndarray, s: np.ndarray, threads: int = 0,
-           want_acc: bool = False):
-    """y = fp16_rne(x . (q*s)^T) in FP64.  x: uint16 [M,K] fp16 bits,
-    q: int8 [N,K], s: uint16 [N,K/128] fp16 bits.  Returns y as uint16
-    [M,N] (and the FP64 sums if ``want_acc``)."""
+           want_acc: bool = False, act: str = "fp16"):
+    """y = rne(x . (q*s)^T) in FP64.  x: uint16 [M,K] activation bits
+    (binary16, or bfloat16 with ``act="bf16"``), q: int8 [N,K], s: uint16
+    [N,K/128] fp16 bits.  Returns y as uint16 [M,N] bits of the activation
+    type (and the FP64 sums if ``want_acc``)."""
     x = np.ascontiguousarray(x, dtype=np.uint16)
     q = np.ascontiguousarray(q, dtype=np.int8)
     s = np.ascontiguousarray(s, dtype=np.uint16)
@@ -81,8 +98,10 @@ def linear(x: np.ndarray, q: np.ndarray, s: np.ndarray, threads: int = 0,
     acc = np.zeros((M, N), dtype=np.float64) if want_acc else None
     if threads <= 0:
         threads = os.cpu_count() or 1
-    rc = lib().w4o_linear(_ptr(x), _ptr(q), _ptr(s), M, N, K, _ptr(y),
-                          _ptr(acc) if acc is not None else None, threads)
+    if act not in ("fp16", "bf16"):
+        raise ValueError("act must be fp16 or bf16")
+    rc = lib().w4o_linear_act(_ptr(x), 1 if act == "bf16" else 0, _ptr(q), _ptr(s), M, N, K, _ptr(y),
+                              _ptr(acc) if acc is not None else None, threads)
     if rc != 0:
         raise ValueError("w4o_linear failed: %d" % rc)
     return (y, acc) if want_acc else y

@@ -83,6 +83,60 @@ uint16_t w4o_half_from_double(double v)
     return (uint16_t)(sign | bits);
 }
 
+/* ---- bfloat16 -------------------------------------------------------------- */
+/* bfloat16 (the upper half of IEEE 754 binary32): 1 sign bit, 8 exponent
+ * bits (bias 127), 7 fraction bits.  Exponent field 0 encodes subnormals
+ * f * 2^-133; field 255 encodes inf/NaN; otherwise the value is
+ * (128 + f) * 2^(e - 134). */
+double w4o_double_from_bf16(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 255;
+    int f = b & 127;
+    double mag;
+    if (e == 0)
+        mag = ldexp((double)f, -133);
+    else if (e == 255)
+        mag = f ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(128 + f), e - 134);
+    return sign ? -mag : mag;
+}
+
+uint16_t w4o_bf16_from_double(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    if (isnan(v))
+        return (uint16_t)(sign | 0x7FC0u);
+    double a = fabs(v);
+    /* largest finite: 255 * 2^120; the next step would be 256 * 2^120 =
+     * 2^128, so the midpoint 255.5 * 2^120 and above round to infinity */
+    if (a >= ldexp(255.5, 120))
+        return (uint16_t)(sign | 0x7F80u);
+    if (a == 0.0)
+        return sign;
+    /* unbiased exponent of a, clamped below at -126 (subnormals share the
+     * quantum of the smallest normal binade) */
+    int E;
+    (void)frexp(a, &E);
+    int e = E - 1;
+    if (e < -126)
+        e = -126;
+    double n = ldexp(a, 7 - e); /* a / 2^(e - 7), exact */
+    double fl = floor(n);
+    double frac = n - fl;
+    double r = fl;
+    if (frac > 0.5 || (frac == 0.5 && fmod(fl, 2.0) != 0.0))
+        r = fl + 1.0;
+    /* r in [0, 256]; r = 256 carries into the next exponent */
+    unsigned bits;
+    if (e == -126 && r < 128.0)
+        bits = (unsigned)r;
+    else
+        bits = ((unsigned)(e + 127) << 7) + (unsigned)(r - 128.0);
+    return (uint16_t)(sign | bits);
+}
+
 /* ---- the projection --------------------------------------------------- */
 typedef struct {
     const uint16_t* x;
@@ -92,6 +146,8 @@ typedef struct {
     uint16_t* y;
     double* acc;
     int64_t n_begin, n_end;
+    double (*x_value)(uint16_t);  /* activation decoding (x) */
+    uint16_t (*y_bits)(double);   /* output rounding (y) */
 } w4o_job;
 
 static void* w4o_rows(void* arg)
@@ -108,9 +164,9 @@ static void* w4o_rows(void* arg)
                 /* w[n,k] = q[n,k] * s[n, k/128]; every product is exact in
                  * FP64 (11 + 4 + 11 significant bits). */
                 double w = (double)qn[k] * w4o_double_from_half(sn[k / 128]);
-                sum += w4o_double_from_half(xm[k]) * w;
+                sum += jb->x_value(xm[k]) * w;
             }
-            jb->y[m * jb->N + n] = w4o_half_from_double(sum);
+            jb->y[m * jb->N + n] = jb->y_bits(sum);
             if (jb->acc)
                 jb->acc[m * jb->N + n] = sum;
         }
@@ -122,6 +178,15 @@ int w4o_linear(const uint16_t* x, const int8_t* q, const uint16_t* s,
                int64_t M, int64_t N, int64_t K,
                uint16_t* y, double* acc, int nthreads)
 {
+    return w4o_linear_act(x, 0, q, s, M, N, K, y, acc, nthreads);
+}
+
+int w4o_linear_act(const uint16_t* x, int act, const int8_t* q, const uint16_t* s,
+                   int64_t M, int64_t N, int64_t K,
+                   uint16_t* y, double* acc, int nthreads)
+{
+    if (act != 0 && act != 1)
+        return -1;
     if (M < 0 || N < 0 || K < 0 || K % 128 != 0)
         return -1;
     if (M == 0 || N == 0)
@@ -144,7 +209,9 @@ int w4o_linear(const uint16_t* x, const int8_t* q, const uint16_t* s,
     }
     for (int t = 0; t < nthreads; ++t) {
         w4o_job j = {x, q, s, M, N, K, y, acc,
-                     N * t / nthreads, N * (t + 1) / nthreads};
+                     N * t / nthreads, N * (t + 1) / nthreads,
+                     act ? w4o_double_from_bf16 : w4o_double_from_half,
+                     act ? w4o_bf16_from_double : w4o_half_from_double};
         jobs[t] = j;
     }
     int started = 0;

@@ -50,6 +50,21 @@ int w4o_linear(const uint16_t* x, const int8_t* q, const uint16_t* s,
                int64_t M, int64_t N, int64_t K,
                uint16_t* y, double* acc, int nthreads);
 
+/* bfloat16 (the upper 16 bits of IEEE 754 binary32): the exact value of bit
+ * pattern b, and the round-to-nearest, ties-to-even bfloat16 of v
+ * (|v| >= 255.5 * 2^120 gives +/-inf, NaN gives 0x7FC0 with the sign kept).
+ * For the BF16-activation variant of the projection (the benchmark spec names
+ * FP16/BF16 activation conversion). */
+double w4o_double_from_bf16(uint16_t b);
+uint16_t w4o_bf16_from_double(double v);
+
+/* w4o_linear with the activation type chosen: act 0 = binary16 x and y,
+ * act 1 = bfloat16 x and y (scales stay binary16).  Same FP64 sum, k
+ * ascending, one final rounding to the output type.  -1 for a bad act. */
+int w4o_linear_act(const uint16_t* x, int act, const int8_t* q, const uint16_t* s,
+                   int64_t M, int64_t N, int64_t K,
+                   uint16_t* y, double* acc, int nthreads);
+
 /* The packed device layout, written out plainly from its definition
  * (the layout is a design of this library, not of the pages; the pages only
  * say that the nibbles are shuffled for the byte-permute datapath:

@@ -120,6 +120,20 @@ def x_full(seed: int, M: int, K: int) -> np.ndarray:
     return z.astype(np.float16).view(np.uint16)
 
 
+def x_full_bf16(seed: int, M: int, K: int) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) of the same N(0, 1) draws as x_full:
+    the draws go to binary32, then to the nearest bfloat16 (ties to even on
+    the binary32 pattern).  An input recipe only: any fixed rounding would do,
+    as both sides read the same bits."""
+    r = draws(seed, np.arange(M * K, dtype=np.uint64)).reshape(M, K)
+    u1 = ((r >> np.uint64(32)).astype(np.float64) + 1.0) * (2.0 ** -32)
+    u2 = (r & np.uint64(0xFFFFFFFF)).astype(np.float64) * (2.0 ** -32)
+    z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+    b = z.astype(np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return b.astype(np.uint16)
+
+
 def projection_inputs(config: int, layer: int, proj: int, M: int, N: int, K: int,
                       rows=None):
     """(q, s, x) of one projection; ``rows`` limits q and s to a sample of rows."""

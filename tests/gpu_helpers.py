@@ -21,13 +21,27 @@ def h2f(bits):
     return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
 
 
-def assert_close(y_bits, ref_bits, what=""):
-    y, r = h2f(y_bits), h2f(ref_bits)
+def bf2f(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def assert_close(y_bits, ref_bits, what="", act="fp16"):
+    dec = bf2f if act == "bf16" else h2f
+    y, r = dec(y_bits), dec(ref_bits)
     assert y.shape == r.shape, (y.shape, r.shape)
     assert np.all(np.isfinite(y)), what + ": non-finite output"
     rms = float(np.sqrt(np.mean(r * r))) if r.size else 0.0
     err = np.abs(y - r)
-    bound = REL_TOL * np.abs(r) + RMS_TOL * rms
+    if act == "bf16":
+        # bfloat16 output: one unit in the last place of the reference (the
+        # FP32 sum lies within ~1e-5 relative of the exact one, so only the
+        # final rounding can differ, by at most one step of 2^-8..2^-7
+        # relative, which is wider than the binary16 bound) plus the same
+        # rms term
+        e = np.floor(np.log2(np.maximum(np.abs(r), 2.0 ** -126)))
+        bound = 2.0 ** (e - 7) + RMS_TOL * rms
+    else:
+        bound = REL_TOL * np.abs(r) + RMS_TOL * rms
     bad = err > bound
     if np.any(bad):
         i = np.argwhere(bad)[0]
@@ -79,12 +93,12 @@ def synth_weight(config, layer, proj, N, K):
     return packed, w
 
 
-def oracle_rows(config, layer, proj, M, N, K, rows, x_bits=None):
+def oracle_rows(config, layer, proj, M, N, K, rows, x_bits=None, act="fp16"):
     """Oracle y[:, rows] of one seeded projection, from host-drawn q and s rows."""
     q, s, x = synth.projection_inputs(config, layer, proj, M, N, K, rows=rows)
     if x_bits is not None:
         x = x_bits
-    return oracle.linear(x, q, s), x
+    return oracle.linear(x, q, s, act=act), x
 
 
 def sample_rows(rng, N, count=48):

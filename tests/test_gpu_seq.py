@@ -161,3 +161,66 @@ def check_step(meta, ys, CONFIG, M):
         rows = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 24)]))
         ref, _ = oracle_rows(CONFIG, layer, pid, M, N, K, rows, x_bits=x)
         assert_close(host(ys[i])[:, rows], ref, "layer %d proj %d" % (layer, pid))
+
+
+def bf16_problem(rng, M, N, K):
+    x = synth.x_full_bf16(int(rng.integers(1 << 62)), M, K)
+    q = rng.integers(-8, 8, (N, K)).astype(np.int8)
+    s = (0.005 + 0.015 * rng.random((N, K // 128))).astype(np.float16).view(np.uint16)
+    return x, q, s
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 16])
+def test_bf16_sequence_matches_oracle(M):
+    """bfloat16 activations through the persistent sequence (scaled-down
+    layers plus the K-split down shape), against the oracle's bfloat16
+    projection; replays are bit-identical."""
+    rng = np.random.default_rng(100 + M)
+    shapes = MINI * 2 + [(3584, 18944)]
+    probs, keep, ws, xs, ys = [], [], [], [], []
+    for N, K in shapes:
+        x, q, s = bf16_problem(rng, M, N, K)
+        packed, w = pack_on_device(q, s)
+        keep.append(packed)
+        ws.append(w)
+        xs.append(dev(x))
+        ys.append(torch.zeros((M, N), dtype=torch.int16, device="cuda"))
+        probs.append((x, q, s))
+    nb = w4.w4_decode_seq_workspace_bytes(ws, M)
+    buf = torch.zeros(nb + 256, dtype=torch.uint8, device="cuda")
+    off = (-buf.data_ptr()) % 256
+    seq = w4.DecodeSeq(ws, xs, ys, M, workspace=buf[off:off + nb], act="bf16")
+    seq.replay()
+    torch.cuda.synchronize()
+    got = [host(y).copy() for y in ys]
+    for i, (x, q, s) in enumerate(probs):
+        assert_close(got[i], oracle.linear(x, q, s, act="bf16"), "projection %d" % i, act="bf16")
+    seq.replay()
+    seq.eager()
+    torch.cuda.synchronize()
+    for i in range(len(ys)):
+        assert np.array_equal(host(ys[i]), got[i])
+    assert seq.status() == 0
+    seq.close()
+
+
+def test_bf16_activation_type_is_checked():
+    rng = np.random.default_rng(1)
+    x, q, s = rand_problem(rng, 1, 128, 256)
+    packed, w = pack_on_device(q, s)
+    y = torch.zeros((1, 128), dtype=torch.int16, device="cuda")
+    nb = w4.w4_decode_seq_workspace_bytes([w], 1)
+    buf = torch.zeros(nb + 256, dtype=torch.uint8, device="cuda")
+    off = (-buf.data_ptr()) % 256
+    with pytest.raises(KeyError):
+        w4.DecodeSeq([w], [dev(x)], [y], 1, workspace=buf[off:off + nb], act="fp8")
+    with pytest.raises(ValueError):
+        w4.DecodeSeq([w], [dev(x)], [y], 1, act="bf16")  # graph mode is binary16 only
+    import ctypes
+    warr = (w4.Weight * 1)(w)
+    xa = (ctypes.c_void_p * 1)(dev(x).data_ptr())
+    ya = (ctypes.c_void_p * 1)(y.data_ptr())
+    h = ctypes.c_void_p()
+    rc = w4.lib().w4_decode_seq_create_persistent_act(warr, xa, ya, 1, 1, 2, buf[off:].data_ptr(), nb, None,
+                                                      ctypes.byref(h))
+    assert rc == 1 and not h.value  # W4_ERR_ARG, nothing created
