@@ -350,6 +350,44 @@ def bf16_step(torch, w4, synth, st, reps=100):
     return out
 
 
+def swiglu_step(torch, w4, synth, st, reps=100):
+    """The 28-layer step with every gate_up projection fused with its SwiGLU
+    (weights packed by w4_pack_glu from the same seeded q and scales, y =
+    silu(gate) * up of 18944 columns): us/step and weight GB/s."""
+    dev = torch.device("cuda")
+    ws, keep, ys, flags = [], [], [], []
+    for i, (layer, pid, N, K) in enumerate(st["meta"]):
+        if LAYER[pid][0] == "gate_up":
+            G = K // 128
+            q = torch.empty((N, K), dtype=torch.int8, device=dev)
+            s = torch.empty((N, G), dtype=torch.int16, device=dev)
+            synth.q_device(synth.seed_of(CONFIG_ID, layer, pid, synth.T_Q), N, K, q)
+            synth.scale_device(synth.seed_of(CONFIG_ID, layer, pid, synth.T_SCALE), N, G, s)
+            packed = torch.empty(w4.w4_packed_bytes(N, K), dtype=torch.uint8, device=dev)
+            ws.append(w4.w4_pack_glu(q, s, N // 2, K, packed))
+            keep.append(packed)
+            del q, s
+            ys.append(torch.zeros((1, N // 2), dtype=torch.int16, device=dev))
+            flags.append(w4.W4_OP_SWIGLU)
+        else:
+            ws.append(st["ws"][i])
+            ys.append(torch.zeros((1, N), dtype=torch.int16, device=dev))
+            flags.append(0)
+    nbw = w4.w4_decode_seq_workspace_bytes(ws, 1)
+    buf = torch.zeros(nbw + 256, dtype=torch.uint8, device=dev)
+    off = (-buf.data_ptr()) % 256
+    seq = w4.DecodeSeq(ws, st["xs"], ys, 1, workspace=buf[off:off + nbw], op_flags=flags)
+    for _ in range(5):
+        seq.replay()
+    ms = time_replays(torch, seq.replay, reps)
+    peak = measured_peaks()[0].get("hbm_gbs", FALLBACK_HBM_GBS)
+    out = {"us_per_step": ms * 1e3, "GB/s": BYTES_PER_STEP / (ms * 1e-3) / 1e9,
+           "frac_of_hbm": BYTES_PER_STEP / (ms * 1e-3) / 1e9 / peak, "status_word": seq.status()}
+    seq.close()
+    del keep
+    return out
+
+
 def packed_file_load(torch, w4, st):
     """Layer 0's four packed weights written to packed-weight files and read
     back (header + checksum validation + one host-to-device copy each) into
@@ -518,6 +556,7 @@ def main():
         extras["prefill_M512"] = prefill_layer(torch, w4, synth, st)
         extras["packed_file_layer0"] = packed_file_load(torch, w4, st)
         extras["bf16_activations_step_M1"] = bf16_step(torch, w4, synth, st)
+        extras["swiglu_fused_gate_up_step_M1"] = swiglu_step(torch, w4, synth, st)
 
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))

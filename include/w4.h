@@ -130,6 +130,17 @@ w4_status w4_pack(const int8_t* q, const uint16_t* scales, int64_t N, int64_t K,
                   void* dst_dev, size_t dst_bytes, int src_on_device,
                   void* stream, w4_weight* out);
 
+/* Pack a gated MLP weight for W4_OP_SWIGLU (below): q [2I, K] and scales
+ * [2I, K/128] hold the stacked [gate (rows 0..I-1); up (rows I..2I-1)]
+ * weight.  The packed weight (N = 2I, the size w4_pack gives) puts gate rows
+ * 8b..8b+7 and then up rows 8b..8b+7 in 16-row band b, so rows r and r + 8
+ * of every band are the gate and up rows of one output.  I must be a
+ * positive multiple of 8 (W4_ERR_SHAPE).  Otherwise as w4_pack; w4_unpack
+ * returns the interleaved row order. */
+w4_status w4_pack_glu(const int8_t* q, const uint16_t* scales, int64_t I, int64_t K,
+                      void* dst_dev, size_t dst_bytes, int src_on_device,
+                      void* stream, w4_weight* out);
+
 /* Inverse of w4_pack (round trip): q [N, K] int8 and scales [N, K/128]
  * fp16.  dst_on_device selects device (a kernel) or host outputs.
  * Synchronous. */
@@ -277,6 +288,25 @@ w4_status w4_decode_seq_create_persistent_act(const w4_weight* w, const void* co
                                               void* const* y, int n, int M, int act,
                                               void* workspace, size_t workspace_bytes,
                                               void* stream, w4_seq** out);
+
+/* Per-projection options of a persistent sequence. */
+#define W4_OP_SWIGLU 1u /* gated MLP: the weight comes from w4_pack_glu (N = 2I rows,
+                           gate and up interleaved per band) and y receives
+                           h = silu(gate) * up, I columns per token, instead of
+                           the 2I projections (SwiGLU, Qwen2.5's MLP activation;
+                           the pages do not name it) */
+
+/* The same with options per projection: op_flags[i] (W4_OP_*, or NULL for
+ * none).  A W4_OP_SWIGLU projection computes, per token m and row n < I,
+ *   y[m, n] = rne(silu(g) * u),  g = sum_k x*q*s over gate row n,
+ *   u = the same over up row n,  silu(g) = g / (1 + exp(-g)),
+ * from the FP32 sums (no rounding of g and u) with FP32 silu.  W4_ERR_ARG
+ * for an unknown flag, W4_ERR_SHAPE for a gated weight with N % 16 != 0. */
+w4_status w4_decode_seq_create_persistent_ex(const w4_weight* w, const void* const* x,
+                                             void* const* y, const uint32_t* op_flags,
+                                             int n, int M, int act, void* workspace,
+                                             size_t workspace_bytes, void* stream,
+                                             w4_seq** out);
 
 /* Status word of a persistent sequence (a synchronous device read): 0 when
  * every wait of its replays so far completed, non-zero when one gave up after

@@ -73,6 +73,10 @@ _SIGNATURES = {
     "w4_decode_seq_create_persistent_act": (_int, [ctypes.POINTER(Weight), ctypes.POINTER(_vp),
                                                    ctypes.POINTER(_vp), _int, _int, _int, _vp, _sz, _vp,
                                                    ctypes.POINTER(_vp)]),
+    "w4_decode_seq_create_persistent_ex": (_int, [ctypes.POINTER(Weight), ctypes.POINTER(_vp),
+                                                  ctypes.POINTER(_vp), ctypes.POINTER(ctypes.c_uint32), _int, _int,
+                                                  _int, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
+    "w4_pack_glu": (_int, [_vp, _vp, _i64, _i64, _vp, _sz, _int, _vp, ctypes.POINTER(Weight)]),
     "w4_decode_seq_status": (_int, [_vp]),
     "w4_decode_seq_destroy": (None, [_vp]),
     "w4_file_write": (_int, [ctypes.c_char_p, ctypes.POINTER(Weight), _int, _vp]),
@@ -202,6 +206,23 @@ def w4_pack(q, scales, N: int, K: int, dst, dst_bytes: int | None = None, src_on
     return w
 
 
+W4_OP_SWIGLU = 1
+
+
+def w4_pack_glu(q, scales, I: int, K: int, dst, dst_bytes: int | None = None, src_on_device: bool | None = None,
+                stream=None) -> Weight:
+    """Pack a stacked [gate; up] weight (2I rows) with gate and up rows
+    interleaved per band, for a W4_OP_SWIGLU projection."""
+    if src_on_device is None:
+        src_on_device = _on_device(q)
+    if dst_bytes is None:
+        dst_bytes = dst.numel() * dst.element_size()
+    w = Weight()
+    _check(lib().w4_pack_glu(_addr(q), _addr(scales), I, K, _addr(dst), dst_bytes, int(src_on_device),
+                             _stream(stream) if src_on_device else None, ctypes.byref(w)))
+    return w
+
+
 def w4_unpack(w: Weight, q_out, s_out, dst_on_device: bool | None = None, stream=None):
     if dst_on_device is None:
         dst_on_device = not isinstance(q_out, np.ndarray) and getattr(q_out, "is_cuda", False)
@@ -252,7 +273,7 @@ class DecodeSeq:
     ACT = {"fp16": 0, "bf16": 1}
 
     def __init__(self, weights, xs, ys, M: int, use_pdl: bool = True, stream=None, workspace=None,
-                 workspace_bytes: int | None = None, act: str = "fp16"):
+                 workspace_bytes: int | None = None, act: str = "fp16", op_flags=None):
         n = len(weights)
         self._w = (Weight * n)(*weights)
         self._x = (ctypes.c_void_p * n)(*[_addr(t) for t in xs])
@@ -264,12 +285,17 @@ class DecodeSeq:
             if workspace_bytes is None:
                 workspace_bytes = workspace.numel() * workspace.element_size()
             self._ws = workspace
-            _check(lib().w4_decode_seq_create_persistent_act(self._w, self._x, self._y, n, M, self.ACT[act],
-                                                             _addr(workspace), workspace_bytes, _stream(stream),
-                                                             ctypes.byref(self._h)))
+            flags = None
+            if op_flags is not None:
+                self._flags = (ctypes.c_uint32 * n)(*op_flags)
+                flags = self._flags
+            _check(lib().w4_decode_seq_create_persistent_ex(self._w, self._x, self._y, flags, n, M, self.ACT[act],
+                                                            _addr(workspace), workspace_bytes, _stream(stream),
+                                                            ctypes.byref(self._h)))
         else:
-            if act != "fp16":
-                raise ValueError("bfloat16 activations need the persistent sequence (pass a workspace)")
+            if act != "fp16" or op_flags is not None:
+                raise ValueError("bfloat16 activations and projection options need the persistent sequence "
+                                 "(pass a workspace)")
             _check(lib().w4_decode_seq_create(self._w, self._x, self._y, n, M, int(use_pdl), _stream(stream),
                                               ctypes.byref(self._h)))
 

@@ -26,6 +26,16 @@ __host__ __device__ inline int nib_k(int L, int j, int i) {
 // Byte offset of that word inside its tile.
 __host__ __device__ inline int word_offset(int L, int j) { return (j >> 2) * 512 + 16 * L + 4 * (j & 3); }
 
+// Source row of packed row n.  glu_I = 0: the identity.  glu_I = I > 0: the
+// source is a stacked [gate (I rows); up (I rows)] weight and 16-row band b
+// takes gate rows 8b .. 8b+7 then up rows 8b .. 8b+7, so rows r and r + 8 of
+// every band are a (gate, up) pair.
+__host__ __device__ inline int64_t src_row(int64_t n, int64_t glu_I) {
+    if (glu_I == 0) return n;
+    const int64_t b = n >> 4, r = n & 15;
+    return r < 8 ? 8 * b + r : glu_I + 8 * b + (r - 8);
+}
+
 static bool q_in_range(const int8_t* q, size_t n) {
     for (size_t i = 0; i < n; ++i)
         if (q[i] < -8 || q[i] > 7) return false;
@@ -41,7 +51,8 @@ static w4_status check_shape(int64_t N, int64_t K) {
     return W4_OK;
 }
 
-static void pack_host_impl(const int8_t* q, const uint16_t* s, int64_t N, int64_t K, uint8_t* dst) {
+static void pack_host_impl(const int8_t* q, const uint16_t* s, int64_t N, int64_t K, uint8_t* dst,
+                           int64_t glu_I = 0) {
     const int64_t G = num_groups(K), B = num_bands(N);
     for (int64_t b = 0; b < B; ++b) {
         for (int64_t g = 0; g < G; ++g) {
@@ -52,7 +63,7 @@ static void pack_host_impl(const int8_t* q, const uint16_t* s, int64_t N, int64_
                     for (int i = 0; i < 8; ++i) {
                         const int64_t n = b * kBandRows + nib_row(L, i);
                         const int64_t k = g * kGroupK + nib_k(L, j, i);
-                        const uint32_t u = n < N ? (uint32_t)(q[n * K + k] + 8) : 8u;
+                        const uint32_t u = n < N ? (uint32_t)(q[src_row(n, glu_I) * K + k] + 8) : 8u;
                         word |= u << (4 * i);
                     }
                     memcpy(tile + word_offset(L, j), &word, 4);  // little-endian hosts only
@@ -60,8 +71,8 @@ static void pack_host_impl(const int8_t* q, const uint16_t* s, int64_t N, int64_
             }
             for (int p = 0; p < 8; ++p) {
                 const int64_t n0 = b * kBandRows + p, n1 = n0 + 8;
-                const uint32_t lo = n0 < N ? s[n0 * G + g] : 0u;
-                const uint32_t hi = n1 < N ? s[n1 * G + g] : 0u;
+                const uint32_t lo = n0 < N ? s[src_row(n0, glu_I) * G + g] : 0u;
+                const uint32_t hi = n1 < N ? s[src_row(n1, glu_I) * G + g] : 0u;
                 const uint32_t word = lo | (hi << 16);
                 memcpy(tile + kScaleOffset + 4 * p, &word, 4);
             }
@@ -101,7 +112,7 @@ static void unpack_host_impl(const uint8_t* src, int64_t N, int64_t K, int8_t* q
 // write the tile's scale words.
 __global__ void __launch_bounds__(256) pack_kernel(const int8_t* __restrict__ q,
                                                    const uint16_t* __restrict__ s, int64_t N, int64_t K,
-                                                   uint8_t* __restrict__ dst, unsigned* bad) {
+                                                   uint8_t* __restrict__ dst, unsigned* bad, int64_t glu_I) {
     const int64_t G = K / kGroupK;
     const int64_t t = blockIdx.x;
     const int64_t b = t / G, g = t % G;
@@ -112,7 +123,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const int8_t* __restrict__ q,
     for (int i = 0; i < 8; ++i) {
         const int64_t n = b * kBandRows + nib_row(L, i);
         int v = 0;
-        if (n < N) v = q[n * K + g * kGroupK + nib_k(L, j, i)];
+        if (n < N) v = q[src_row(n, glu_I) * K + g * kGroupK + nib_k(L, j, i)];
         ok &= (v >= -8 && v <= 7);
         word |= (uint32_t)((v + 8) & 15) << (4 * i);
     }
@@ -121,8 +132,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const int8_t* __restrict__ q,
     if (threadIdx.x < 8) {
         const int p = threadIdx.x;
         const int64_t n0 = b * kBandRows + p, n1 = n0 + 8;
-        const uint32_t lo = n0 < N ? s[n0 * G + g] : 0u;
-        const uint32_t hi = n1 < N ? s[n1 * G + g] : 0u;
+        const uint32_t lo = n0 < N ? s[src_row(n0, glu_I) * G + g] : 0u;
+        const uint32_t hi = n1 < N ? s[src_row(n1, glu_I) * G + g] : 0u;
         *reinterpret_cast<uint32_t*>(tile + kScaleOffset + 4 * p) = lo | (hi << 16);
     }
     if (!ok) atomicOr(bad, 1u);
@@ -212,9 +223,8 @@ extern "C" w4_status w4_unpack_host(const void* packed, int64_t N, int64_t K, in
     return W4_OK;
 }
 
-extern "C" w4_status w4_pack(const int8_t* q, const uint16_t* scales, int64_t N, int64_t K, void* dst_dev,
-                             size_t dst_bytes, int src_on_device, void* stream, w4_weight* out) {
-    clear_error();
+static w4_status pack_impl(const int8_t* q, const uint16_t* scales, int64_t N, int64_t K, void* dst_dev,
+                           size_t dst_bytes, int src_on_device, void* stream, w4_weight* out, int64_t glu_I) {
     w4_status st = check_shape(N, K);
     if (st != W4_OK) return st;
     if (!q || !scales || !dst_dev || (src_on_device != 0 && src_on_device != 1)) {
@@ -237,7 +247,7 @@ extern "C" w4_status w4_pack(const int8_t* q, const uint16_t* scales, int64_t N,
             return W4_ERR_RANGE;
         }
         std::vector<uint8_t> host(need);
-        pack_host_impl(q, scales, N, K, host.data());
+        pack_host_impl(q, scales, N, K, host.data(), glu_I);
         W4_CUDA_TRY(cudaMemcpyAsync(dst_dev, host.data(), need, cudaMemcpyHostToDevice, s));
         W4_CUDA_TRY(cudaStreamSynchronize(s));
     } else {
@@ -247,7 +257,7 @@ extern "C" w4_status w4_pack(const int8_t* q, const uint16_t* scales, int64_t N,
         cudaError_t e = cudaMemsetAsync(bad, 0, sizeof(unsigned), s);
         const int64_t tiles = num_bands(N) * num_groups(K);
         if (e == cudaSuccess) {
-            pack_kernel<<<(unsigned)tiles, 256, 0, s>>>(q, scales, N, K, static_cast<uint8_t*>(dst_dev), bad);
+            pack_kernel<<<(unsigned)tiles, 256, 0, s>>>(q, scales, N, K, static_cast<uint8_t*>(dst_dev), bad, glu_I);
             e = cudaGetLastError();
         }
         if (e == cudaSuccess) e = cudaMemcpyAsync(&h_bad, bad, sizeof(unsigned), cudaMemcpyDeviceToHost, s);
@@ -267,6 +277,22 @@ extern "C" w4_status w4_pack(const int8_t* q, const uint16_t* scales, int64_t N,
         out->version = W4_PACK_VERSION;
     }
     return W4_OK;
+}
+
+extern "C" w4_status w4_pack(const int8_t* q, const uint16_t* scales, int64_t N, int64_t K, void* dst_dev,
+                             size_t dst_bytes, int src_on_device, void* stream, w4_weight* out) {
+    clear_error();
+    return pack_impl(q, scales, N, K, dst_dev, dst_bytes, src_on_device, stream, out, 0);
+}
+
+extern "C" w4_status w4_pack_glu(const int8_t* q, const uint16_t* scales, int64_t I, int64_t K, void* dst_dev,
+                                 size_t dst_bytes, int src_on_device, void* stream, w4_weight* out) {
+    clear_error();
+    if (I < 8 || I % 8 != 0) {
+        set_error("gated weight: I=%lld rows per half must be a positive multiple of 8", (long long)I);
+        return W4_ERR_SHAPE;
+    }
+    return pack_impl(q, scales, 2 * I, K, dst_dev, dst_bytes, src_on_device, stream, out, I);
 }
 
 extern "C" w4_status w4_unpack(const w4_weight* w, int8_t* q, uint16_t* scales, int dst_on_device, void* stream) {

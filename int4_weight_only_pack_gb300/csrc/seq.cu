@@ -169,19 +169,28 @@ extern "C" size_t w4_decode_seq_workspace_bytes(const w4_weight* w, int n, int M
     return step_workspace_bytes(w, n, M);
 }
 
-extern "C" w4_status w4_decode_seq_create_persistent_act(const w4_weight* w, const void* const* x,
-                                                         void* const* y, int n, int M, int act, void* workspace,
-                                                         size_t workspace_bytes, void* stream, w4_seq** out);
+extern "C" w4_status w4_decode_seq_create_persistent_ex(const w4_weight* w, const void* const* x,
+                                                        void* const* y, const uint32_t* op_flags, int n, int M,
+                                                        int act, void* workspace, size_t workspace_bytes,
+                                                        void* stream, w4_seq** out);
 
 extern "C" w4_status w4_decode_seq_create_persistent(const w4_weight* w, const void* const* x, void* const* y, int n,
                                                      int M, void* workspace, size_t workspace_bytes, void* stream,
                                                      w4_seq** out) {
-    return w4_decode_seq_create_persistent_act(w, x, y, n, M, W4_ACT_F16, workspace, workspace_bytes, stream, out);
+    return w4_decode_seq_create_persistent_ex(w, x, y, nullptr, n, M, W4_ACT_F16, workspace, workspace_bytes, stream,
+                                              out);
 }
 
 extern "C" w4_status w4_decode_seq_create_persistent_act(const w4_weight* w, const void* const* x,
                                                          void* const* y, int n, int M, int act, void* workspace,
                                                          size_t workspace_bytes, void* stream, w4_seq** out) {
+    return w4_decode_seq_create_persistent_ex(w, x, y, nullptr, n, M, act, workspace, workspace_bytes, stream, out);
+}
+
+extern "C" w4_status w4_decode_seq_create_persistent_ex(const w4_weight* w, const void* const* x,
+                                                        void* const* y, const uint32_t* op_flags, int n, int M,
+                                                        int act, void* workspace, size_t workspace_bytes,
+                                                        void* stream, w4_seq** out) {
     clear_error();
     if (!w || !x || !y || !out || n < 1) {
         set_error("NULL argument or n < 1");
@@ -195,13 +204,22 @@ extern "C" w4_status w4_decode_seq_create_persistent_act(const w4_weight* w, con
     for (int i = 0; i < n; ++i) {
         w4_status st = check_gemv_args(x[i], &w[i], y[i], M);
         if (st != W4_OK) return st;
+        const uint32_t f = op_flags ? op_flags[i] : 0u;
+        if (f & ~(uint32_t)W4_OP_SWIGLU) {
+            set_error("projection %d: unknown flags 0x%x", i, f);
+            return W4_ERR_ARG;
+        }
+        if ((f & W4_OP_SWIGLU) && w[i].N % 16 != 0) {
+            set_error("projection %d: a gated weight needs N = 2I rows with I a multiple of 8 (w4_pack_glu)", i);
+            return W4_ERR_SHAPE;
+        }
     }
     w4_seq* s = new w4_seq();
     s->n = n;
     s->M = M;
     s->persistent = true;
     cudaStream_t user = static_cast<cudaStream_t>(stream);
-    w4_status st = step_prepare(w, x, y, n, M, act, workspace, workspace_bytes, user, &s->step);
+    w4_status st = step_prepare(w, x, y, op_flags, n, M, act, workspace, workspace_bytes, user, &s->step);
     if (st != W4_OK) {
         delete s;
         return st;

@@ -55,7 +55,9 @@ struct StepOp {
     float* part;    // K split: partials [bands][S][16*M]
     unsigned* cnt;  // K split: arrivals per band
     int N, K, G, bands;
-    int S, cps;  // K splits; CTAs per split (grid / S)
+    int16_t S;      // K splits
+    int16_t flags;  // W4_OP_* of the projection
+    int cps;        // CTAs per split (grid / S)
 };
 static_assert(sizeof(StepOp) == 64, "one projection record");
 
@@ -96,7 +98,7 @@ struct StepSmem {
         x = (geo + nops * 16 + 127) & ~127;
         xsum = x + dec::x_bytes(MP, gpc_max);
         park = xsum + dec::xsum_bytes(MP, gpc_max);
-        total = park + kWarps * 2 * 16 * MP * 4;
+        total = park + kWarps * 3 * 16 * MP * 4;  // two parked shares + a finishing scratch per warp
     }
 };
 
@@ -216,45 +218,64 @@ __device__ __forceinline__ void for_frag(const float (&acc)[(MP + 7) / 8][4], in
 // this split's partial; the arrival that completes the band adds the S
 // partials in split order and writes y.
 template <int ACT, typename V>
-__device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, int M, int lane, V&& visit) {
+__device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, int M, int lane, V&& visit,
+                                            float* scratch, int MP) {
     using Ops = dec::ActOps<ACT>;
     const int n0 = band * 16;
+    const bool glu = (o.flags & W4_OP_SWIGLU) != 0;
+    // the band's final FP32 sums go to y, or (gated) to this warp's scratch
+    auto emit = [&](int row, int m, float v) {
+        if (glu)
+            scratch[row * MP + m] = v;
+        else if (n0 + row < o.N)
+            o.y[(size_t)m * o.N + n0 + row] = Ops::round(v);
+    };
     if (o.S == 1) {
-        visit([&](int row, int m, float v) {
-            if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = Ops::round(v);
-        });
-        return;
-    }
-    const int pb = 16 * M;
-    float* mine = o.part + ((size_t)band * o.S + r) * pb;
-    visit([&](int row, int m, float v) { mine[row * M + m] = v; });
-    // the warp's stores are ordered before lane 0's fence by the warp barrier
-    __syncwarp();
-    unsigned last = 0;
-    if (lane == 0) {
-        __threadfence();
-        last = atomicAdd(o.cnt + band, 1u) == (unsigned)(o.S - 1);
-        if (last) __threadfence();
-    }
-    last = __shfl_sync(0xFFFFFFFFu, last, 0);
-    if (!last) return;
-    const float* base = o.part + (size_t)band * o.S * pb;
-    visit([&](int row, int m, float) {
-        // eight partials in flight at a time, added in split order
-        const float* pp = base + row * M + m;
-        float sum = 0.f;
-        int s = 0;
-        for (; s + 8 <= o.S; s += 8) {
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = __ldcg(pp + (size_t)(s + e) * pb);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) sum += v[e];
+        visit(emit);
+    } else {
+        const int pb = 16 * M;
+        float* mine = o.part + ((size_t)band * o.S + r) * pb;
+        visit([&](int row, int m, float v) { mine[row * M + m] = v; });
+        // the warp's stores are ordered before lane 0's fence by the warp barrier
+        __syncwarp();
+        unsigned last = 0;
+        if (lane == 0) {
+            __threadfence();
+            last = atomicAdd(o.cnt + band, 1u) == (unsigned)(o.S - 1);
+            if (last) __threadfence();
         }
-        for (; s < o.S; ++s) sum += __ldcg(pp + (size_t)s * pb);
-        if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = Ops::round(sum);
-    });
-    if (lane == 0) o.cnt[band] = 0;  // ready for the next replay
+        last = __shfl_sync(0xFFFFFFFFu, last, 0);
+        if (!last) return;
+        const float* base = o.part + (size_t)band * o.S * pb;
+        visit([&](int row, int m, float) {
+            // eight partials in flight at a time, added in split order
+            const float* pp = base + row * M + m;
+            float sum = 0.f;
+            int s = 0;
+            for (; s + 8 <= o.S; s += 8) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = __ldcg(pp + (size_t)(s + e) * pb);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) sum += v[e];
+            }
+            for (; s < o.S; ++s) sum += __ldcg(pp + (size_t)s * pb);
+            emit(row, m, sum);
+        });
+        if (lane == 0) o.cnt[band] = 0;  // ready for the next replay
+    }
+    if (!glu) return;
+    // gated projection: rows r and r + 8 of the band are gate and up row
+    // 8*band + r; y (I = N/2 columns) gets silu(gate) * up
+    __syncwarp();
+    const int I = o.N / 2;
+    for (int oi = lane; oi < 8 * M; oi += 32) {
+        const int rr = oi / M, m = oi - rr * M;
+        const float g = scratch[rr * MP + m], u = scratch[(rr + 8) * MP + m];
+        const int n = band * 8 + rr;
+        if (n < I) o.y[(size_t)m * I + n] = Ops::round(g / (1.f + expf(-g)) * u);
+    }
+    __syncwarp();
 }
 
 template <int MP, int ACT>
@@ -273,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L.x);
     float* xsum = reinterpret_cast<float*>(smem + L.xsum);
     float* park = reinterpret_cast<float*>(smem + L.park);
-    float* park_w = park + warp * 2 * PB;
+    float* park_w = park + warp * 3 * PB;
+    float* scratch_w = park_w + 2 * PB;
 
     for (int i = threadIdx.x; i < nops; i += kThreads) put_geo(geo + i, a.ops[i], c);
     // x slices are small and read by every CTA of a split: keep the next one
@@ -370,7 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     const int us = u * q.Gs;
                     if (us >= t0 && us + q.Gs <= t1) {
                         // the whole band is this warp's: finish it from the accumulators
-                        finish_band<ACT>(o, q.ub + u, q.r, M, lane, [&](auto&& f) { for_frag<MP>(acc, lane, M, f); });
+                        finish_band<ACT>(o, q.ub + u, q.r, M, lane, [&](auto&& f) { for_frag<MP>(acc, lane, M, f); },
+                                         scratch_w, MP);
                     } else {
                         // cut between warps: park this warp's share
                         float* dst = park_w + (u == u_first ? 0 : PB);
@@ -397,11 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                         for (int w2 = warp - 1; w2 < kWarps; ++w2) {
                             const int lo = warp_lo(Tc, w2), hi = warp_lo(Tc, w2 + 1);
                             if (lo >= be) break;
-                            if (lo < hi) sum += park[(w2 * 2 + (lo >= bs ? 0 : 1)) * PB + row * MP + m];
+                            if (lo < hi) sum += park[(w2 * 3 + (lo >= bs ? 0 : 1)) * PB + row * MP + m];
                         }
                         f(row, m, sum);
                     }
-                });
+                }, scratch_w, MP);
             }
         }
         // this CTA is done with projection i: the barrier orders every
@@ -558,8 +581,8 @@ size_t step_workspace_bytes(const w4_weight* w, int n, int M) {
     return pl.total;
 }
 
-w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y, int n, int M, int act, void* ws,
-                       size_t ws_bytes, cudaStream_t stream, StepLaunch* out) {
+w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y, const uint32_t* op_flags, int n,
+                       int M, int act, void* ws, size_t ws_bytes, cudaStream_t stream, StepLaunch* out) {
     const int MP = padded(M);
     StepPlan pl;
     if (!plan_step(w, n, M, sm_count_now(), &pl)) {
@@ -584,6 +607,7 @@ w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y,
     char* base = static_cast<char*>(ws);
     for (int i = 0; i < n; ++i) {
         StepOp& o = pl.ops[i];
+        o.flags = (int16_t)(op_flags ? op_flags[i] : 0u);
         o.w = static_cast<const uint8_t*>(w[i].data);
         o.x = static_cast<const uint32_t*>(x[i]);
         o.y = static_cast<uint16_t*>(y[i]);

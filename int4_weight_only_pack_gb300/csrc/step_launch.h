@@ -21,9 +21,9 @@ struct StepLaunch {
     int NC = 0, smem = 0;
 };
 
-// act: 0 binary16 activations, 1 bfloat16.
-w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y, int n, int M, int act, void* ws,
-                       size_t ws_bytes, cudaStream_t stream, StepLaunch* out);
+// act: 0 binary16 activations, 1 bfloat16; op_flags: W4_OP_* per projection (may be NULL).
+w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y, const uint32_t* op_flags, int n,
+                       int M, int act, void* ws, size_t ws_bytes, cudaStream_t stream, StepLaunch* out);
 w4_status step_launch(const StepLaunch& s, cudaStream_t stream);
 int step_status(const StepLaunch& s);
 size_t step_workspace_bytes(const w4_weight* w, int n, int M);

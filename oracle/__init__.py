@@ -107,6 +107,23 @@ def linear(x: np.ndarray, q: np.ndarray, s: np.ndarray, threads: int = 0,
     return (y, acc) if want_acc else y
 
 
+def swiglu(x: np.ndarray, q: np.ndarray, s: np.ndarray, threads: int = 0, want_acc: bool = False,
+           act: str = "fp16"):
+    """Gated MLP output h = rne(silu(g) * u) of a stacked [gate; up] weight
+    (q [2I, K], s [2I, K/128]): g and u are the FP64 sums of gate row n and up
+    row n (no intermediate rounding), silu(g) = g / (1 + exp(-g)) in FP64.
+    SwiGLU is Qwen2.5's MLP activation; the pages do not name it.  Returns h
+    as uint16 [M, I] bits of the activation type (and the FP64 h)."""
+    _, acc = linear(x, q, s, threads=threads, want_acc=True, act=act)
+    I = q.shape[0] // 2
+    g, u = acc[:, :I], acc[:, I:]
+    with np.errstate(over="ignore"):
+        h = g / (1.0 + np.exp(-g)) * u
+    enc = bf16_from_double if act == "bf16" else half_from_double
+    bits = np.array([enc(v) for v in h.ravel()], dtype=np.uint16).reshape(h.shape)
+    return (bits, h) if want_acc else bits
+
+
 def pack_layout(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     """The packed layout of (q, s), written from its definition (uint8)."""
     q = np.ascontiguousarray(q, dtype=np.int8)

@@ -86,3 +86,21 @@ def test_device_pack_rejects_out_of_range_q():
     with pytest.raises(w4.W4Error) as e:
         w4.w4_pack(dev(q), dev(s), 32, 256, packed, dst_bytes=100)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("I,K", [(8, 128), (320, 256), (72, 1152)])
+def test_pack_glu_is_the_layout_of_interleaved_rows(I, K):
+    """w4_pack_glu equals the oracle's layout writer applied to the stacked
+    [gate; up] rows permuted (in numpy) so that band b holds gate rows
+    8b..8b+7 then up rows 8b..8b+7."""
+    rng = np.random.default_rng(I + K)
+    q = rng.integers(-8, 8, (2 * I, K)).astype(np.int8)
+    s = (0.005 + 0.015 * rng.random((2 * I, K // 128))).astype(np.float16).view(np.uint16)
+    order = np.concatenate([np.concatenate([np.arange(8 * b, 8 * b + 8), I + np.arange(8 * b, 8 * b + 8)])
+                            for b in range(I // 8)])
+    want = oracle.pack_layout(q[order], s[order])
+    dst = torch.zeros(w4.w4_packed_bytes(2 * I, K), dtype=torch.uint8, device="cuda")
+    w = w4.w4_pack_glu(dev(q), dev(s), I, K, dst)
+    torch.cuda.synchronize()
+    assert (w.N, w.K) == (2 * I, K)
+    assert np.array_equal(dst.cpu().numpy(), want)

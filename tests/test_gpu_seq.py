@@ -224,3 +224,63 @@ def test_bf16_activation_type_is_checked():
     rc = w4.lib().w4_decode_seq_create_persistent_act(warr, xa, ya, 1, 1, 2, buf[off:].data_ptr(), nb, None,
                                                       ctypes.byref(h))
     assert rc == 1 and not h.value  # W4_ERR_ARG, nothing created
+
+
+@pytest.mark.parametrize("M,act", [(1, "fp16"), (5, "fp16"), (16, "fp16"), (1, "bf16"), (3, "bf16")])
+def test_swiglu_projection_in_sequence(M, act):
+    """Gated MLP projections (W4_OP_SWIGLU, weights from w4_pack_glu) mixed
+    with plain ones in one persistent sequence, against the oracle's
+    h = rne(silu(g) * u); includes the real gate_up shape (I = 18944)."""
+    rng = np.random.default_rng(200 + M)
+    plan = [("plain", 160, 256), ("glu", 320, 256), ("plain", 640, 1280), ("glu", 18944, 3584)]
+    keep, ws, xs, ys, flags, probs = [], [], [], [], [], []
+    for kind, n, K in plan:
+        rows = 2 * n if kind == "glu" else n
+        if act == "bf16":
+            x, q, s = bf16_problem(rng, M, rows, K)
+        else:
+            x, q, s = rand_problem(rng, M, rows, K)
+        packed = torch.empty(w4.w4_packed_bytes(rows, K), dtype=torch.uint8, device="cuda")
+        if kind == "glu":
+            w = w4.w4_pack_glu(dev(q), dev(s), n, K, packed)
+        else:
+            w = w4.w4_pack(dev(q), dev(s), rows, K, packed)
+        keep.append(packed)
+        ws.append(w)
+        xs.append(dev(x))
+        ys.append(torch.zeros((M, n), dtype=torch.int16, device="cuda"))
+        flags.append(w4.W4_OP_SWIGLU if kind == "glu" else 0)
+        probs.append((kind, x, q, s))
+    nb = w4.w4_decode_seq_workspace_bytes(ws, M)
+    buf = torch.zeros(nb + 256, dtype=torch.uint8, device="cuda")
+    off = (-buf.data_ptr()) % 256
+    seq = w4.DecodeSeq(ws, xs, ys, M, workspace=buf[off:off + nb], act=act, op_flags=flags)
+    seq.replay()
+    torch.cuda.synchronize()
+    assert seq.status() == 0
+    for i, (kind, x, q, s) in enumerate(probs):
+        ref = oracle.swiglu(x, q, s, act=act) if kind == "glu" else oracle.linear(x, q, s, act=act)
+        assert_close(host(ys[i]), ref, "%s projection %d" % (kind, i), act=act)
+    seq.close()
+
+
+def test_swiglu_flag_checks():
+    rng = np.random.default_rng(9)
+    x, q, s = rand_problem(rng, 1, 40, 256)  # N = 40 is not a gated weight
+    packed, w = pack_on_device(q, s)
+    y = torch.zeros((1, 20), dtype=torch.int16, device="cuda")
+    nb = w4.w4_decode_seq_workspace_bytes([w], 1)
+    buf = torch.zeros(nb + 256, dtype=torch.uint8, device="cuda")
+    off = (-buf.data_ptr()) % 256
+    with pytest.raises(w4.W4Error) as e:
+        w4.DecodeSeq([w], [dev(x)], [y], 1, workspace=buf[off:off + nb], op_flags=[w4.W4_OP_SWIGLU])
+    assert e.value.status == 2
+    with pytest.raises(w4.W4Error) as e:
+        w4.DecodeSeq([w], [dev(x)], [y], 1, workspace=buf[off:off + nb], op_flags=[4])
+    assert e.value.status == 1
+    q2 = rng.integers(-8, 8, (24, 256)).astype(np.int8)  # I = 12: not a multiple of 8
+    s2 = (0.005 + 0.015 * rng.random((24, 2))).astype(np.float16).view(np.uint16)
+    dst = torch.empty(w4.w4_packed_bytes(24, 256), dtype=torch.uint8, device="cuda")
+    with pytest.raises(w4.W4Error) as e:
+        w4.w4_pack_glu(dev(q2), dev(s2), 12, 256, dst)
+    assert e.value.status == 2
