@@ -388,6 +388,25 @@ def swiglu_step(torch, w4, synth, st, reps=100):
     return out
 
 
+def int8_step(torch, w4, st, reps=100):
+    """The same 28-layer step on the pages' Path A: x (binary16, as in the
+    headline) quantised per token to INT8 inside the kernel and dotted with
+    dp4a.  us/step and weight GB/s, to set against the binary16 headline."""
+    nbw = w4.w4_decode_seq_workspace_bytes(st["ws"], 1)
+    buf = torch.zeros(nbw + 256, dtype=torch.uint8, device="cuda")
+    off = (-buf.data_ptr()) % 256
+    ys = [torch.zeros_like(y) for y in st["ys"]]
+    seq = w4.DecodeSeq(st["ws"], st["xs"], ys, 1, workspace=buf[off:off + nbw], act="int8")
+    for _ in range(5):
+        seq.replay()
+    ms = time_replays(torch, seq.replay, reps)
+    peak = measured_peaks()[0].get("hbm_gbs", FALLBACK_HBM_GBS)
+    out = {"us_per_step": ms * 1e3, "GB/s": BYTES_PER_STEP / (ms * 1e-3) / 1e9,
+           "frac_of_hbm": BYTES_PER_STEP / (ms * 1e-3) / 1e9 / peak, "status_word": seq.status()}
+    seq.close()
+    return out
+
+
 def packed_file_load(torch, w4, st):
     """Layer 0's four packed weights written to packed-weight files and read
     back (header + checksum validation + one host-to-device copy each) into
@@ -557,6 +576,7 @@ def main():
         extras["packed_file_layer0"] = packed_file_load(torch, w4, st)
         extras["bf16_activations_step_M1"] = bf16_step(torch, w4, synth, st)
         extras["swiglu_fused_gate_up_step_M1"] = swiglu_step(torch, w4, synth, st)
+        extras["path_a_int8_step_M1"] = int8_step(torch, w4, st)
 
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))

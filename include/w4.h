@@ -276,9 +276,15 @@ w4_status w4_decode_seq_create_persistent(const w4_weight* w, const void* const*
 /* Activation types of the persistent sequence. */
 #define W4_ACT_F16 0  /* x and y IEEE binary16 (the pages' FP16 activations) */
 #define W4_ACT_BF16 1 /* x and y bfloat16; scales stay binary16 */
+#define W4_ACT_I8 2   /* the pages' Path A ("3. The INT8 vs. FP16 Activation Trade-off"):
+                         x binary16, quantised per token to INT8 inside the kernel
+                         (sx = max|x| / 127 and xq = rne(x / sx) in IEEE binary32),
+                         exact integer group sums (dp4a), y binary16 =
+                         rne(sum_g s * sx * sum_k xq * q) with FP32 scaling */
 
 /* w4_decode_seq_create_persistent with the activation type chosen (act =
- * W4_ACT_F16 is w4_decode_seq_create_persistent).  With W4_ACT_BF16, x and y
+ * W4_ACT_F16 is w4_decode_seq_create_persistent; W4_ACT_I8 is described
+ * above).  With W4_ACT_BF16, x and y
  * are bfloat16 and y = bf16_rne(sum x * q * s) with FP32 accumulation: the
  * the benchmark spec's FP16/BF16 activation conversion applied to the pages'
  * projection ("Building a Custom LLM Inference Runtime ...", "Technical

@@ -270,7 +270,7 @@ class DecodeSeq:
     (w4_decode_seq_create_persistent); otherwise as a graph of one kernel per
     projection (w4_decode_seq_create)."""
 
-    ACT = {"fp16": 0, "bf16": 1}
+    ACT = {"fp16": 0, "bf16": 1, "int8": 2}
 
     def __init__(self, weights, xs, ys, M: int, use_pdl: bool = True, stream=None, workspace=None,
                  workspace_bytes: int | None = None, act: str = "fp16", op_flags=None):

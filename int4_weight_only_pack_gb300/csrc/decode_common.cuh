@@ -37,7 +37,7 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
 }
 
 // Activation types: binary16 (the pages' FP16 activations) or bfloat16.
-enum : int { kActF16 = 0, kActBF16 = 1 };
+enum : int { kActF16 = 0, kActBF16 = 1, kActI8 = 2 };  // kActI8: binary16 x quantised to INT8 (Path A)
 
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -118,6 +118,11 @@ struct ActOps<kActBF16> {
     }
 };
 
+template <>
+struct ActOps<kActI8> {
+    __device__ static __forceinline__ uint16_t round(float v) { return __half_as_ushort(__float2half_rn(v)); }
+};
+
 // Shared-memory bytes of an x slice of Gs groups for MP padded tokens, and of
 // its per-group sums: xsum[gl * xsum_stride(MP) + m] (the stride is even so
 // that a lane reads its token pair as one float2; eight floats of slack cover
@@ -126,7 +131,7 @@ struct ActOps<kActBF16> {
 __host__ __device__ constexpr int x_bytes(int MP, int Gs) { return MP * Gs * 256; }
 __host__ __device__ constexpr int xsum_stride(int MP) { return MP < 2 ? 2 : MP; }
 __host__ __device__ constexpr int xsum_bytes(int MP, int Gs) {
-    return ((Gs * xsum_stride(MP) + 8) * 4 + 15) & ~15;
+    return ((Gs * xsum_stride(MP) + 8 + 16) * 4 + 15) & ~15;  // + 16 floats: per-token scales (INT8 path)
 }
 
 // Stage x[0:M, 128*g_lo : 128*(g_lo+Gs)) (fp16 pairs; row stride K/2 words)
@@ -262,7 +267,7 @@ struct TileMac {
     uint4 xv[4][NT];                         // x fragments of up to four tiles
     float2 X[4][NT];                         // group sums of up to four tiles
 
-    __device__ __forceinline__ TileMac(uint32_t x_smem, uint32_t xsum_smem, int lane) {
+    __device__ __forceinline__ TileMac(uint32_t x_smem, uint32_t xsum_smem, int lane, int /*Gs*/ = 0) {
         const int tok = lane >> 2, cl4 = lane & 3;
         xfrag = x_smem + (uint32_t)(((tok % MP) * 4 + cl4) * 16);
         xsum = xsum_smem + (uint32_t)(2 * cl4 * 4);
@@ -365,6 +370,152 @@ __device__ __forceinline__ void block_sums(const float* red, int BB, int nb, int
         }
     }
 }
+
+// ---- Path A: INT8 activations ----------------------------------------------------
+// Per-token symmetric quantisation in IEEE binary32 (round-to-nearest
+// division, then round half to even): sx = max_k |x| / 127,
+// xq = rne(x / sx) clamped to +-127.  The CTA reads the whole row for the
+// maximum and quantises its K slice into shared memory as bytes in the order
+// the nibble bytes come out of a packed word ((v & 0x0F0F0F0F) gives k 4c+0,
+// 4c+2, 4c+1, 4c+3 of rows r; (v >> 4) the same of rows r + 8): word
+// ((gl*MP + m)*4 + c)*8 + j holds k16 step j of lane class c.  Per group and
+// token the integer sum of xq goes to xsum[gl*xsum_stride(MP) + m] (as int)
+// and sx to xsum[Gs*xsum_stride(MP) + 8 + m].
+template <int MP, int NCONS>
+__device__ __forceinline__ void stage_x_q8(const uint32_t* x, int M, int K, int g_lo, int Gs, uint32_t* xs,
+                                           float* xsum, float* red /* NCONS / 32 * MP floats of scratch */) {
+    constexpr int kWarps = NCONS / 32;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kp = K / 2;
+    float* sxs = xsum + Gs * xsum_stride(MP) + 8;
+    int* isum = reinterpret_cast<int*>(xsum);
+    for (int m = 0; m < M; ++m) {
+        float mx = 0.f;
+        for (int i = tid; i < kp; i += NCONS) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(x + (size_t)m * kp + i));
+            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+        if (lane == 0) red[warp * MP + m] = mx;
+    }
+    tc::named_barrier(1, NCONS);
+    if (tid < MP) {
+        float mx = 0.f;
+        if (tid < M)
+            for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, red[w * MP + tid]);
+        sxs[tid] = __fdiv_rn(mx, 127.f);
+    }
+    tc::named_barrier(1, NCONS);
+    // quantise the slice: one thread per (token, group, k16 step, lane class)
+    const uint32_t* xg = x + (size_t)g_lo * 64;
+    for (int idx = tid; idx < MP * Gs * 32; idx += NCONS) {
+        const int m = idx / (Gs * 32), rest = idx - m * (Gs * 32);
+        const int gl = rest >> 5, jc = rest & 31, j = jc >> 2, c = jc & 3;
+        uint32_t word = 0;
+        if (m < M) {
+            const float sc = sxs[m];
+            const int k0 = gl * 128 + 16 * j + 4 * c;  // within the slice
+            const uint32_t w01 = xg[(size_t)m * kp + k0 / 2], w23 = xg[(size_t)m * kp + k0 / 2 + 1];
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w01));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w23));
+            const float v[4] = {a.x, b.x, a.y, b.y};  // k 4c+0, 4c+2, 4c+1, 4c+3
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int qv = 0;
+                if (sc > 0.f) qv = max(-127, min(127, __float2int_rn(__fdiv_rn(v[e], sc))));
+                word |= (uint32_t)(qv & 0xFF) << (8 * e);
+            }
+        }
+        xs[((gl * MP + m) * 4 + c) * 8 + j] = word;
+    }
+    tc::named_barrier(1, NCONS);
+    // integer sum of xq per group and token
+    for (int idx = warp; idx < Gs * MP; idx += kWarps) {
+        const int gl = idx / MP, m = idx - gl * MP;
+        const uint32_t w = xs[((gl * MP + m) * 4 + (lane >> 3)) * 8 + (lane & 7)];
+        int sum = (int)(int8_t)(w & 0xFF) + (int)(int8_t)((w >> 8) & 0xFF) + (int)(int8_t)((w >> 16) & 0xFF) +
+                  (int)(int8_t)(w >> 24);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+        if (lane == 0) isum[gl * xsum_stride(MP) + m] = sum;
+    }
+    tc::named_barrier(1, NCONS);
+}
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Path A tile multiply-accumulate: per lane, for rows r and r + 8 and every
+// token, exact integer dot products of the nibbles u (unsigned bytes) with
+// xq (signed bytes) over the lane's 32 k of the group (dp4a); the four lanes
+// of a row quad add theirs (shuffles), and each lane keeps the tokens its MMA
+// fragment position owns, so the reduction and finishing code is the one of
+// the tensor-core path:
+//     acc += s * sx * (sum_k u*xq - 8 * sum_k xq)
+template <int MP>
+struct TileMac<MP, kActI8> {
+    static constexpr int NT = (MP + 7) / 8;
+    uint32_t xq_base, xsum_base, sx_base;
+    int gs_stride;
+
+    __device__ __forceinline__ TileMac(uint32_t x_smem, uint32_t xsum_smem, int lane, int Gs) {
+        const int c = lane & 3;
+        xq_base = x_smem + (uint32_t)(c * 8 * 4);
+        xsum_base = xsum_smem;
+        sx_base = xsum_smem + (uint32_t)((Gs * xsum_stride(MP) + 8) * 4);
+        gs_stride = Gs;
+    }
+
+    template <int NTL>
+    __device__ __forceinline__ void run_tiles(uint32_t ta, int gl, int lane, float (&acc)[NT][4]) {
+#pragma unroll
+        for (int n = 0; n < NTL; ++n) run(ta + (uint32_t)(n * kTileBytes), gl + n, lane, acc);
+    }
+
+    __device__ __forceinline__ void run(uint32_t ta, int gl, int lane, float (&acc)[NT][4]) {
+        const uint4 lo4 = lds128(ta + 16 * lane), hi4 = lds128(ta + 512 + 16 * lane);
+        const uint32_t sc = lds32(ta + kScaleOffset + 4 * (lane >> 2));
+        const uint32_t wd[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+        uint32_t lo[8], hi[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            lo[j] = wd[j] & 0x0F0F0F0Fu;
+            hi[j] = (wd[j] >> 4) & 0x0F0F0F0Fu;
+        }
+        const float2 s = __half22float2(*reinterpret_cast<const __half2*>(&sc));  // rows r, r + 8
+        const int cl4 = lane & 3;
+        const int* isum = reinterpret_cast<const int*>(__cvta_shared_to_generic(xsum_base));
+        const float* sx = reinterpret_cast<const float*>(__cvta_shared_to_generic(sx_base));
+#pragma unroll
+        for (int m = 0; m < MP; ++m) {
+            const uint32_t xa = xq_base + (uint32_t)((gl * MP + m) * 4 * 8 * 4);
+            const uint4 x0 = lds128(xa), x1 = lds128(xa + 16);
+            const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            int ar = 0, ar8 = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                ar = dp4a_us(lo[j], xw[j], ar);
+                ar8 = dp4a_us(hi[j], xw[j], ar8);
+            }
+            ar += __shfl_xor_sync(0xFFFFFFFFu, ar, 1);
+            ar8 += __shfl_xor_sync(0xFFFFFFFFu, ar8, 1);
+            ar += __shfl_xor_sync(0xFFFFFFFFu, ar, 2);
+            ar8 += __shfl_xor_sync(0xFFFFFFFFu, ar8, 2);
+            // the lane whose fragment position holds token m keeps it
+            const int nt = m >> 3, e = m & 1;
+            if (((m & 7) >> 1) == cl4) {
+                const int b8 = 8 * isum[gl * xsum_stride(MP) + m];
+                const float f = sx[m];
+                acc[nt][e] = fmaf(s.x * f, (float)(ar - b8), acc[nt][e]);
+                acc[nt][2 + e] = fmaf(s.y * f, (float)(ar8 - b8), acc[nt][2 + e]);
+            }
+        }
+    }
+};
 
 }  // namespace dec
 }  // namespace w4

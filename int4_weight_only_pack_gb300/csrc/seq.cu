@@ -197,7 +197,7 @@ extern "C" w4_status w4_decode_seq_create_persistent_ex(const w4_weight* w, cons
         return W4_ERR_ARG;
     }
     *out = nullptr;
-    if (act != W4_ACT_F16 && act != W4_ACT_BF16) {
+    if (act != W4_ACT_F16 && act != W4_ACT_BF16 && act != W4_ACT_I8) {
         set_error("unknown activation type %d", act);
         return W4_ERR_ARG;
     }

@@ -346,8 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         }
         const Geo q = get_geo(geo + i);
         if (q.nu > 0) {
-            dec::stage_x_async<MP, kThreads, ACT>(o.x, M, o.K, q.g_lo, q.Gs, xs, xsum);
-            dec::TileMac<MP, ACT> mac(sbase + L.x, sbase + L.xsum, lane);
+            if constexpr (ACT == dec::kActI8)
+                dec::stage_x_q8<MP, kThreads>(o.x, M, o.K, q.g_lo, q.Gs, xs, xsum, park);  // parks are free now
+            else
+                dec::stage_x_async<MP, kThreads, ACT>(o.x, M, o.K, q.g_lo, q.Gs, xs, xsum);
+            dec::TileMac<MP, ACT> mac(sbase + L.x, sbase + L.xsum, lane, q.Gs);
             const int Tc = q.Tc();
             const int t0 = warp_lo(Tc, warp), t1 = warp_lo(Tc, warp + 1);
             const int u_first = div_small(t0, q.Gs, q.inv_gs);
@@ -468,7 +471,9 @@ StepKernel step_fn_act(int MP) {
     }
 }
 StepKernel step_fn(int MP, int act) {
-    return act == dec::kActBF16 ? step_fn_act<dec::kActBF16>(MP) : step_fn_act<dec::kActF16>(MP);
+    if (act == dec::kActBF16) return step_fn_act<dec::kActBF16>(MP);
+    if (act == dec::kActI8) return step_fn_act<dec::kActI8>(MP);
+    return step_fn_act<dec::kActF16>(MP);
 }
 
 int padded(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }

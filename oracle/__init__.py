@@ -50,6 +50,13 @@ def lib():
         L.w4o_linear_act.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                      ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        L.w4o_quantize_x8.restype = None
+        L.w4o_quantize_x8.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                      ctypes.c_void_p]
+        L.w4o_linear_q8.restype = ctypes.c_int
+        L.w4o_linear_q8.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                    ctypes.c_void_p, ctypes.c_void_p]
         L.w4o_linear.restype = ctypes.c_int
         L.w4o_linear.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
@@ -104,6 +111,31 @@ def linear(x: np.ndarray, q: np.ndarray, s: np.ndarray, threads: int = 0,
                               _ptr(acc) if acc is not None else None, threads)
     if rc != 0:
         raise ValueError("w4o_linear failed: %d" % rc)
+    return (y, acc) if want_acc else y
+
+
+def quantize_x8(x: np.ndarray):
+    """Path A's per-token INT8 quantisation of fp16 x [M, K]: (xq int8, sx float32)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    M, K = x.shape
+    xq = np.zeros((M, K), dtype=np.int8)
+    sx = np.zeros(M, dtype=np.float32)
+    lib().w4o_quantize_x8(_ptr(x), M, K, _ptr(xq), _ptr(sx))
+    return xq, sx
+
+
+def linear_q8(x: np.ndarray, q: np.ndarray, s: np.ndarray, want_acc: bool = False):
+    """Path A: y = fp16_rne(sum_g s * sx * sum_k xq * q) (uint16 [M, N])."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    s = np.ascontiguousarray(s, dtype=np.uint16)
+    M, K = x.shape
+    N = q.shape[0]
+    y = np.zeros((M, N), dtype=np.uint16)
+    acc = np.zeros((M, N), dtype=np.float64) if want_acc else None
+    rc = lib().w4o_linear_q8(_ptr(x), _ptr(q), _ptr(s), M, N, K, _ptr(y), _ptr(acc) if acc is not None else None)
+    if rc != 0:
+        raise ValueError("w4o_linear_q8 failed: %d" % rc)
     return (y, acc) if want_acc else y
 
 

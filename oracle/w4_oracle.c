@@ -137,6 +137,80 @@ uint16_t w4o_bf16_from_double(double v)
     return (uint16_t)(sign | bits);
 }
 
+/* ---- INT8 activations (Path A) ------------------------------------------ */
+/* Per-token symmetric INT8 quantisation in IEEE binary32 (the precision the
+ * GPU takes the same integer decision in): amax = max_k |x|, sx = amax / 127,
+ * xq = round-half-even(x / sx), clamped to [-127, 127]; sx = 0 (all-zero row)
+ * gives xq = 0. */
+void w4o_quantize_x8(const uint16_t* x, int64_t M, int64_t K, int8_t* xq, float* sx)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            const float v = fabsf((float)w4o_double_from_half(x[m * K + k]));
+            if (v > amax)
+                amax = v;
+        }
+        const float scale = amax / 127.0f;
+        sx[m] = scale;
+        for (int64_t k = 0; k < K; ++k) {
+            long r = 0;
+            if (scale > 0.0f) {
+                const float t = (float)w4o_double_from_half(x[m * K + k]) / scale;
+                r = lrintf(t); /* default rounding mode: to nearest, ties to even */
+                if (r > 127)
+                    r = 127;
+                if (r < -127)
+                    r = -127;
+            }
+            xq[m * K + k] = (int8_t)r;
+        }
+    }
+}
+
+/* y[m,n] = half_rne( sum_g s[n,g] * sx[m] * sum_{k in g} xq[m,k] * q[n,k] ):
+ * the integer group sums exactly (int64), the scaling and the sum over
+ * groups in FP64.  acc as in w4o_linear.  Same return codes. */
+int w4o_linear_q8(const uint16_t* x, const int8_t* q, const uint16_t* s,
+                  int64_t M, int64_t N, int64_t K, uint16_t* y, double* acc)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 128 != 0)
+        return -1;
+    if (M == 0 || N == 0)
+        return 0;
+    if (!x || !q || !s || !y)
+        return -1;
+    for (int64_t i = 0; i < N * K; ++i)
+        if (q[i] < -8 || q[i] > 7)
+            return -2;
+    int8_t* xq = (int8_t*)malloc((size_t)(M * K));
+    float* sx = (float*)malloc((size_t)M * sizeof(float));
+    if (!xq || !sx) {
+        free(xq);
+        free(sx);
+        return -1;
+    }
+    w4o_quantize_x8(x, M, K, xq, sx);
+    const int64_t G = K / 128;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t m = 0; m < M; ++m) {
+            double sum = 0.0;
+            for (int64_t g = 0; g < G; ++g) {
+                int64_t isum = 0;
+                for (int64_t k = 128 * g; k < 128 * g + 128; ++k)
+                    isum += (int64_t)xq[m * K + k] * (int64_t)q[n * K + k];
+                sum += w4o_double_from_half(s[n * G + g]) * (double)sx[m] * (double)isum;
+            }
+            y[m * N + n] = w4o_half_from_double(sum);
+            if (acc)
+                acc[m * N + n] = sum;
+        }
+    }
+    free(xq);
+    free(sx);
+    return 0;
+}
+
 /* ---- the projection --------------------------------------------------- */
 typedef struct {
     const uint16_t* x;

@@ -65,6 +65,19 @@ int w4o_linear_act(const uint16_t* x, int act, const int8_t* q, const uint16_t* 
                    int64_t M, int64_t N, int64_t K,
                    uint16_t* y, double* acc, int nthreads);
 
+/* Path A of the pages ("Building a Custom LLM Inference Runtime ...", "3. The
+ * INT8 vs. FP16 Activation Trade-off"; "The Architecture of Modern Inference
+ * ...", "3. The Performance Paradox"): activations quantised to INT8 and
+ * integer dot products.  The pages give no quantisation details; the
+ * reading taken: per-token symmetric absmax, in IEEE binary32,
+ * sx = max|x| / 127, xq = rne(x / sx) clamped to +-127 (the integer
+ * decision in the GPU's precision), then
+ * y = half_rne(sum_g s * sx * sum_{k in g} xq * q) with exact integer group
+ * sums and FP64 scaling.  w4o_quantize_x8 exposes the quantisation. */
+void w4o_quantize_x8(const uint16_t* x, int64_t M, int64_t K, int8_t* xq, float* sx);
+int w4o_linear_q8(const uint16_t* x, const int8_t* q, const uint16_t* s,
+                  int64_t M, int64_t N, int64_t K, uint16_t* y, double* acc);
+
 /* The packed device layout, written out plainly from its definition
  * (the layout is a design of this library, not of the pages; the pages only
  * say that the nibbles are shuffled for the byte-permute datapath:

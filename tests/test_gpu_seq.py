@@ -221,7 +221,7 @@ def test_bf16_activation_type_is_checked():
     xa = (ctypes.c_void_p * 1)(dev(x).data_ptr())
     ya = (ctypes.c_void_p * 1)(y.data_ptr())
     h = ctypes.c_void_p()
-    rc = w4.lib().w4_decode_seq_create_persistent_act(warr, xa, ya, 1, 1, 2, buf[off:].data_ptr(), nb, None,
+    rc = w4.lib().w4_decode_seq_create_persistent_act(warr, xa, ya, 1, 1, 7, buf[off:].data_ptr(), nb, None,
                                                       ctypes.byref(h))
     assert rc == 1 and not h.value  # W4_ERR_ARG, nothing created
 
@@ -284,3 +284,60 @@ def test_swiglu_flag_checks():
     with pytest.raises(w4.W4Error) as e:
         w4.w4_pack_glu(dev(q2), dev(s2), 12, 256, dst)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("M", [1, 2, 8, 16])
+def test_int8_path_matches_oracle(M):
+    """Path A (W4_ACT_I8): x quantised per token to INT8 inside the kernel,
+    exact integer group sums, against the oracle's Path A (same binary32
+    quantisation decisions, exact integer sums, FP64 scaling).  Includes the
+    K-split down shape and an all-zero token."""
+    rng = np.random.default_rng(300 + M)
+    shapes = MINI + [(3584, 18944), (4608, 3584)]
+    probs, keep, ws, xs, ys = [], [], [], [], []
+    for N, K in shapes:
+        x, q, s = rand_problem(rng, M, N, K)
+        if M > 1:
+            x[M - 1] = 0  # sx = 0: xq = 0, y = 0
+        packed, w = pack_on_device(q, s)
+        keep.append(packed)
+        ws.append(w)
+        xs.append(dev(x))
+        ys.append(torch.zeros((M, N), dtype=torch.int16, device="cuda"))
+        probs.append((x, q, s))
+    nb = w4.w4_decode_seq_workspace_bytes(ws, M)
+    buf = torch.zeros(nb + 256, dtype=torch.uint8, device="cuda")
+    off = (-buf.data_ptr()) % 256
+    seq = w4.DecodeSeq(ws, xs, ys, M, workspace=buf[off:off + nb], act="int8")
+    seq.replay()
+    torch.cuda.synchronize()
+    assert seq.status() == 0
+    for i, (x, q, s) in enumerate(probs):
+        got = host(ys[i])
+        assert_close(got, oracle.linear_q8(x, q, s), "projection %d" % i)
+        if M > 1:
+            assert np.all((got[M - 1] & 0x7FFF) == 0)
+    seq.close()
+
+
+def test_int8_path_accuracy_against_fp16_activations():
+    """What INT8 activations cost in accuracy (the trade-off the pages weigh):
+    Path A's y against the unquantised W4A16 oracle, rms error relative to
+    rms(y), on the four layer shapes at M = 1 (per-token absmax INT8 keeps it
+    near 1%)."""
+    rng = np.random.default_rng(7)
+    for name, (N, K) in LAYER.items():
+        x, q, s = rand_problem(rng, 1, N, K)
+        packed, w = pack_on_device(q, s)
+        y = torch.zeros((1, N), dtype=torch.int16, device="cuda")
+        nb = w4.w4_decode_seq_workspace_bytes([w], 1)
+        buf = torch.zeros(nb + 256, dtype=torch.uint8, device="cuda")
+        off = (-buf.data_ptr()) % 256
+        seq = w4.DecodeSeq([w], [dev(x)], [y], 1, workspace=buf[off:off + nb], act="int8")
+        seq.replay()
+        torch.cuda.synchronize()
+        ya = host(y).view(np.float16).astype(np.float64)
+        yb = oracle.linear(x, q, s).view(np.float16).astype(np.float64)
+        rel = np.sqrt(np.mean((ya - yb) ** 2)) / np.sqrt(np.mean(yb ** 2))
+        assert 1e-4 < rel < 0.03, (name, rel)
+        seq.close()
