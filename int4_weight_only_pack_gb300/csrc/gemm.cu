@@ -12,12 +12,13 @@
 // One CTA computes a 128 (weight rows) x 128 (tokens) tile over a K range,
 // one 128-wide group per pipeline stage, with warp-specialised roles:
 //   warp 0     TMA producer: x tile [128 tokens][128 K] as two 128-byte
-//              swizzled boxes (zero fill past M)
+//              swizzled boxes (zero fill past M), and the group's 8 packed
+//              weight tiles (bulk copies) into the same pipeline stage
 //   warp 1     one thread issues 8 tcgen05.mma (128x128x16) per group into a
 //              TMEM buffer (two buffers alternate), then commits
-//   warps 4-7  dequant: stream the 8 packed tiles of the group (16-byte
-//              non-coherent loads, next group prefetched), unpack nibbles to
-//              exact fp16 q, write them K-major with the 128-byte swizzle
+//   warps 4-7  dequant: read the group's packed tiles from the stage, unpack
+//              nibbles to exact fp16 q, write them K-major with the 128-byte
+//              swizzle
 //   warps 8-15 promote: read the group's FP32 partial from TMEM, multiply by
 //              the group scale and add to FP32 accumulators in registers;
 //              finally write y (or an FP32 split-K partial)
@@ -46,9 +47,10 @@ constexpr int kBN = 128;                   // tokens per CTA
 constexpr int kStages = 3;                 // one 128-wide K group per stage
 constexpr int kAStage = kBM * 128 * 2;     // 32 KB of fp16 q
 constexpr int kBStage = kBN * 128 * 2;     // 32 KB of fp16 x
+constexpr int kWStage = 8 * kTileBytes;    // the group's 8 packed tiles (one per band)
 constexpr int kThreads = 512;
 constexpr int kTmemCols = 256;             // two 128-column FP32 accumulators
-constexpr int kSmemBytes = kStages * (kAStage + kBStage) + 1024 + 256;
+constexpr int kSmemBytes = kStages * (kAStage + kBStage + kWStage) + 1024 + 256;
 constexpr size_t kStatusBytes = 256;       // workspace head: status word (+ padding)
 
 struct GemmParams {
@@ -64,10 +66,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + kStages * kAStage;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBStage);
+    uint8_t* sW = sB + kStages * kBStage;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sW + kStages * kWStage);
     // barrier slots
     const uint32_t x_full = tc::smem_addr(bars), a_full = x_full + 8 * kStages, empty = a_full + 8 * kStages,
-                   d_full = empty + 8 * kStages, d_empty = d_full + 16;
+                   d_full = empty + 8 * kStages, d_empty = d_full + 16, w_full = d_empty + 16;
     __shared__ uint32_t tmem_base_sh;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -83,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             tc::mbar_init(x_full + 8 * s, 1);
             tc::mbar_init(a_full + 8 * s, 4);
             tc::mbar_init(empty + 8 * s, 1);
+            tc::mbar_init(w_full + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(d_full + 8 * b, 1);
@@ -113,11 +117,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const int k0 = (g_lo + it) * 128;
                 tc::tma_load_2d(dst, &xmap, k0, tok0, x_full + 8 * s);
                 tc::tma_load_2d(dst + kBStage / 2, &xmap, k0 + 64, tok0, x_full + 8 * s);
+                // the group's packed tiles, one per band of this CTA
+                const int nb = min(8, p.bands - band0);
+                tc::mbar_arrive_expect_tx(w_full + 8 * s, (uint32_t)(nb * kTileBytes));
+                const uint32_t wdst = tc::smem_addr(sW + s * kWStage);
+                for (int bi = 0; bi < nb; ++bi)
+                    tc::bulk_load(wdst + (uint32_t)(bi * kTileBytes),
+                                  p.w + ((size_t)(band0 + bi) * p.G + g_lo + it) * kTileBytes, kTileBytes,
+                                  w_full + 8 * s);
                 ++issued;
             }
-            // drain: the last load of every stage has landed before the CTA exits
-            for (int it = issued - 1; it >= 0 && it >= issued - kStages; --it)
+            // drain: the last loads of every stage have landed before the CTA exits
+            for (int it = issued - 1; it >= 0 && it >= issued - kStages; --it) {
                 if (!tc::mbar_wait(x_full + 8 * (it % kStages), (it / kStages) & 1)) atomicOr(p.status, 2);
+                if (!tc::mbar_wait(w_full + 8 * (it % kStages), (it / kStages) & 1)) atomicOr(p.status, 2);
+            }
         }
     } else if (warp == 1) {
         // ---- MMA issuer -------------------------------------------------------
@@ -152,29 +166,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         // ---- dequant: 2 bands per warp ----------------------------------------
         const int dw = warp - 4;
         const int r = lane >> 2, c = lane & 3;
-        uint4 lo[2], hi[2], nlo[2], nhi[2];
-        auto load = [&](int it, uint4 (&L)[2], uint4 (&H)[2]) {
-#pragma unroll
-            for (int bi = 0; bi < 2; ++bi) {
-                const int bg = band0 + 2 * dw + bi;
-                if (bg < p.bands) {
-                    const uint8_t* t = p.w + ((size_t)bg * p.G + g_lo + it) * kTileBytes;
-                    L[bi] = ld_stream16(t + 16 * lane);
-                    H[bi] = ld_stream16(t + 512 + 16 * lane);
-                } else {
-                    L[bi] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);  // q = 0
-                    H[bi] = L[bi];
-                }
-            }
-        };
-        if (ng > 0) load(0, lo, hi);
+        uint4 lo[2], hi[2];
         for (int it = 0; it < ng; ++it) {
             const int s = it % kStages;
             const uint32_t ph = (it / kStages) & 1;
-            if (it + 1 < ng) load(it + 1, nlo, nhi);
-            if (!tc::mbar_wait(empty + 8 * s, ph ^ 1)) {
+            // the packed tiles have landed (and, as the producer waited for the
+            // stage to be free before loading them, the A slot is free too)
+            if (!tc::mbar_wait(w_full + 8 * s, ph)) {
                 atomicOr(p.status, 16);
                 break;
+            }
+#pragma unroll
+            for (int bi = 0; bi < 2; ++bi) {
+                if (band0 + 2 * dw + bi < p.bands) {
+                    const uint32_t t = tc::smem_addr(sW + s * kWStage + (2 * dw + bi) * kTileBytes);
+                    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(lo[bi].x), "=r"(lo[bi].y), "=r"(lo[bi].z), "=r"(lo[bi].w)
+                                 : "r"(t + 16 * lane));
+                    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(hi[bi].x), "=r"(hi[bi].y), "=r"(hi[bi].z), "=r"(hi[bi].w)
+                                 : "r"(t + 512 + 16 * lane));
+                } else {
+                    lo[bi] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);  // q = 0
+                    hi[bi] = lo[bi];
+                }
             }
             const uint32_t a0 = tc::smem_addr(sA + s * kAStage);
 #pragma unroll
@@ -196,11 +211,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             tc::fence_async_shared();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(a_full + 8 * s);
-#pragma unroll
-            for (int bi = 0; bi < 2; ++bi) {
-                lo[bi] = nlo[bi];
-                hi[bi] = nhi[bi];
-            }
         }
     } else if (warp >= 8) {
         // ---- promote + epilogue -------------------------------------------------
@@ -217,12 +227,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(sc + (size_t)(g_lo + it) * kTileBytes));
             return __half2float(__ushort_as_half(h));
         };
+        // scales two groups ahead of the accumulator they multiply
         float s_cur = ng > 0 ? scale_of(0) : 0.f;
+        float s_nxt = ng > 1 ? scale_of(1) : 0.f;
         bool ok = true;
         for (int it = 0; it < ng; ++it) {
             const int b = it & 1;
             const uint32_t bph = (it >> 1) & 1;
-            const float s_next = (it + 1 < ng) ? scale_of(it + 1) : 0.f;
+            const float s_far = (it + 2 < ng) ? scale_of(it + 2) : 0.f;
             if (!tc::mbar_wait(d_full + 8 * b, bph)) {
                 atomicOr(p.status, 32);
                 ok = false;
@@ -242,7 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(d_empty + 8 * b);
-            s_cur = s_next;
+            s_cur = s_nxt;
+            s_nxt = s_far;
         }
         const int n = band0 * 16 + row;
         if (ok && row_ok && n < p.N) {

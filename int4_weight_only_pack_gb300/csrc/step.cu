@@ -217,56 +217,71 @@ __device__ __forceinline__ void for_frag(const float (&acc)[(MP + 7) / 8][4], in
 // is held by exactly one lane of the warp).  S == 1: write y.  S > 1: publish
 // this split's partial; the arrival that completes the band adds the S
 // partials in split order and writes y.
+// The final FP32 sums of band `band` of a K-split projection: publish this
+// split's partial; the arrival that completes the band adds the S partials
+// in split order (eight loads in flight) and hands each sum to emit(row, m,
+// sum).  False for every other arrival.
+template <typename V, typename E>
+__device__ __forceinline__ bool combine_splits(const StepOp& o, int band, int r, int M, int lane, V&& visit,
+                                               E&& emit) {
+    const int pb = 16 * M;
+    float* mine = o.part + ((size_t)band * o.S + r) * pb;
+    visit([&](int row, int m, float v) { mine[row * M + m] = v; });
+    // the warp's stores are ordered before lane 0's fence by the warp barrier
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0) {
+        __threadfence();
+        last = atomicAdd(o.cnt + band, 1u) == (unsigned)(o.S - 1);
+        if (last) __threadfence();
+    }
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    if (!last) return false;
+    const float* base = o.part + (size_t)band * o.S * pb;
+    visit([&](int row, int m, float) {
+        const float* pp = base + row * M + m;
+        float sum = 0.f;
+        int s = 0;
+        for (; s + 8 <= o.S; s += 8) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = __ldcg(pp + (size_t)(s + e) * pb);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sum += v[e];
+        }
+        for (; s < o.S; ++s) sum += __ldcg(pp + (size_t)s * pb);
+        emit(row, m, sum);
+    });
+    if (lane == 0) o.cnt[band] = 0;  // ready for the next replay
+    return true;
+}
+
+// Finish band `band` of projection o from per-lane outputs (visit(f) calls
+// f(row, m, value) for each output this lane holds; every output of the band
+// is held by exactly one lane of the warp).  Plain projection: the sums go to
+// y.  Gated projection (W4_OP_SWIGLU): rows r and r + 8 of the band are gate
+// and up row 8*band + r; the sums go to this warp's scratch and y (I = N/2
+// columns) gets silu(gate) * up.
 template <int ACT, typename V>
 __device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, int M, int lane, V&& visit,
                                             float* scratch, int MP) {
     using Ops = dec::ActOps<ACT>;
     const int n0 = band * 16;
-    const bool glu = (o.flags & W4_OP_SWIGLU) != 0;
-    // the band's final FP32 sums go to y, or (gated) to this warp's scratch
-    auto emit = [&](int row, int m, float v) {
-        if (glu)
-            scratch[row * MP + m] = v;
-        else if (n0 + row < o.N)
-            o.y[(size_t)m * o.N + n0 + row] = Ops::round(v);
-    };
-    if (o.S == 1) {
-        visit(emit);
-    } else {
-        const int pb = 16 * M;
-        float* mine = o.part + ((size_t)band * o.S + r) * pb;
-        visit([&](int row, int m, float v) { mine[row * M + m] = v; });
-        // the warp's stores are ordered before lane 0's fence by the warp barrier
-        __syncwarp();
-        unsigned last = 0;
-        if (lane == 0) {
-            __threadfence();
-            last = atomicAdd(o.cnt + band, 1u) == (unsigned)(o.S - 1);
-            if (last) __threadfence();
-        }
-        last = __shfl_sync(0xFFFFFFFFu, last, 0);
-        if (!last) return;
-        const float* base = o.part + (size_t)band * o.S * pb;
-        visit([&](int row, int m, float) {
-            // eight partials in flight at a time, added in split order
-            const float* pp = base + row * M + m;
-            float sum = 0.f;
-            int s = 0;
-            for (; s + 8 <= o.S; s += 8) {
-                float v[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = __ldcg(pp + (size_t)(s + e) * pb);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) sum += v[e];
-            }
-            for (; s < o.S; ++s) sum += __ldcg(pp + (size_t)s * pb);
-            emit(row, m, sum);
-        });
-        if (lane == 0) o.cnt[band] = 0;  // ready for the next replay
+    if (!(o.flags & W4_OP_SWIGLU)) {
+        auto to_y = [&](int row, int m, float v) {
+            if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = Ops::round(v);
+        };
+        if (o.S == 1)
+            visit(to_y);
+        else
+            combine_splits(o, band, r, M, lane, visit, to_y);
+        return;
     }
-    if (!glu) return;
-    // gated projection: rows r and r + 8 of the band are gate and up row
-    // 8*band + r; y (I = N/2 columns) gets silu(gate) * up
+    auto to_scratch = [&](int row, int m, float v) { scratch[row * MP + m] = v; };
+    if (o.S == 1)
+        visit(to_scratch);
+    else if (!combine_splits(o, band, r, M, lane, visit, to_scratch))
+        return;
     __syncwarp();
     const int I = o.N / 2;
     for (int oi = lane; oi < 8 * M; oi += 32) {
