@@ -14,11 +14,14 @@
 //   warp 0     TMA producer: x tile [128 tokens][128 K] as two 128-byte
 //              swizzled boxes (zero fill past M), and the group's 8 packed
 //              weight tiles (bulk copies) into the same pipeline stage
-//   warp 1     one thread issues 8 tcgen05.mma (128x128x16) per group into a
-//              TMEM buffer (two buffers alternate), then commits
+//   warp 1     one thread issues 8 tcgen05.mma (128x128x16) per group, A
+//              from tensor memory and B (x) from shared memory, into a TMEM
+//              accumulator (two alternate), then commits
 //   warps 4-7  dequant: read the group's packed tiles from the stage, unpack
-//              nibbles to exact fp16 q, write them K-major with the 128-byte
-//              swizzle
+//              nibbles to exact fp16 q and store them straight into the
+//              stage's A columns of tensor memory (one 16-lane x 256-bit
+//              store per band and K step: the packed tile's lane layout is
+//              that store's register layout)
 //   warps 8-15 promote: read the group's FP32 partial from TMEM, multiply by
 //              the group scale and add to FP32 accumulators in registers;
 //              finally write y (or an FP32 split-K partial)
@@ -44,13 +47,16 @@ namespace {
 
 constexpr int kBM = 128;                   // weight rows per CTA (8 bands)
 constexpr int kBN = 128;                   // tokens per CTA
-constexpr int kStages = 3;                 // one 128-wide K group per stage
-constexpr int kAStage = kBM * 128 * 2;     // 32 KB of fp16 q
+constexpr int kStages = 4;                 // one 128-wide K group per stage
 constexpr int kBStage = kBN * 128 * 2;     // 32 KB of fp16 x
 constexpr int kWStage = 8 * kTileBytes;    // the group's 8 packed tiles (one per band)
 constexpr int kThreads = 512;
-constexpr int kTmemCols = 256;             // two 128-column FP32 accumulators
-constexpr int kSmemBytes = kStages * (kAStage + kBStage + kWStage) + 1024 + 256;
+// Tensor memory: two 128-column FP32 accumulators, then one 64-column block
+// of fp16 q pairs (128 rows x 128 K) per stage.
+constexpr int kACol0 = 256;
+constexpr int kTmemCols = 512;
+static_assert(kACol0 + 64 * kStages <= kTmemCols, "tensor memory columns");
+constexpr int kSmemBytes = kStages * (kBStage + kWStage) + 1024 + 256;
 constexpr size_t kStatusBytes = 256;       // workspace head: status word (+ padding)
 
 struct GemmParams {
@@ -64,8 +70,7 @@ struct GemmParams {
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + kStages * kAStage;
+    uint8_t* sB = smem;
     uint8_t* sW = sB + kStages * kBStage;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sW + kStages * kWStage);
     // barrier slots
@@ -147,12 +152,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     break;
                 }
                 tc::fence_after_sync();
-                const uint32_t a0 = tc::smem_addr(sA + s * kAStage), b0 = tc::smem_addr(sB + s * kBStage);
+                const uint32_t a0 = tmem + kACol0 + 64 * s, b0 = tc::smem_addr(sB + s * kBStage);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const uint32_t off = (j >> 2) * (kAStage / 2) + (j & 3) * 32;
-                    tc::mma_f16(tmem + b * 128, tc::sw128_kmajor_desc(a0 + off), tc::sw128_kmajor_desc(b0 + off), idesc,
-                                j > 0);
+                    const uint32_t off = (j >> 2) * (kBStage / 2) + (j & 3) * 32;
+                    tc::mma_f16_ta(tmem + b * 128, a0 + 8 * j, tc::sw128_kmajor_desc(b0 + off), idesc, j > 0);
                 }
                 tc::mma_commit(empty + 8 * s);
                 tc::mma_commit(d_full + 8 * b);
@@ -163,52 +167,51 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 atomicOr(p.status, 8);
         }
     } else if (warp >= 4 && warp < 8) {
-        // ---- dequant: 2 bands per warp ----------------------------------------
+        // ---- dequant: 2 bands per warp, TMEM lanes 32*dw .. 32*dw + 31 -------
         const int dw = warp - 4;
-        const int r = lane >> 2, c = lane & 3;
-        uint4 lo[2], hi[2];
         for (int it = 0; it < ng; ++it) {
             const int s = it % kStages;
             const uint32_t ph = (it / kStages) & 1;
-            // the packed tiles have landed (and, as the producer waited for the
-            // stage to be free before loading them, the A slot is free too)
+            // the packed tiles have landed; the producer waited for the stage
+            // to be free before loading them, so the MMAs that read this
+            // stage's A columns have completed too
             if (!tc::mbar_wait(w_full + 8 * s, ph)) {
                 atomicOr(p.status, 16);
                 break;
             }
+            tc::fence_after_sync();
 #pragma unroll
             for (int bi = 0; bi < 2; ++bi) {
+                uint4 lo, hi;
                 if (band0 + 2 * dw + bi < p.bands) {
                     const uint32_t t = tc::smem_addr(sW + s * kWStage + (2 * dw + bi) * kTileBytes);
                     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                                 : "=r"(lo[bi].x), "=r"(lo[bi].y), "=r"(lo[bi].z), "=r"(lo[bi].w)
+                                 : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w)
                                  : "r"(t + 16 * lane));
                     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                                 : "=r"(hi[bi].x), "=r"(hi[bi].y), "=r"(hi[bi].z), "=r"(hi[bi].w)
+                                 : "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
                                  : "r"(t + 512 + 16 * lane));
                 } else {
-                    lo[bi] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);  // q = 0
-                    hi[bi] = lo[bi];
+                    lo = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);  // q = 0
+                    hi = lo;
                 }
-            }
-            const uint32_t a0 = tc::smem_addr(sA + s * kAStage);
-#pragma unroll
-            for (int bi = 0; bi < 2; ++bi) {
-                const uint32_t wd[8] = {lo[bi].x, lo[bi].y, lo[bi].z, lo[bi].w, hi[bi].x, hi[bi].y, hi[bi].z, hi[bi].w};
-                const int row0 = 16 * (2 * dw + bi) + r;  // row1 = row0 + 8 shares row0's swizzle phase
+                const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                // K step j -> columns 8j .. 8j+7: lane (r, c) holds rows r and
+                // r + 8, k pairs 2c and 2c + 1 of the step
+                uint32_t a[32];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    uint32_t a[4];
-                    unpack_word(wd[j], a);
-                    const uint32_t chunk = 2 * (j & 3) + (c >> 1);
-                    const uint32_t addr = a0 + (j >> 2) * (kAStage / 2) + row0 * 128 + ((chunk ^ (uint32_t)r) << 4) +
-                                          (c & 1) * 8;
-                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a[0]), "r"(a[2]) : "memory");
-                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr + 1024), "r"(a[1]), "r"(a[3])
-                                 : "memory");
+                    uint32_t q4[4];
+                    unpack_word(wd[j], q4);
+                    a[4 * j + 0] = q4[0];
+                    a[4 * j + 1] = q4[2];
+                    a[4 * j + 2] = q4[1];
+                    a[4 * j + 3] = q4[3];
                 }
+                tc::tmem_st_16x256_x8(tmem + ((uint32_t)(32 * dw + 16 * bi) << 16) + kACol0 + 64 * s, a);
             }
-            tc::fence_async_shared();
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(a_full + 8 * s);
         }
