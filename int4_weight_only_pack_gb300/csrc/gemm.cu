@@ -9,22 +9,29 @@
 // its FP32 scale and added in FP32 registers.  The scale is never folded into
 // an FP16 weight, so the weights reach the tensor core exactly.
 //
-// One CTA computes a 128 (weight rows) x 128 (tokens) tile over a K range,
-// one 128-wide group per pipeline stage, with warp-specialised roles:
-//   warp 0     TMA producer: x tile [128 tokens][128 K] as two 128-byte
+// One CTA computes a 128 (weight rows) x 192 (tokens) tile over a K range,
+// one 128-wide group per pipeline step, with warp-specialised roles:
+//   warp 0     TMA producer: x tile [192 tokens][128 K] as two 128-byte
 //              swizzled boxes (zero fill past M), and the group's 8 packed
-//              weight tiles (bulk copies) into the same pipeline stage
-//   warp 1     one thread issues 8 tcgen05.mma (128x128x16) per group, A
-//              from tensor memory and B (x) from shared memory, into a TMEM
-//              accumulator (two alternate), then commits
+//              weight tiles (bulk copies) into the same shared-memory stage
+//   warp 1     one thread issues 8 tcgen05.mma (128x192x16) per group, A
+//              from tensor memory and B (x) from shared memory, into one of
+//              two TMEM accumulators, then commits
 //   warps 4-7  dequant: read the group's packed tiles from the stage, unpack
-//              nibbles to exact fp16 q and store them straight into the
-//              stage's A columns of tensor memory (one 16-lane x 256-bit
-//              store per band and K step: the packed tile's lane layout is
-//              that store's register layout)
-//   warps 8-15 promote: read the group's FP32 partial from TMEM, multiply by
-//              the group scale and add to FP32 accumulators in registers;
-//              finally write y (or an FP32 split-K partial)
+//              nibbles to exact fp16 q and store them straight into one of
+//              two A slots of tensor memory (16-lane x 256-bit stores: the
+//              packed tile's lane layout is that store's register layout)
+//   warps 8-15 promote: read a group's FP32 partial from TMEM, hand the
+//              accumulator back, multiply by the group scale and add to
+//              FP32 accumulators in registers (96 per thread: these two
+//              warpgroups take registers from the other two); finally write
+//              y (or an FP32 split-K partial)
+// Tile width: a 128xNx16 MMA takes about as long for N = 128 as for N = 256
+// on this tensor core, so narrow tiles waste it; but two 256-column
+// accumulators fill tensor memory and leave no room for A, and with one
+// accumulator the MMAs wait for every group's partial to be read out.  192
+// tokens leave room for two accumulators and two A slots (192 + 192 + 2 x 64
+// = 512 columns).
 // Every mbarrier wait is bounded; a timeout sets the status word in the
 // workspace and the CTA drains and exits instead of hanging.
 #include <cuda.h>
@@ -46,16 +53,23 @@ w4_status check_gemv_args(const void* x, const w4_weight* w, const void* y, int 
 namespace {
 
 constexpr int kBM = 128;                   // weight rows per CTA (8 bands)
-constexpr int kBN = 128;                   // tokens per CTA
-constexpr int kStages = 4;                 // one 128-wide K group per stage
-constexpr int kBStage = kBN * 128 * 2;     // 32 KB of fp16 x
+constexpr int kBN = 192;                   // tokens per CTA
+constexpr int kStages = 4;                 // shared-memory stages (one group each)
+constexpr int kASlots = 2;                 // A slots in tensor memory
+constexpr int kBStage = kBN * 128 * 2;     // 48 KB of fp16 x
 constexpr int kWStage = 8 * kTileBytes;    // the group's 8 packed tiles (one per band)
 constexpr int kThreads = 512;
-// Tensor memory: two 128-column FP32 accumulators, then one 64-column block
-// of fp16 q pairs (128 rows x 128 K) per stage.
-constexpr int kACol0 = 256;
+// Tensor memory: two kBN-column FP32 accumulators, then one 64-column block
+// of fp16 q pairs (128 rows x 128 K) per A slot.
+constexpr int kACol0 = 2 * kBN;
 constexpr int kTmemCols = 512;
-static_assert(kACol0 + 64 * kStages <= kTmemCols, "tensor memory columns");
+static_assert(kACol0 + 64 * kASlots <= kTmemCols, "tensor memory columns");
+static_assert(kBN % 32 == 0 && kBN % 16 == 0 && kBN <= 256, "MMA N and promote column blocks");
+// Registers per thread after the split: warpgroups 0-1 (producer, issuer,
+// dequant) give up registers to warpgroups 2-3 (promote).  The four shares
+// add up to the 128 x 512 the CTA is launched with.
+constexpr int kRegsLow = 112, kRegsHigh = 144;
+static_assert(2 * kRegsLow + 2 * kRegsHigh == 4 * 128, "register split");
 constexpr int kSmemBytes = kStages * (kBStage + kWStage) + 1024 + 256;
 constexpr size_t kStatusBytes = 256;       // workspace head: status word (+ padding)
 
@@ -74,8 +88,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     uint8_t* sW = sB + kStages * kBStage;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sW + kStages * kWStage);
     // barrier slots
-    const uint32_t x_full = tc::smem_addr(bars), a_full = x_full + 8 * kStages, empty = a_full + 8 * kStages,
-                   d_full = empty + 8 * kStages, d_empty = d_full + 16, w_full = d_empty + 16;
+    const uint32_t x_full = tc::smem_addr(bars), w_full = x_full + 8 * kStages, empty = w_full + 8 * kStages,
+                   a_full = empty + 8 * kStages, a_empty = a_full + 8 * kASlots, d_full = a_empty + 8 * kASlots,
+                   d_empty = d_full + 16;
     __shared__ uint32_t tmem_base_sh;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -89,9 +104,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             tc::mbar_init(x_full + 8 * s, 1);
-            tc::mbar_init(a_full + 8 * s, 4);
-            tc::mbar_init(empty + 8 * s, 1);
             tc::mbar_init(w_full + 8 * s, 1);
+            tc::mbar_init(empty + 8 * s, 1);
+        }
+        for (int a = 0; a < kASlots; ++a) {
+            tc::mbar_init(a_full + 8 * a, 4);
+            tc::mbar_init(a_empty + 8 * a, 1);
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(d_full + 8 * b, 1);
@@ -106,9 +124,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base_sh;
 
+    // Each role runs under its warpgroup's register limit: the limit is set
+    // in the same branch as the role's code.
+    if (warp < 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0) {
         // ---- TMA producer ---------------------------------------------------
         if (lane == 0) {
+            const int nb = min(8, p.bands - band0);
             int issued = 0;
             for (int it = 0; it < ng; ++it) {
                 const int s = it % kStages;
@@ -123,7 +146,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 tc::tma_load_2d(dst, &xmap, k0, tok0, x_full + 8 * s);
                 tc::tma_load_2d(dst + kBStage / 2, &xmap, k0 + 64, tok0, x_full + 8 * s);
                 // the group's packed tiles, one per band of this CTA
-                const int nb = min(8, p.bands - band0);
                 tc::mbar_arrive_expect_tx(w_full + 8 * s, (uint32_t)(nb * kTileBytes));
                 const uint32_t wdst = tc::smem_addr(sW + s * kWStage);
                 for (int bi = 0; bi < nb; ++bi)
@@ -144,21 +166,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             constexpr uint32_t idesc = tc::idesc_f16_f32(kBM, kBN);
             int done = 0;
             for (int it = 0; it < ng; ++it) {
-                const int s = it % kStages, b = it & 1;
-                const uint32_t ph = (it / kStages) & 1, bph = (it >> 1) & 1;
-                if (!tc::mbar_wait(x_full + 8 * s, ph) || !tc::mbar_wait(a_full + 8 * s, ph) ||
-                    !tc::mbar_wait(d_empty + 8 * b, bph ^ 1)) {
+                const int s = it % kStages, a = it % kASlots, b = it & 1;
+                const uint32_t ph = (it / kStages) & 1, aph = (it / kASlots) & 1;
+                // accumulator b was read out (two groups back) by the promote warps
+                if (!tc::mbar_wait(x_full + 8 * s, ph) || !tc::mbar_wait(a_full + 8 * a, aph) ||
+                    !tc::mbar_wait(d_empty + 8 * b, ((it >> 1) & 1) ^ 1)) {
                     atomicOr(p.status, 4);
                     break;
                 }
                 tc::fence_after_sync();
-                const uint32_t a0 = tmem + kACol0 + 64 * s, b0 = tc::smem_addr(sB + s * kBStage);
+                const uint32_t a0 = tmem + kACol0 + 64 * a, b0 = tc::smem_addr(sB + s * kBStage);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t off = (j >> 2) * (kBStage / 2) + (j & 3) * 32;
-                    tc::mma_f16_ta(tmem + b * 128, a0 + 8 * j, tc::sw128_kmajor_desc(b0 + off), idesc, j > 0);
+                    tc::mma_f16_ta(tmem + b * kBN, a0 + 8 * j, tc::sw128_kmajor_desc(b0 + off), idesc, j > 0);
                 }
                 tc::mma_commit(empty + 8 * s);
+                tc::mma_commit(a_empty + 8 * a);
                 tc::mma_commit(d_full + 8 * b);
                 done = it + 1;
             }
@@ -166,16 +190,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             if (done > 0 && !tc::mbar_wait(d_full + 8 * ((done - 1) & 1), ((done - 1) >> 1) & 1))
                 atomicOr(p.status, 8);
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4) {
         // ---- dequant: 2 bands per warp, TMEM lanes 32*dw .. 32*dw + 31 -------
         const int dw = warp - 4;
         for (int it = 0; it < ng; ++it) {
-            const int s = it % kStages;
-            const uint32_t ph = (it / kStages) & 1;
-            // the packed tiles have landed; the producer waited for the stage
-            // to be free before loading them, so the MMAs that read this
-            // stage's A columns have completed too
-            if (!tc::mbar_wait(w_full + 8 * s, ph)) {
+            const int s = it % kStages, a = it % kASlots;
+            const uint32_t ph = (it / kStages) & 1, aph = (it / kASlots) & 1;
+            // the packed tiles have landed, and the MMAs that read this A slot
+            // (kASlots groups back) have completed
+            if (!tc::mbar_wait(w_full + 8 * s, ph) || !tc::mbar_wait(a_empty + 8 * a, aph ^ 1)) {
                 atomicOr(p.status, 16);
                 break;
             }
@@ -195,36 +218,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     lo = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);  // q = 0
                     hi = lo;
                 }
-                const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
                 // K step j -> columns 8j .. 8j+7: lane (r, c) holds rows r and
-                // r + 8, k pairs 2c and 2c + 1 of the step
-                uint32_t a[32];
+                // r + 8, k pairs 2c and 2c + 1 of the step; two stores of four
+                // steps (k 0..63 from lo, 64..127 from hi)
+                const uint32_t taddr = tmem + ((uint32_t)(32 * dw + 16 * bi) << 16) + kACol0 + 64 * a;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t q4[4];
-                    unpack_word(wd[j], q4);
-                    a[4 * j + 0] = q4[0];
-                    a[4 * j + 1] = q4[2];
-                    a[4 * j + 2] = q4[1];
-                    a[4 * j + 3] = q4[3];
+                for (int h = 0; h < 2; ++h) {
+                    const uint4 wv = h ? hi : lo;
+                    const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+                    uint32_t q16[16];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t q4[4];
+                        unpack_word(wd[j], q4);
+                        q16[4 * j + 0] = q4[0];
+                        q16[4 * j + 1] = q4[2];
+                        q16[4 * j + 2] = q4[1];
+                        q16[4 * j + 3] = q4[3];
+                    }
+                    tc::tmem_st_16x256_x4(taddr + 32 * h, q16);
                 }
-                tc::tmem_st_16x256_x8(tmem + ((uint32_t)(32 * dw + 16 * bi) << 16) + kACol0 + 64 * s, a);
             }
             tc::tmem_wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(a_full + 8 * s);
+            if (lane == 0) tc::mbar_arrive(a_full + 8 * a);
         }
-    } else if (warp >= 8) {
+    }
+    } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+    {
         // ---- promote + epilogue -------------------------------------------------
         const int quarter = warp & 3, half = (warp - 8) >> 2;
         const int row = 32 * quarter + lane;  // TMEM lane = weight row within the tile
         const int bandg = band0 + (row >> 4), rr = row & 15;
         const bool row_ok = bandg < p.bands;
         const uint8_t* sc = p.w + (size_t)bandg * p.G * kTileBytes + kScaleOffset + 4 * (rr & 7) + 2 * (rr >> 3);
-        float acc[64];
+        constexpr int kCols = kBN / 2;  // tokens of this thread: the warp's half of the tile
+        float acc[kCols];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+        for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
         auto scale_of = [&](int it) -> float {
             if (!row_ok) return 0.f;
             const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(sc + (size_t)(g_lo + it) * kTileBytes));
@@ -236,44 +269,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         bool ok = true;
         for (int it = 0; it < ng; ++it) {
             const int b = it & 1;
-            const uint32_t bph = (it >> 1) & 1;
             const float s_far = (it + 2 < ng) ? scale_of(it + 2) : 0.f;
-            if (!tc::mbar_wait(d_full + 8 * b, bph)) {
+            if (!tc::mbar_wait(d_full + 8 * b, (it >> 1) & 1)) {
                 atomicOr(p.status, 32);
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-            const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + b * 128 + 64 * half;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + b * kBN + kCols * half;
             uint32_t v[32];
-            tc::tmem_ld_32x32(taddr, v);
-            tc::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = fmaf(s_cur, __uint_as_float(v[i]), acc[i]);
-            tc::tmem_ld_32x32(taddr + 32, v);
-            tc::tmem_wait_ld();
+            for (int c = 0; c < kCols / 32; ++c) {
+                tc::tmem_ld_32x32(taddr + 32 * c, v);
+                tc::tmem_wait_ld();
+                if (c == kCols / 32 - 1) {
+                    // the whole partial is in registers: hand the accumulator back
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(d_empty + 8 * b);
+                }
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(s_cur, __uint_as_float(v[i]), acc[32 + i]);
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(d_empty + 8 * b);
+                for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(s_cur, __uint_as_float(v[i]), acc[32 * c + i]);
+            }
             s_cur = s_nxt;
             s_nxt = s_far;
         }
         const int n = band0 * 16 + row;
         if (ok && row_ok && n < p.N) {
-            const int t0 = tok0 + 64 * half;
+            const int t0 = tok0 + kCols * half;
             if (p.part == nullptr) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
+                for (int i = 0; i < kCols; ++i)
                     if (t0 + i < p.M) p.y[(size_t)(t0 + i) * p.N + n] = __half_as_ushort(__float2half_rn(acc[i]));
             } else {
                 float* dst = p.part + (size_t)split * p.M * p.N;
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
+                for (int i = 0; i < kCols; ++i)
                     if (t0 + i < p.M) dst[(size_t)(t0 + i) * p.N + n] = acc[i];
             }
         }
+    }
     }
 
     tc::fence_before_sync();
@@ -308,15 +343,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+// K splits of one call.  Cost, in units of one group's MMAs on one SM (about
+// 0.65 us): waves of CTAs (152 SMs) x groups per CTA, plus, for s > 1, the
+// FP32 partials written and read back by the reduce (8 bytes per output and
+// split, about 4.4 MB of HBM traffic per unit).  Each split keeps >= 4 groups.
 int gemm_splits(int M, int64_t N, int64_t K) {
     const int64_t tiles = ((N + kBM - 1) / kBM) * ((M + kBN - 1) / kBN);
     const int G = (int)(K / kGroupK);
-    if (tiles >= 120 || G < 64) return 1;
-    // smallest waves-per-split among 1..8 splits with >= 16 groups each
     int best = 1;
-    double best_t = 1e30;
-    for (int s = 1; s <= 8 && G / s >= 16; ++s) {
-        const double t = (double)((tiles * s + 151) / 152) / s + 0.02 * (s > 1);
+    double best_t = 1e300;
+    for (int s = 1; s <= 16 && (G + s - 1) / s >= 4; ++s) {
+        const double waves = (double)((tiles * s + 151) / 152);
+        const double t = waves * ((G + s - 1) / s) + (s > 1 ? (double)s * M * (double)N * 8.0 / 4.4e6 : 0.0);
         if (t < best_t - 1e-9) {
             best_t = t;
             best = s;
