@@ -239,9 +239,11 @@ def cpu_baseline(oracle, synth, budget_s: float = 12.0):
 
 
 def run_one_projection(args):
-    """One projection of layer 0 at M = 1, launched --warmup + --steps times
-    back to back (a profiler target; weights larger than L2 only for gate_up
-    and down, so the printed rate of the others is L2-assisted)."""
+    """One projection of layer 0 at M = --profile-m tokens (1 by default),
+    launched --warmup + --steps times back to back: a profiler target.  M <= 16
+    runs the decode kernel (weights larger than L2 only for gate_up and down,
+    so the printed rate of the others is L2-assisted); larger M runs the
+    prefill GEMM with its workspace."""
     import torch
     import int4_weight_only_pack_gb300 as w4
     from int4_weight_only_pack_gb300 import build as w4build
@@ -258,14 +260,28 @@ def run_one_projection(args):
     packed = torch.empty(w4.w4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
     w = w4.w4_pack(q, s, N, K, packed)
     del q, s
-    x = torch.from_numpy(synth.x_full(synth.seed_of(CONFIG_ID, 0, pid, synth.T_X), 1, K).view(np.int16)).cuda()
-    y = torch.zeros((1, N), dtype=torch.int16, device="cuda")
+    M = max(1, args.profile_m)
+    x = torch.from_numpy(synth.x_full(synth.seed_of(CONFIG_ID, 0, pid, synth.T_X), M, K).view(np.int16)).cuda()
+    y = torch.zeros((M, N), dtype=torch.int16, device="cuda")
+    if M <= 16:
+        def run():
+            w4.w4a16_gemv(x, w, y, M)
+    else:
+        nbw = w4.w4_workspace_bytes(M, N, K)
+        wsb = torch.zeros(max(nbw, 256), dtype=torch.uint8, device="cuda")
+
+        def run():
+            w4.w4a16_gemm(x, w, y, M, wsb, nbw)
     for _ in range(args.warmup):
-        w4.w4a16_gemv(x, w, y, 1)
-    ms = time_replays(torch, lambda: w4.w4a16_gemv(x, w, y, 1), args.steps)
+        run()
+    ms = time_replays(torch, run, args.steps)
     nb = w4.w4_packed_bytes(N, K)
-    print(json.dumps({"projection": args.profile_projection, "N": N, "K": K, "launches": args.steps,
-                      "us_per_launch": ms * 1e3, "GB/s": nb / (ms * 1e-3) / 1e9}), flush=True)
+    line = {"projection": args.profile_projection, "M": M, "N": N, "K": K, "launches": args.steps,
+            "us_per_launch": ms * 1e3, "GB/s": nb / (ms * 1e-3) / 1e9}
+    if M > 16:
+        line["TFLOP/s"] = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        line["status_word"] = int(wsb[:4].view(torch.int32).item())
+    print(json.dumps(line), flush=True)
     return 0
 
 
@@ -454,8 +470,10 @@ def main():
                     help="with --no-extras: a step of the first L layers only (a small case for a profiler; "
                          "prints a profiler line, not the benchmark line)")
     ap.add_argument("--profile-projection", choices=[n for n, _, _ in LAYER], default=None,
-                    help="launch one projection of layer 0 (M=1, library launch shape) --steps times: a small "
+                    help="launch one projection of layer 0 (library launch shape) --steps times: a small "
                          "case for a profiler")
+    ap.add_argument("--profile-m", type=int, default=1,
+                    help="with --profile-projection: tokens (M > 16 runs the prefill GEMM)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
