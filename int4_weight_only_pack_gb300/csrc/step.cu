@@ -218,10 +218,17 @@ __device__ __forceinline__ void for_frag(const float (&acc)[(MP + 7) / 8][4], in
 // this split's partial; the arrival that completes the band adds the S
 // partials in split order and writes y.
 // The final FP32 sums of band `band` of a K-split projection: publish this
-// split's partial; the arrival that completes the band adds the S partials
-// in split order (eight loads in flight) and hands each sum to emit(row, m,
-// sum).  False for every other arrival.
-template <typename V, typename E>
+// split's partial; the arrival that completes the band adds the S partials in
+// split order and hands each sum to emit(row, m, sum).  False for every other
+// arrival.  For 8 or more (padded) tokens the adding warp walks the band's
+// outputs in lane-strided batches of kCombineOut and issues every load of a
+// batch (kCombineOut outputs x up to 8 splits) before adding any: one output
+// and one split at a time, each load is a dependent L2 round trip, which at
+// 16 tokens (8 outputs per lane) made this the longest stretch of a
+// projection.  For fewer tokens (at most one output per lane) the plain loop
+// below measured faster.
+constexpr int kCombineOut = 4;
+template <int MP, typename V, typename E>
 __device__ __forceinline__ bool combine_splits(const StepOp& o, int band, int r, int M, int lane, V&& visit,
                                                E&& emit) {
     const int pb = 16 * M;
@@ -238,20 +245,49 @@ __device__ __forceinline__ bool combine_splits(const StepOp& o, int band, int r,
     last = __shfl_sync(0xFFFFFFFFu, last, 0);
     if (!last) return false;
     const float* base = o.part + (size_t)band * o.S * pb;
-    visit([&](int row, int m, float) {
-        const float* pp = base + row * M + m;
-        float sum = 0.f;
-        int s = 0;
-        for (; s + 8 <= o.S; s += 8) {
-            float v[8];
+    if constexpr (MP < 8) {
+        visit([&](int row, int m, float) {
+            const float* pp = base + row * M + m;
+            float sum = 0.f;
+            int s = 0;
+            for (; s + 8 <= o.S; s += 8) {
+                float v[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = __ldcg(pp + (size_t)(s + e) * pb);
+                for (int e = 0; e < 8; ++e) v[e] = __ldcg(pp + (size_t)(s + e) * pb);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) sum += v[e];
+                for (int e = 0; e < 8; ++e) sum += v[e];
+            }
+            for (; s < o.S; ++s) sum += __ldcg(pp + (size_t)s * pb);
+            emit(row, m, sum);
+        });
+        if (lane == 0) o.cnt[band] = 0;  // ready for the next replay
+        return true;
+    }
+    for (int o0 = 0; o0 < pb; o0 += 32 * kCombineOut) {
+        float sum[kCombineOut];
+#pragma unroll
+        for (int j = 0; j < kCombineOut; ++j) sum[j] = 0.f;
+        for (int s = 0; s < o.S; s += 8) {
+            float v[kCombineOut][8];
+#pragma unroll
+            for (int j = 0; j < kCombineOut; ++j) {
+                const int idx = o0 + 32 * j + lane;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    v[j][e] = (idx < pb && s + e < o.S) ? __ldcg(base + (size_t)(s + e) * pb + idx) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < kCombineOut; ++j)
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (s + e < o.S) sum[j] += v[j][e];  // only real splits: 0 + -0 would flip a zero's sign
         }
-        for (; s < o.S; ++s) sum += __ldcg(pp + (size_t)s * pb);
-        emit(row, m, sum);
-    });
+#pragma unroll
+        for (int j = 0; j < kCombineOut; ++j) {
+            const int idx = o0 + 32 * j + lane;
+            if (idx < pb) emit(idx / M, idx % M, sum[j]);
+        }
+    }
     if (lane == 0) o.cnt[band] = 0;  // ready for the next replay
     return true;
 }
@@ -262,7 +298,7 @@ __device__ __forceinline__ bool combine_splits(const StepOp& o, int band, int r,
 // y.  Gated projection (W4_OP_SWIGLU): rows r and r + 8 of the band are gate
 // and up row 8*band + r; the sums go to this warp's scratch and y (I = N/2
 // columns) gets silu(gate) * up.
-template <int ACT, typename V>
+template <int ACT, int MPT, typename V>
 __device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, int M, int lane, V&& visit,
                                             float* scratch, int MP) {
     using Ops = dec::ActOps<ACT>;
@@ -274,13 +310,13 @@ __device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, in
         if (o.S == 1)
             visit(to_y);
         else
-            combine_splits(o, band, r, M, lane, visit, to_y);
+            combine_splits<MPT>(o, band, r, M, lane, visit, to_y);
         return;
     }
     auto to_scratch = [&](int row, int m, float v) { scratch[row * MP + m] = v; };
     if (o.S == 1)
         visit(to_scratch);
-    else if (!combine_splits(o, band, r, M, lane, visit, to_scratch))
+    else if (!combine_splits<MPT>(o, band, r, M, lane, visit, to_scratch))
         return;
     __syncwarp();
     const int I = o.N / 2;
@@ -410,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     const int us = u * q.Gs;
                     if (us >= t0 && us + q.Gs <= t1) {
                         // the whole band is this warp's: finish it from the accumulators
-                        finish_band<ACT>(o, q.ub + u, q.r, M, lane, [&](auto&& f) { for_frag<MP>(acc, lane, M, f); },
+                        finish_band<ACT, MP>(o, q.ub + u, q.r, M, lane, [&](auto&& f) { for_frag<MP>(acc, lane, M, f); },
                                          scratch_w, MP);
                     } else {
                         // cut between warps: park this warp's share
@@ -431,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             // then holds the band's first tile)
             const int bs = u_first * q.Gs, be = bs + q.Gs;
             if (warp > 0 && t0 < Tc && t0 != bs && warp_lo(Tc, warp - 1) <= bs) {
-                finish_band<ACT>(o, q.ub + u_first, q.r, M, lane, [&](auto&& f) {
+                finish_band<ACT, MP>(o, q.ub + u_first, q.r, M, lane, [&](auto&& f) {
                     for (int oi = lane; oi < 16 * M; oi += 32) {
                         const int row = oi / M, m = oi - row * M;
                         float sum = 0.f;
