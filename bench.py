@@ -589,6 +589,27 @@ def main():
                                     "depth": cfg.depth}}
             one.close()
         extras["per_projection_back_to_back_28_layers"] = per
+        # the same 28 projections of one type chained in the persistent step
+        # kernel (each still waits for the previous one to finish)
+        perp = {}
+        for pid, (name, N, K) in enumerate(LAYER):
+            idx = [i for i, m in enumerate(st["meta"]) if m[1] == pid]
+            wsl = [st["ws"][i] for i in idx]
+            nbw1 = w4.w4_decode_seq_workspace_bytes(wsl, M)
+            wb1 = torch.zeros(nbw1 + 256, dtype=torch.uint8, device="cuda")
+            o1 = (-wb1.data_ptr()) % 256
+            one = w4.DecodeSeq(wsl, [st["xs"][i] for i in idx], [st["ys"][i] for i in idx], M,
+                               workspace=wb1[o1:o1 + nbw1])
+            for _ in range(3):
+                one.replay()
+            us = time_replays(torch, one.replay, 100) * 1e3 / len(idx)
+            nb = (N * K) // 2 + N * (K // 128) * 2
+            perp[name] = {"us": us, "GB/s": nb / (us * 1e-6) / 1e9, "bytes": nb,
+                          "frac_of_hbm": nb / (us * 1e-6) / 1e9 / measured_peaks()[0].get("hbm_gbs", 6698.2),
+                          "status_word": one.status()}
+            one.close()
+            del wb1
+        extras["per_projection_persistent_chain_28_layers"] = perp
         extras["small_batch_step"] = small_batch_sweep(torch, w4, synth, st)
         extras["prefill_M512"] = prefill_layer(torch, w4, synth, st)
         extras["packed_file_layer0"] = packed_file_load(torch, w4, st)
