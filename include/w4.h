@@ -286,9 +286,9 @@ w4_status w4_decode_seq_create_persistent(const w4_weight* w, const void* const*
  * W4_ACT_F16 is w4_decode_seq_create_persistent; W4_ACT_I8 is described
  * above).  With W4_ACT_BF16, x and y
  * are bfloat16 and y = bf16_rne(sum x * q * s) with FP32 accumulation: the
- * the benchmark spec's FP16/BF16 activation conversion applied to the pages'
- * projection ("Building a Custom LLM Inference Runtime ...", "Technical
- * Specifications and Hardware Alignment").  Same workspace size as the
+ * pages' projection ("Building a Custom LLM Inference Runtime ...",
+ * "Technical Specifications and Hardware Alignment") with the nibble
+ * conversion producing bfloat16 instead of binary16 operands.  Same workspace size as the
  * binary16 sequence.  W4_ERR_ARG for another act. */
 w4_status w4_decode_seq_create_persistent_act(const w4_weight* w, const void* const* x,
                                               void* const* y, int n, int M, int act,

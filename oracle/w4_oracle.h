@@ -53,8 +53,8 @@ int w4o_linear(const uint16_t* x, const int8_t* q, const uint16_t* s,
 /* bfloat16 (the upper 16 bits of IEEE 754 binary32): the exact value of bit
  * pattern b, and the round-to-nearest, ties-to-even bfloat16 of v
  * (|v| >= 255.5 * 2^120 gives +/-inf, NaN gives 0x7FC0 with the sign kept).
- * For the BF16-activation variant of the projection (the benchmark spec names
- * FP16/BF16 activation conversion). */
+ * For the BF16-activation variant of the projection (x and y in bfloat16
+ * instead of binary16, weights and scales unchanged). */
 double w4o_double_from_bf16(uint16_t b);
 uint16_t w4o_bf16_from_double(double v);
 

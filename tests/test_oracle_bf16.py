@@ -11,9 +11,9 @@ projection, each against something other than the oracle itself:
 - the projection with bfloat16 x and y: exact rational brute force and the
   closed form y = bf16(s * sum x) for q = 1.
 
-The BF16-activation variant is the benchmark spec's FP16/BF16 activation
-conversion applied to the pages' W4A16 projection ("Building a Custom LLM
-Inference Runtime ...", "Technical Specifications and Hardware Alignment")."""
+The BF16-activation variant is the pages' W4A16 projection ("Building a
+Custom LLM Inference Runtime ...", "Technical Specifications and Hardware
+Alignment") with bfloat16 x and y in place of binary16."""
 import bisect
 import math
 from fractions import Fraction
