@@ -45,6 +45,23 @@ def rank_info():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(torch, value: float, world: int, device: str = "cuda") -> float:
+    """The largest of the ranks' values (each rank passes its own): the
+    slowest replica's time is the job's time.  One rank: the value itself."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every replica streams BYTES_PER_STEP per step,
+    and the job's step time is the slowest rank's."""
+    return world * BYTES_PER_STEP / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -528,11 +545,7 @@ def main():
     ev1.record(s)
     barrier()
     clocks = sampler.stop() if sampler else None
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(torch, ev0.elapsed_time(ev1) / args.steps, world)
     if layers != LAYERS:
         nb = BYTES_PER_STEP // LAYERS * layers
         if rank == 0:
@@ -541,8 +554,8 @@ def main():
                               "status_word": seq.status()}), flush=True)
         seq.close()
         return 0
-    value = world * BYTES_PER_STEP / (ms * 1e-3) / 1e9
-    per_gpu = BYTES_PER_STEP / (ms * 1e-3) / 1e9
+    value = job_gbs(world, ms)
+    per_gpu = job_gbs(1, ms)
     launches = seq.kernels()
 
     # e2e through the C ABI with host buffers: pinned x in, replay, y out, sync
@@ -558,11 +571,7 @@ def main():
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
             seq.run_host(x_pin, st["x_arena"], xb, st["y_arena"], y_pin, yb, s)
-        e2e_s = (time.perf_counter() - t0) / e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_s], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = max_over_ranks(torch, (time.perf_counter() - t0) / e2e_steps, world)
 
     extras = {}
     if not args.no_extras:
@@ -647,7 +656,7 @@ def main():
                 "roofline": roof,
                 "cpu_baseline": cpu,
                 "e2e": None if e2e_s is None else {
-                    "value": world * BYTES_PER_STEP / e2e_s / 1e9, "unit": "GB/s",
+                    "value": job_gbs(world, e2e_s * 1e3), "unit": "GB/s",
                     "us_per_step": e2e_s * 1e6, "h2d_bytes_per_step": xb, "d2h_bytes_per_step": yb,
                     "via": "w4_decode_seq_run_host (pinned host x -> device, replay, device y -> pinned host, sync)"},
                 "gpu_launches": launches * args.steps,
