@@ -260,9 +260,7 @@ __device__ __forceinline__ bool combine_splits(const StepOp& o, int band, int r,
             for (; s < o.S; ++s) sum += __ldcg(pp + (size_t)s * pb);
             emit(row, m, sum);
         });
-        if (lane == 0) o.cnt[band] = 0;  // ready for the next replay
-        return true;
-    }
+    } else {
     for (int o0 = 0; o0 < pb; o0 += 32 * kCombineOut) {
         float sum[kCombineOut];
 #pragma unroll
@@ -287,6 +285,7 @@ __device__ __forceinline__ bool combine_splits(const StepOp& o, int band, int r,
             const int idx = o0 + 32 * j + lane;
             if (idx < pb) emit(idx / M, idx % M, sum[j]);
         }
+    }
     }
     if (lane == 0) o.cnt[band] = 0;  // ready for the next replay
     return true;
@@ -544,7 +543,8 @@ struct StepPlan {
 
 // K split of one projection: S divides NC (the CTAs of a split are c % S),
 // the x slice fits its budget, and the largest per-CTA share of tiles (plus a
-// fixed cost for combining partials when S > 1) is smallest.  0 if no split fits.
+// fixed cost for combining partials when S > 1, plus the x slice's staging
+// for up to 4 tokens) is smallest.  0 if no split fits.
 static int choose_split(int bands, int G, int MP, int NC) {
     int best = 0;
     long best_cost = LONG_MAX;
@@ -553,7 +553,11 @@ static int choose_split(int bands, int G, int MP, int NC) {
         const int Gs = (G + S - 1) / S;
         if (dec::x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs) > x_budget(MP)) continue;
         const int cps = NC / S;
-        const long cost = (long)((bands + cps - 1) / cps) * Gs + (S > 1 ? kSplitPenalty + 4 * S : 0);
+        // up to 4 tokens, staging the x slice (an L2 round trip plus ~3 tile-times per KB
+        // under load) is counted too; from 8 tokens on, more splits cost more in partials
+        // than they save in staging, and the plain count measured better
+        const long x_cost = MP <= 4 ? 3L * (dec::x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs)) / 1024 : 0;
+        const long cost = (long)((bands + cps - 1) / cps) * Gs + (S > 1 ? kSplitPenalty + 4 * S : 0) + x_cost;
         if (cost < best_cost) {
             best_cost = cost;
             best = S;
