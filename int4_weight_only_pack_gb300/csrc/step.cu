@@ -85,9 +85,12 @@ constexpr int kSplitPenalty = 64;        // tiles: the cost of combining K-split
                                          // plus 4 per split
 constexpr int kMaxCtaTiles = 1 << 22;    // per-CTA tiles of one projection (float division below)
 // x slice + its group sums: small for one or two tokens so that the rings keep
-// three slots per warp; larger for more tokens (x grows with them), where
-// fewer K splits are worth a shallower ring
-__host__ __device__ constexpr int x_budget(int MP) { return MP <= 2 ? 20 * 1024 : 40 * 1024; }
+// three slots per warp; 60 KB for up to 8 tokens, where a K = 3584 projection
+// then needs no K split (its partials cost far more than the shallower ring:
+// the 8-token step went 1883 -> 1643 us) and two ring slots per warp still fit
+// next to a full projection table; 40 KB for 16 tokens, whose parked partials
+// leave no room for a larger slice
+__host__ __device__ constexpr int x_budget(int MP) { return MP <= 2 ? 20 * 1024 : MP <= 8 ? 60 * 1024 : 40 * 1024; }
 
 struct StepSmem {
     int R, bar, geo, x, xsum, park, total;
