@@ -69,7 +69,8 @@ struct StepArgs {
     unsigned* exit_cnt;  // CTAs finished with the step
     int* status;         // set non-zero when a wait gives up
     int gpc_max;         // largest x slice (groups): shared-memory sizing
-    int ring;            // ring slots per warp
+    int ring;            // ring slots per warp; at 16 tokens also the parked partials per warp in bits
+                         // 16-31 (2, or 3 with the finishing scratch): one field keeps the table's offset
     StepOp ops[kMaxStepOps];
 };
 static_assert(sizeof(StepArgs) <= 32000, "kernel parameter space");
@@ -85,23 +86,25 @@ constexpr int kSplitPenalty = 64;        // tiles: the cost of combining K-split
                                          // plus 4 per split
 constexpr int kMaxCtaTiles = 1 << 22;    // per-CTA tiles of one projection (float division below)
 // x slice + its group sums: small for one or two tokens so that the rings keep
-// three slots per warp; 60 KB for up to 8 tokens, where a K = 3584 projection
-// then needs no K split (its partials cost far more than the shallower ring:
-// the 8-token step went 1883 -> 1643 us) and two ring slots per warp still fit
-// next to a full projection table; 40 KB for 16 tokens, whose parked partials
-// leave no room for a larger slice
-__host__ __device__ constexpr int x_budget(int MP) { return MP <= 2 ? 20 * 1024 : MP <= 8 ? 60 * 1024 : 40 * 1024; }
+// three slots per warp; 60 KB from 3 tokens on, where a K = 3584 projection
+// needs no K split up to 8 tokens and two at 16 (the partials cost far more
+// than the shallower ring: the 8-token step went 1883 -> 1643 us).  Where a
+// plan with this slice cannot keep two ring slots per warp (a long projection
+// table, or 16 tokens with a gated projection's finishing scratch), the
+// fallback budget is used instead.
+__host__ __device__ constexpr int x_budget(int MP) { return MP <= 2 ? 20 * 1024 : 60 * 1024; }
+__host__ __device__ constexpr int x_budget_fallback(int MP) { return MP <= 2 ? 20 * 1024 : MP <= 8 ? 60 * 1024 : 40 * 1024; }
 
 struct StepSmem {
     int R, bar, geo, x, xsum, park, total;
-    __host__ __device__ StepSmem(int R_, int MP, int gpc_max, int nops) {
+    __host__ __device__ StepSmem(int R_, int MP, int gpc_max, int nops, int shares) {
         R = R_;
         bar = kWarps * R * kSlotTiles * kTileBytes;  // rings first: warp w's at w*R*4*1056
         geo = bar + kWarps * R * 8;
         x = (geo + nops * 16 + 127) & ~127;
         xsum = x + dec::x_bytes(MP, gpc_max);
         park = xsum + dec::xsum_bytes(MP, gpc_max);
-        total = park + kWarps * 3 * 16 * MP * 4;  // two parked shares + a finishing scratch per warp
+        total = park + kWarps * shares * 16 * MP * 4;  // two parked shares (+ a finishing scratch) per warp
     }
 };
 
@@ -338,7 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NC = gridDim.x, c = blockIdx.x, M = a.M, nops = a.nops;
-    const StepSmem L(a.ring, MP, a.gpc_max, nops);
+    // parked shares: 3 below 16 tokens, else from the table
+    const int PS = MP >= 16 ? (a.ring >> 16) : 3;
+    const StepSmem L(MP >= 16 ? (a.ring & 0xFFFF) : a.ring, MP, a.gpc_max, nops, PS);
     const int R = L.R;
     const uint32_t sbase = tc::smem_addr(smem);
     const uint32_t ring_w = sbase + (uint32_t)(warp * R * kSlotTiles * kTileBytes);
@@ -347,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L.x);
     float* xsum = reinterpret_cast<float*>(smem + L.xsum);
     float* park = reinterpret_cast<float*>(smem + L.park);
-    float* park_w = park + warp * 3 * PB;
+    float* park_w = park + warp * PS * PB;
     float* scratch_w = park_w + 2 * PB;
 
     for (int i = threadIdx.x; i < nops; i += kThreads) put_geo(geo + i, a.ops[i], c);
@@ -476,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                         for (int w2 = warp - 1; w2 < kWarps; ++w2) {
                             const int lo = warp_lo(Tc, w2), hi = warp_lo(Tc, w2 + 1);
                             if (lo >= be) break;
-                            if (lo < hi) sum += park[(w2 * 3 + (lo >= bs ? 0 : 1)) * PB + row * MP + m];
+                            if (lo < hi) sum += park[(w2 * PS + (lo >= bs ? 0 : 1)) * PB + row * MP + m];
                         }
                         f(row, m, sum);
                     }
@@ -538,7 +543,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 // ---- host-side plan ---------------------------------------------------------------
 struct StepPlan {
-    int MP = 1, NC = 0, gpc_max = 1, R = 0, smem = 0;
+    int MP = 1, NC = 0, gpc_max = 1, R = 0, smem = 0, shares = 2;
     std::vector<StepOp> ops;  // device pointers filled against a workspace base
     size_t done_off = 0, exit_off = 0, status_off = 0, total = 0;
     std::vector<size_t> cnt_off, part_off;
@@ -548,13 +553,13 @@ struct StepPlan {
 // the x slice fits its budget, and the largest per-CTA share of tiles (plus a
 // fixed cost for combining partials when S > 1, plus the x slice's staging
 // for up to 4 tokens) is smallest.  0 if no split fits.
-static int choose_split(int bands, int G, int MP, int NC) {
+static int choose_split(int bands, int G, int MP, int NC, int budget) {
     int best = 0;
     long best_cost = LONG_MAX;
     for (int S = 1; S <= std::min(G, NC); ++S) {
         if (NC % S) continue;
         const int Gs = (G + S - 1) / S;
-        if (dec::x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs) > x_budget(MP)) continue;
+        if (dec::x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs) > budget) continue;
         const int cps = NC / S;
         // up to 4 tokens, staging the x slice (an L2 round trip plus ~3 tile-times per KB
         // under load) is counted too; from 8 tokens on, more splits cost more in partials
@@ -570,9 +575,11 @@ static int choose_split(int bands, int G, int MP, int NC) {
 }
 
 // Splits, shared-memory sizing (the rings take what the rest leaves) and the
-// workspace layout.  False if some projection cannot be planned.
-static bool plan_step(const w4_weight* w, int n, int M, int NC, StepPlan* pl) {
+// workspace layout for x slices of at most `budget` bytes and `shares` parked
+// partials per warp.  False if some projection cannot be planned.
+static bool plan_step_with(const w4_weight* w, int n, int M, int NC, int budget, int shares, StepPlan* pl) {
     pl->MP = padded(M);
+    pl->shares = shares;
     pl->NC = NC;
     pl->ops.assign(n, StepOp{});
     pl->cnt_off.assign(n, 0);
@@ -585,7 +592,7 @@ static bool plan_step(const w4_weight* w, int n, int M, int NC, StepPlan* pl) {
         o.K = (int)w[i].K;
         o.G = (int)(w[i].K / kGroupK);
         o.bands = (int)num_bands(w[i].N);
-        o.S = choose_split(o.bands, o.G, pl->MP, NC);
+        o.S = choose_split(o.bands, o.G, pl->MP, NC, budget);
         if (o.S == 0) {
             fits = false;
             o.S = 1;
@@ -598,10 +605,10 @@ static bool plan_step(const w4_weight* w, int n, int M, int NC, StepPlan* pl) {
             fits = false;
         pl->gpc_max = std::max(pl->gpc_max, (o.G + o.S - 1) / o.S);
     }
-    const int fixed = StepSmem(0, pl->MP, pl->gpc_max, n).total;
+    const int fixed = StepSmem(0, pl->MP, pl->gpc_max, n, shares).total;
     pl->R = std::min(kMaxRing, (kSmemBudget - fixed) / (kWarps * (kSlotTiles * kTileBytes + 8)));
-    while (pl->R > 0 && StepSmem(pl->R, pl->MP, pl->gpc_max, n).total > kSmemBudget) --pl->R;
-    pl->smem = StepSmem(pl->R, pl->MP, pl->gpc_max, n).total;
+    while (pl->R > 0 && StepSmem(pl->R, pl->MP, pl->gpc_max, n, shares).total > kSmemBudget) --pl->R;
+    pl->smem = StepSmem(pl->R, pl->MP, pl->gpc_max, n, shares).total;
     size_t off = 0;
     pl->done_off = off;
     off = align_up(off + sizeof(unsigned) * n);
@@ -621,6 +628,19 @@ static bool plan_step(const w4_weight* w, int n, int M, int NC, StepPlan* pl) {
     return fits && pl->R >= 2;
 }
 
+// The plan with the large x budget, or, if that cannot keep two ring slots
+// per warp, with the fallback budget.  The finishing scratch (a third parked
+// share per warp) is left out only at 16 tokens without a gated projection,
+// where the 16 KB it frees lets a 60 KB x slice (2 K splits instead of 4)
+// keep two ring slots: 3689 -> 3418 us.  Below 16 tokens the kernel keeps
+// three shares as a constant (its code is unchanged there: a run-time share
+// count or ring mask measured 4-35 us slower at 1-8 tokens).
+static bool plan_step(const w4_weight* w, int n, int M, int NC, bool gated, StepPlan* pl) {
+    const int MP = padded(M), shares = (gated || MP < 16) ? 3 : 2;
+    if (plan_step_with(w, n, M, NC, x_budget(MP), shares, pl)) return true;
+    return x_budget_fallback(MP) != x_budget(MP) && plan_step_with(w, n, M, NC, x_budget_fallback(MP), shares, pl);
+}
+
 static int sm_count_now() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -638,17 +658,22 @@ static int step_grid(int MP, int act, int smem) {
     return per_sm >= 1 ? sm_count_now() : 0;
 }
 
+// Enough for the sequence with or without gated projections (the plans can
+// differ in their splits).
 size_t step_workspace_bytes(const w4_weight* w, int n, int M) {
-    StepPlan pl;
-    plan_step(w, n, M, sm_count_now(), &pl);
-    return pl.total;
+    StepPlan plain, gated;
+    plan_step(w, n, M, sm_count_now(), false, &plain);
+    plan_step(w, n, M, sm_count_now(), true, &gated);
+    return std::max(plain.total, gated.total);
 }
 
 w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y, const uint32_t* op_flags, int n,
                        int M, int act, void* ws, size_t ws_bytes, cudaStream_t stream, StepLaunch* out) {
     const int MP = padded(M);
+    bool gated = false;
+    for (int i = 0; i < n && op_flags; ++i) gated = gated || (op_flags[i] & W4_OP_SWIGLU);
     StepPlan pl;
-    if (!plan_step(w, n, M, sm_count_now(), &pl)) {
+    if (!plan_step(w, n, M, sm_count_now(), gated, &pl)) {
         set_error("the persistent step kernel cannot take this sequence (%d projections; at most %d, and each "
                   "must fit its shared-memory and index limits)",
                   n, kMaxStepOps);
@@ -687,7 +712,7 @@ w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y,
     a->exit_cnt = reinterpret_cast<unsigned*>(base + pl.exit_off);
     a->status = reinterpret_cast<int*>(base + pl.status_off);
     a->gpc_max = pl.gpc_max;
-    a->ring = pl.R;
+    a->ring = pl.R | (pl.MP >= 16 ? pl.shares << 16 : 0);
     std::copy(pl.ops.begin(), pl.ops.end(), a->ops);
     out->fn = reinterpret_cast<const void*>(step_fn(MP, act));
     out->status = a->status;
