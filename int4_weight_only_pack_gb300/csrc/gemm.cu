@@ -53,24 +53,27 @@ w4_status check_gemv_args(const void* x, const w4_weight* w, const void* y, int 
 namespace {
 
 constexpr int kBM = 128;                   // weight rows per CTA (8 bands)
-constexpr int kBN = 192;                   // tokens per CTA
 constexpr int kStages = 4;                 // shared-memory stages (one group each)
 constexpr int kASlots = 2;                 // A slots in tensor memory
-constexpr int kBStage = kBN * 128 * 2;     // 48 KB of fp16 x
 constexpr int kWStage = 8 * kTileBytes;    // the group's 8 packed tiles (one per band)
 constexpr int kThreads = 512;
-// Tensor memory: two kBN-column FP32 accumulators, then one 64-column block
-// of fp16 q pairs (128 rows x 128 K) per A slot.
-constexpr int kACol0 = 2 * kBN;
 constexpr int kTmemCols = 512;
-static_assert(kACol0 + 64 * kASlots <= kTmemCols, "tensor memory columns");
-static_assert(kBN % 32 == 0 && kBN % 16 == 0 && kBN <= 256, "MMA N and promote column blocks");
+// Per tile width BN (tokens per CTA: 128 or 192): the x stage (BN x 128 fp16),
+// and tensor memory as two BN-column FP32 accumulators followed by one
+// 64-column block of fp16 q pairs (128 rows x 128 K) per A slot.
+template <int BN>
+struct Tile {
+    static constexpr int kBStage = BN * 128 * 2;
+    static constexpr int kACol0 = 2 * BN;
+    static constexpr int kSmemBytes = kStages * (kBStage + kWStage) + 1024 + 256;
+    static_assert(kACol0 + 64 * kASlots <= kTmemCols, "tensor memory columns");
+    static_assert(BN % 64 == 0 && BN <= 256, "MMA N and promote column blocks");
+};
 // Registers per thread after the split: warpgroups 0-1 (producer, issuer,
 // dequant) give up registers to warpgroups 2-3 (promote).  The four shares
 // add up to the 128 x 512 the CTA is launched with.
 constexpr int kRegsLow = 112, kRegsHigh = 144;
 static_assert(2 * kRegsLow + 2 * kRegsHigh == 4 * 128, "register split");
-constexpr int kSmemBytes = kStages * (kBStage + kWStage) + 1024 + 256;
 constexpr size_t kStatusBytes = 256;       // workspace head: status word (+ padding)
 
 struct GemmParams {
@@ -81,7 +84,9 @@ struct GemmParams {
     int M, N, K, G, bands, splits;
 };
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, GemmParams p) {
+    constexpr int kBN = BN, kBStage = Tile<BN>::kBStage, kACol0 = Tile<BN>::kACol0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sB = smem;
@@ -343,29 +348,55 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// K splits of one call.  Cost, in units of one group's MMAs on one SM (about
-// 0.65 us): waves of CTAs (152 SMs) x groups per CTA, plus, for s > 1, the
-// FP32 partials written and read back by the reduce (8 bytes per output and
-// split, about 4.4 MB of HBM traffic per unit).  Each split keeps >= 4 groups.
-int gemm_splits(int M, int64_t N, int64_t K) {
-    const int64_t tiles = ((N + kBM - 1) / kBM) * ((M + kBN - 1) / kBN);
+// Tile width and K splits of one call, from a cost in units of one group's
+// work on one SM at the 192-token width (~0.9 us measured): waves of CTAs
+// (152 SMs) x groups per CTA x the width's relative group time (a 128-token
+// group measured 0.89 of a 192-token one), plus, for s > 1, the FP32
+// partials written and read back by the reduce (8 bytes per output and split,
+// ~6.2 MB of HBM traffic per unit).  Each split keeps >= 4 groups.  At
+// M = 512 this picks 128-token tiles for qkv and o (more CTAs busy) and 192
+// for gate_up and down.
+struct GemmPlan {
+    int bn, splits;
+};
+GemmPlan gemm_plan(int M, int64_t N, int64_t K) {
     const int G = (int)(K / kGroupK);
-    int best = 1;
+    GemmPlan best{192, 1};
     double best_t = 1e300;
-    for (int s = 1; s <= 16 && (G + s - 1) / s >= 4; ++s) {
-        const double waves = (double)((tiles * s + 151) / 152);
-        const double t = waves * ((G + s - 1) / s) + (s > 1 ? (double)s * M * (double)N * 8.0 / 4.4e6 : 0.0);
-        if (t < best_t - 1e-9) {
-            best_t = t;
-            best = s;
+    for (int bn : {192, 128}) {
+        const int64_t tiles = ((N + kBM - 1) / kBM) * ((M + bn - 1) / bn);
+        const double rel = bn == 128 ? 0.89 : 1.0;
+        for (int s = 1; s <= 16 && (G + s - 1) / s >= 4; ++s) {
+            const double waves = (double)((tiles * s + 151) / 152);
+            const double t =
+                waves * ((G + s - 1) / s) * rel + (s > 1 ? (double)s * M * (double)N * 8.0 / 6.2e6 : 0.0);
+            if (t < best_t - 1e-9) {
+                best_t = t;
+                best = GemmPlan{bn, s};
+            }
         }
     }
     return best;
 }
 
 size_t gemm_workspace(int M, int64_t N, int64_t K) {
-    const int s = gemm_splits(M, N, K);
+    const int s = gemm_plan(M, N, K).splits;
     return kStatusBytes + (s > 1 ? (size_t)s * M * N * sizeof(float) : 0);
+}
+
+template <int BN>
+w4_status launch_tile(const CUtensorMap& map, const GemmParams& p, cudaStream_t stream) {
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        Tile<BN>::kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(prefill)");
+    const dim3 grid((unsigned)((p.M + BN - 1) / BN), (unsigned)((p.N + kBM - 1) / kBM), (unsigned)p.splits);
+    gemm_tc_kernel<BN><<<grid, kThreads, Tile<BN>::kSmemBytes, stream>>>(map, p);
+    W4_CUDA_TRY(cudaGetLastError());
+    return W4_OK;
 }
 
 }  // namespace
@@ -390,10 +421,11 @@ w4_status launch_gemm_tc(const void* x, const w4_weight* w, void* y, int M, void
         set_error("cuTensorMapEncodeTiled is not available from the driver");
         return W4_ERR_UNSUPPORTED;
     }
+    const GemmPlan plan = gemm_plan(M, w->N, w->K);
     CUtensorMap map;
     const cuuint64_t gdim[2] = {(cuuint64_t)w->K, (cuuint64_t)M};
     const cuuint64_t gstride[1] = {(cuuint64_t)w->K * 2};
-    const cuuint32_t box[2] = {64, kBN};
+    const cuuint32_t box[2] = {64, (cuuint32_t)plan.bn};
     const cuuint32_t estride[2] = {1, 1};
     CUresult cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), gdim, gstride, box, estride,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -402,13 +434,6 @@ w4_status launch_gemm_tc(const void* x, const w4_weight* w, void* y, int M, void
         set_error("cuTensorMapEncodeTiled failed (%d)", (int)cr);
         return W4_ERR_CUDA;
     }
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(prefill)");
-
     GemmParams p;
     p.w = static_cast<const uint8_t*>(w->data);
     p.y = static_cast<uint16_t*>(y);
@@ -418,13 +443,12 @@ w4_status launch_gemm_tc(const void* x, const w4_weight* w, void* y, int M, void
     p.K = (int)w->K;
     p.G = (int)num_groups(w->K);
     p.bands = (int)num_bands(w->N);
-    p.splits = gemm_splits(M, w->N, w->K);
+    p.splits = plan.splits;
     p.part = p.splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(ws) + kStatusBytes) : nullptr;
 
     W4_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(int), stream));
-    const dim3 grid((unsigned)((M + kBN - 1) / kBN), (unsigned)((p.N + kBM - 1) / kBM), (unsigned)p.splits);
-    gemm_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map, p);
-    W4_CUDA_TRY(cudaGetLastError());
+    const w4_status st = plan.bn == 128 ? launch_tile<128>(map, p, stream) : launch_tile<192>(map, p, stream);
+    if (st != W4_OK) return st;
     if (p.splits > 1) {
         const size_t count = (size_t)M * p.N;
         size_t blocks = (count + 255) / 256;
