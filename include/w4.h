@@ -95,7 +95,9 @@ int w4_version(void);
  *     (r, 4c..4c+1), (r+8, 4c..4c+1), (r, 4c+2..4c+3), (r+8, 4c+2..4c+3):
  *     an m16n8k16 A fragment once k inside each 16-block is relabelled
  *     (fragment k 2c, 2c+1, 2c+8, 2c+9 <-> 4c .. 4c+3, the same relabelling
- *     applied to the activations), and two 8-byte rows of a K-major tile.
+ *     applied to the activations), and, in natural k order, the registers
+ *     of one 16-lane x 256-bit tensor-memory store (lanes r and r + 8,
+ *     32-bit columns 2c and 2c + 1 of the k16 step).
  *   - Bytes 1024 + 4p .. +3 (p = 0..7) hold the fp16 scales of rows p (low
  *     half) and p + 8 (high half).
  *   - Rows n >= N of the last band are padding: u = 8 (q = 0), scale 0.
