@@ -231,8 +231,8 @@ __device__ __forceinline__ void for_frag(const float (&acc)[(MP + 7) / 8][4], in
 // batch (kCombineOut outputs x up to 8 splits) before adding any: one output
 // and one split at a time, each load is a dependent L2 round trip, which at
 // 16 tokens (8 outputs per lane) made this the longest stretch of a
-// projection.  For fewer tokens (at most one output per lane) the plain loop
-// below measured faster.
+// projection.  At one token each lane issues its output's split loads at
+// once; at 2 and 4 tokens the plain loop measured faster.
 constexpr int kCombineOut = 4;
 template <int MP, typename V, typename E>
 __device__ __forceinline__ bool combine_splits(const StepOp& o, int band, int r, int M, int lane, V&& visit,
@@ -251,7 +251,23 @@ __device__ __forceinline__ bool combine_splits(const StepOp& o, int band, int r,
     last = __shfl_sync(0xFFFFFFFFu, last, 0);
     if (!last) return false;
     const float* base = o.part + (size_t)band * o.S * pb;
-    if constexpr (MP < 8) {
+    if constexpr (MP == 1) {
+        // one token: at most one output per lane; every split's load in flight at once
+        // (4 splits for down: 939 against 944 us per step; slower at 2 and 4 tokens)
+        visit([&](int row, int m, float) {
+            const float* pp = base + row * M + m;
+            float sum = 0.f;
+            for (int s = 0; s < o.S; s += 8) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = (s + e < o.S) ? __ldcg(pp + (size_t)(s + e) * pb) : 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (s + e < o.S) sum += v[e];  // only real splits: 0 + -0 would flip a zero's sign
+            }
+            emit(row, m, sum);
+        });
+    } else if constexpr (MP < 8) {
         visit([&](int row, int m, float) {
             const float* pp = base + row * M + m;
             float sum = 0.f;
