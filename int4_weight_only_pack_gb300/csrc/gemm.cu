@@ -9,12 +9,13 @@
 // its FP32 scale and added in FP32 registers.  The scale is never folded into
 // an FP16 weight, so the weights reach the tensor core exactly.
 //
-// One CTA computes a 128 (weight rows) x 192 (tokens) tile over a K range,
+// One CTA computes a 128 (weight rows) x BN (tokens: 192, or 128 where that
+// keeps more SMs busy; chosen per call with the K split) tile over a K range,
 // one 128-wide group per pipeline step, with warp-specialised roles:
-//   warp 0     TMA producer: x tile [192 tokens][128 K] as two 128-byte
+//   warp 0     TMA producer: x tile [BN tokens][128 K] as two 128-byte
 //              swizzled boxes (zero fill past M), and the group's 8 packed
 //              weight tiles (bulk copies) into the same shared-memory stage
-//   warp 1     one thread issues 8 tcgen05.mma (128x192x16) per group, A
+//   warp 1     one thread issues 8 tcgen05.mma (128xBNx16) per group, A
 //              from tensor memory and B (x) from shared memory, into one of
 //              two TMEM accumulators, then commits
 //   warps 4-7  dequant: read the group's packed tiles from the stage, unpack
@@ -23,15 +24,16 @@
 //              packed tile's lane layout is that store's register layout)
 //   warps 8-15 promote: read a group's FP32 partial from TMEM, hand the
 //              accumulator back, multiply by the group scale and add to
-//              FP32 accumulators in registers (96 per thread: these two
+//              FP32 accumulators in registers (BN/2 per thread: these two
 //              warpgroups take registers from the other two); finally write
 //              y (or an FP32 split-K partial)
-// Tile width: a 128xNx16 MMA takes about as long for N = 128 as for N = 256
-// on this tensor core, so narrow tiles waste it; but two 256-column
-// accumulators fill tensor memory and leave no room for A, and with one
-// accumulator the MMAs wait for every group's partial to be read out.  192
-// tokens leave room for two accumulators and two A slots (192 + 192 + 2 x 64
-// = 512 columns).
+// Tile width: the MMA instruction is full rate from N = 128 up, but in this
+// loop (per-group commits and barrier handshakes) 8 MMAs cost about as much
+// at N = 128 as at N = 256, so wide tiles pay.  Two 256-column accumulators
+// would fill tensor memory and leave no room for A, and with one accumulator
+// the MMAs wait for every group's partial to be read out; 192 tokens leave
+// room for two accumulators and two A slots (192 + 192 + 2 x 64 = 512
+// columns).
 // Every mbarrier wait is bounded; a timeout sets the status word in the
 // workspace and the CTA drains and exits instead of hanging.
 #include <cuda.h>
