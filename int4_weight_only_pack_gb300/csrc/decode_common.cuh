@@ -234,6 +234,55 @@ __device__ __forceinline__ void stage_x_async(const uint32_t* x, int M, int K, i
     tc::named_barrier(1, NCONS);
 }
 
+// Natural-order x slice (the step kernel from 4 tokens on): token m's Gs*128
+// values are contiguous at byte m * x_row_bytes(Gs); rows are padded by 32
+// bytes so that the 8-byte fragment loads of 8 tokens (a half warp's) fall in
+// distinct banks.  One bulk copy per token row fills it.
+__host__ __device__ constexpr int x_row_bytes(int Gs) { return Gs * 256 + 32; }
+__host__ __device__ constexpr int x_bytes_nat(int MP, int Gs) { return MP * x_row_bytes(Gs); }
+
+// Stage x[0:M, 128*g_lo : 128*(g_lo+Gs)) into `xs` in natural order (one bulk
+// copy per token row, completing on the mbarrier `bar`, whose phase `phase`
+// this staging completes), zero the rows of padded tokens M..MP-1, and write
+// the sum of x over every group and token m < M into xsum[gl*xsum_stride(MP)
+// + m] -- each lane adding the same four values in the same order as with the
+// fragment layout, so the sums are the same bits.  Called by all NCONS
+// threads; returns with them synchronised; false if the copies did not land
+// within the wait's bound.  x must be 16-byte aligned and K a multiple of 128.
+template <int MP, int NCONS, int ACT = kActF16>
+__device__ __forceinline__ bool stage_x_bulk(const uint32_t* x, int M, int K, int g_lo, int Gs, uint32_t* xs,
+                                             float* xsum, uint32_t bar, uint32_t phase) {
+    constexpr int kWarps = NCONS / 32;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = x_row_bytes(Gs), row_w = row / 4;
+    if (tid == 0) {
+        tc::mbar_arrive_expect_tx(bar, (uint32_t)(M * Gs * 256));
+        const uint32_t xs_s = tc::smem_addr(xs);
+        for (int m = 0; m < M; ++m)
+            tc::bulk_load(xs_s + (uint32_t)(m * row), x + (size_t)m * (K / 2) + (size_t)g_lo * 64, (uint32_t)(Gs * 256),
+                          bar);
+    }
+    for (int i = tid; i < (MP - M) * Gs * 64; i += NCONS) {
+        const int m = M + i / (Gs * 64), w = i - (m - M) * (Gs * 64);
+        xs[m * row_w + w] = 0;
+    }
+    const bool ok = tc::mbar_wait(bar, phase);
+    for (int idx = warp; idx < Gs * M; idx += kWarps) {
+        const int gl = idx / M, m = idx - gl * M;
+        const int q = lane >> 3, c = (lane >> 1) & 3, e = (lane & 1) * 2;
+        const int st = 2 * q + (e >> 1);  // k16 step; the lane's k are 4c .. 4c+3 of it
+        const uint32_t* src = xs + m * row_w + gl * 64 + st * 8 + c * 2;
+        const float2 f0 = ActOps<ACT>::to_float2(src[0]);
+        const float2 f1 = ActOps<ACT>::to_float2(src[1]);
+        float sum = (f0.x + f0.y) + (f1.x + f1.y);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+        if (lane == 0) xsum[gl * xsum_stride(MP) + m] = sum;
+    }
+    tc::named_barrier(1, NCONS);
+    return ok;
+}
+
 // Predicated shared-memory loads: lanes whose predicate is false issue no
 // access (and cost no bandwidth) and keep the register's previous contents.
 __device__ __forceinline__ void lds128_if(uint4& v, uint32_t a, uint32_t pred) {
@@ -245,6 +294,11 @@ __device__ __forceinline__ void lds128_if(uint4& v, uint32_t a, uint32_t pred) {
 __device__ __forceinline__ void lds64f_if(float2& v, uint32_t a, uint32_t pred) {
     asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p ld.shared.v2.f32 {%0,%1}, [%3];\n}\n"
                  : "+f"(v.x), "+f"(v.y)
+                 : "r"(pred), "r"(a));
+}
+__device__ __forceinline__ void lds64_if(uint32_t& lo, uint32_t& hi, uint32_t a, uint32_t pred) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p ld.shared.v2.u32 {%0,%1}, [%3];\n}\n"
+                 : "+r"(lo), "+r"(hi)
                  : "r"(pred), "r"(a));
 }
 
@@ -266,6 +320,7 @@ struct TileMac {
     uint32_t xl, sl;                         // load predicates: x fragments, group sums
     uint4 xv[4][NT];                         // x fragments of up to four tiles
     float2 X[4][NT];                         // group sums of up to four tiles
+    int xrow = 0;                            // natural x layout: bytes per token row
 
     __device__ __forceinline__ TileMac(uint32_t x_smem, uint32_t xsum_smem, int lane, int /*Gs*/ = 0) {
         const int tok = lane >> 2, cl4 = lane & 3;
@@ -282,11 +337,21 @@ struct TileMac {
             }
     }
 
+    // Read x from the natural layout of stage_x_bulk (rows of row_bytes)
+    // instead of the fragment layout: run_tiles<NTL, true>.
+    __device__ __forceinline__ void set_natural(uint32_t x_smem, int lane, int row_bytes) {
+        const int tok = lane >> 2, cl4 = lane & 3;
+        xrow = row_bytes;
+        xfrag = x_smem + (uint32_t)((tok % MP) * row_bytes + cl4 * 8);
+    }
+
     // acc += s * sum_{k in group} x * q for NTL consecutive tiles at ta, ta +
     // 1056, ... (groups gl, gl + 1, ... of one band), their MMA chains
     // interleaved; the tiles are added to acc in order.  Per tile and row:
     //     acc += s * (kLo * D - kBias * sum_k x)      (kHi for rows r + 8)
-    template <int NTL>
+    // NAT: x in the natural layout (two 8-byte loads per pair of k16 steps:
+    // the same registers as the fragment layout's one 16-byte load).
+    template <int NTL, bool NAT = false>
     __device__ __forceinline__ void run_tiles(uint32_t ta, int gl, int lane, float (&acc)[NT][4]) {
         uint32_t wd[NTL][8], sc[NTL];
 #pragma unroll
@@ -300,15 +365,22 @@ struct TileMac {
             for (int nt = 0; nt < NT; ++nt)
                 lds64f_if(X[n][nt], xsum + (uint32_t)(((gl + n) * xsum_stride(MP) + nt * 8) * 4), sl);
         }
-        const uint32_t xa0 = xfrag + (uint32_t)gl * (MP * 256);
+        const uint32_t xa0 = NAT ? xfrag + (uint32_t)gl * 256 : xfrag + (uint32_t)gl * (MP * 256);
         float pe[NTL][NT][4], po[NTL][NT][4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {  // k16 steps 2q (even chain) and 2q + 1 (odd chain)
 #pragma unroll
             for (int n = 0; n < NTL; ++n) {
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    lds128_if(xv[n][nt], xa0 + (uint32_t)(n * MP * 256 + q * MP * 64 + nt * 512), xl);
+                for (int nt = 0; nt < NT; ++nt) {
+                    if constexpr (NAT) {
+                        const uint32_t a = xa0 + (uint32_t)(n * 256 + q * 64 + nt * 8 * xrow);
+                        lds64_if(xv[n][nt].x, xv[n][nt].y, a, xl);
+                        lds64_if(xv[n][nt].z, xv[n][nt].w, a + 32, xl);
+                    } else {
+                        lds128_if(xv[n][nt], xa0 + (uint32_t)(n * MP * 256 + q * MP * 64 + nt * 512), xl);
+                    }
+                }
                 uint32_t a[4], b[4];
                 Ops::unpack(wd[n][2 * q], a);
                 Ops::unpack(wd[n][2 * q + 1], b);
@@ -470,7 +542,7 @@ struct TileMac<MP, kActI8> {
         gs_stride = Gs;
     }
 
-    template <int NTL>
+    template <int NTL, bool NAT = false>  // NAT: unused (Path A keeps its own x layout)
     __device__ __forceinline__ void run_tiles(uint32_t ta, int gl, int lane, float (&acc)[NT][4]) {
 #pragma unroll
         for (int n = 0; n < NTL; ++n) run(ta + (uint32_t)(n * kTileBytes), gl + n, lane, acc);

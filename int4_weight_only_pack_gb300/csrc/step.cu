@@ -95,14 +95,25 @@ constexpr int kMaxCtaTiles = 1 << 22;    // per-CTA tiles of one projection (flo
 __host__ __device__ constexpr int x_budget(int MP) { return MP <= 2 ? 20 * 1024 : 60 * 1024; }
 __host__ __device__ constexpr int x_budget_fallback(int MP) { return MP <= 2 ? 20 * 1024 : MP <= 8 ? 60 * 1024 : 40 * 1024; }
 
+// x slice bytes: the fragment layout up to two tokens, from four on the
+// natural layout that one bulk copy per token row fills (see stage_x_bulk:
+// the larger slices staged by many 8-byte copies took 2.5 us at 4 tokens;
+// step 1212 -> 1190 us at 4 tokens, 1645 -> 1565 at 8, 3420 -> 3336 at 16;
+// unchanged at 1, 2 us slower at 2)
+__host__ __device__ constexpr bool step_x_natural(int MP) { return MP >= 4; }
+__host__ __device__ constexpr int step_x_bytes(int MP, int Gs) {
+    return step_x_natural(MP) ? dec::x_bytes_nat(MP, Gs) : dec::x_bytes(MP, Gs);
+}
+
 struct StepSmem {
-    int R, bar, geo, x, xsum, park, total;
+    int R, bar, xbar, geo, x, xsum, park, total;
     __host__ __device__ StepSmem(int R_, int MP, int gpc_max, int nops, int shares) {
         R = R_;
         bar = kWarps * R * kSlotTiles * kTileBytes;  // rings first: warp w's at w*R*4*1056
-        geo = bar + kWarps * R * 8;
+        xbar = bar + kWarps * R * 8;                 // x staging (natural layout only)
+        geo = xbar + (step_x_natural(MP) ? 16 : 0);
         x = (geo + nops * 16 + 127) & ~127;
-        xsum = x + dec::x_bytes(MP, gpc_max);
+        xsum = x + step_x_bytes(MP, gpc_max);
         park = xsum + dec::xsum_bytes(MP, gpc_max);
         total = park + kWarps * shares * 16 * MP * 4;  // two parked shares (+ a finishing scratch) per warp
     }
@@ -384,6 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         }
     };
     if (lane < R) tc::mbar_init(bar_w + 8 * lane, 1);
+    // x slices from four tokens on: natural layout, one bulk copy per token row
+    constexpr bool kNat = step_x_natural(MP) && ACT != dec::kActI8;
+    const uint32_t xbar = sbase + (uint32_t)L.xbar;
+    uint32_t xphase = 0;
+    if (kNat && threadIdx.x == 0) tc::mbar_init(xbar, 1);
     tc::mbar_init_fence();
     __syncthreads();
     if (threadIdx.x == 0) prefetch_x(0);
@@ -422,9 +438,16 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         if (q.nu > 0) {
             if constexpr (ACT == dec::kActI8)
                 dec::stage_x_q8<MP, kThreads>(o.x, M, o.K, q.g_lo, q.Gs, xs, xsum, park);  // parks are free now
-            else
+            else if constexpr (!kNat)
                 dec::stage_x_async<MP, kThreads, ACT>(o.x, M, o.K, q.g_lo, q.Gs, xs, xsum);
+            else {
+                if (!dec::stage_x_bulk<MP, kThreads, ACT>(o.x, M, o.K, q.g_lo, q.Gs, xs, xsum, xbar, xphase) &&
+                    threadIdx.x == 0)
+                    atomicOr(a.status, 8);
+                xphase ^= 1;
+            }
             dec::TileMac<MP, ACT> mac(sbase + L.x, sbase + L.xsum, lane, q.Gs);
+            if constexpr (kNat) mac.set_natural(sbase + L.x, lane, dec::x_row_bytes(q.Gs));
             const int Tc = q.Tc();
             const int t0 = warp_lo(Tc, warp), t1 = warp_lo(Tc, warp + 1);
             const int u_first = div_small(t0, q.Gs, q.inv_gs);
@@ -443,14 +466,16 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                         --inflight;
                         static_assert(kSlotTiles == 4, "chunk cases below");
                         if constexpr (MP >= 16) {  // register budget: at most two tiles at once
-                            if (n >= 2) mac.template run_tiles<2>(ta, gl, lane, acc);
-                            if (n == 4) mac.template run_tiles<2>(ta + 2 * kTileBytes, gl + 2, lane, acc);
-                            if (n & 1) mac.run(ta + (uint32_t)((n - 1) * kTileBytes), gl + n - 1, lane, acc);
+                            if (n >= 2) mac.template run_tiles<2, kNat>(ta, gl, lane, acc);
+                            if (n == 4) mac.template run_tiles<2, kNat>(ta + 2 * kTileBytes, gl + 2, lane, acc);
+                            if (n & 1)
+                                mac.template run_tiles<1, kNat>(ta + (uint32_t)((n - 1) * kTileBytes), gl + n - 1,
+                                                                lane, acc);
                         } else {
-                            if (n == 4) mac.template run_tiles<4>(ta, gl, lane, acc);
-                            else if (n == 3) mac.template run_tiles<3>(ta, gl, lane, acc);
-                            else if (n == 2) mac.template run_tiles<2>(ta, gl, lane, acc);
-                            else mac.run(ta, gl, lane, acc);
+                            if (n == 4) mac.template run_tiles<4, kNat>(ta, gl, lane, acc);
+                            else if (n == 3) mac.template run_tiles<3, kNat>(ta, gl, lane, acc);
+                            else if (n == 2) mac.template run_tiles<2, kNat>(ta, gl, lane, acc);
+                            else mac.template run_tiles<1, kNat>(ta, gl, lane, acc);
                         }
                         __syncwarp();  // every lane is done reading the slot
                         if (cur.issue(a, geo, warp, lane, ta, bar)) ++inflight;
@@ -575,12 +600,12 @@ static int choose_split(int bands, int G, int MP, int NC, int budget) {
     for (int S = 1; S <= std::min(G, NC); ++S) {
         if (NC % S) continue;
         const int Gs = (G + S - 1) / S;
-        if (dec::x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs) > budget) continue;
+        if (step_x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs) > budget) continue;
         const int cps = NC / S;
         // up to 4 tokens, staging the x slice (an L2 round trip plus ~3 tile-times per KB
         // under load) is counted too; from 8 tokens on, more splits cost more in partials
         // than they save in staging, and the plain count measured better
-        const long x_cost = MP <= 4 ? 3L * (dec::x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs)) / 1024 : 0;
+        const long x_cost = MP <= 4 ? 3L * (step_x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs)) / 1024 : 0;
         const long cost = (long)((bands + cps - 1) / cps) * Gs + (S > 1 ? kSplitPenalty + 4 * S : 0) + x_cost;
         if (cost < best_cost) {
             best_cost = cost;
