@@ -489,6 +489,8 @@ def main():
     ap.add_argument("--profile-projection", choices=[n for n, _, _ in LAYER], default=None,
                     help="launch one projection of layer 0 (library launch shape) --steps times: a small "
                          "case for a profiler")
+    ap.add_argument("--act", choices=("fp16", "int8"), default="fp16",
+                    help="with --no-extras: activation path of the step (int8 = Path A, x quantised in the kernel)")
     ap.add_argument("--profile-m", type=int, default=1,
                     help="with --profile-projection: tokens (M > 16 runs the prefill GEMM)")
     args = ap.parse_args()
@@ -520,7 +522,8 @@ def main():
     nbw = w4.w4_decode_seq_workspace_bytes(st["ws"], M)
     ws_buf = torch.zeros(nbw + 256, dtype=torch.uint8, device="cuda")
     ws_off = (-ws_buf.data_ptr()) % 256
-    seq = w4.DecodeSeq(st["ws"], st["xs"], st["ys"], M, workspace=ws_buf[ws_off:ws_off + nbw])
+    act = args.act if args.no_extras else "fp16"
+    seq = w4.DecodeSeq(st["ws"], st["xs"], st["ys"], M, workspace=ws_buf[ws_off:ws_off + nbw], act=act)
     for _ in range(args.warmup):
         seq.replay()
     torch.cuda.synchronize()
@@ -549,7 +552,7 @@ def main():
     if layers != LAYERS:
         nb = BYTES_PER_STEP // LAYERS * layers
         if rank == 0:
-            print(json.dumps({"profile_case": "decode step of the first %d layers, M=1" % layers,
+            print(json.dumps({"profile_case": "decode step of the first %d layers, M=1, %s activations" % (layers, act),
                               "bytes_per_step": nb, "us_per_step": ms * 1e3, "GB/s": nb / (ms * 1e-3) / 1e9,
                               "status_word": seq.status()}), flush=True)
         seq.close()
