@@ -309,7 +309,8 @@ def small_batch_sweep(torch, w4, synth, st, Ms=(2, 4, 8, 16), reps=50):
     for M in Ms:
         xs, ys, keep = [], [], []
         for (layer, pid, N, K) in st["meta"]:
-            x = torch.randn((M, K), device="cuda").half().view(torch.int16)
+            x = torch.from_numpy(synth.x_full(synth.seed_of(CONFIG_ID, layer, pid, synth.T_X), M, K)
+                                 .view(np.int16)).cuda()
             y = torch.zeros((M, N), dtype=torch.int16, device="cuda")
             xs.append(x)
             ys.append(y)

@@ -153,6 +153,73 @@ def test_full_decode_step_sampled():
         seq.close()
 
 
+RAGGED = [(200, 1024), (37, 384), (16, 128), (1000, 2432), (3584, 18944), (4608, 3584)]
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 6, 7, 9, 12, 13, 15, 16])
+def test_persistent_step_ragged_shapes_every_token_count(M):
+    """The persistent step kernel on row counts that are not a multiple of 16
+    (a padded last band), a one-band one-group projection, a group count with
+    no small divisor, the down shape (K split across CTAs; at 16 tokens also
+    the smaller x slice) and token counts that pad to 2, 4, 8 and 16: against
+    the oracle, and the same bits on a second replay."""
+    rng = np.random.default_rng(400 + M)
+    probs, keep, ws, xs, ys = [], [], [], [], []
+    for N, K in RAGGED:
+        x, q, s = rand_problem(rng, M, N, K)
+        packed, w = pack_on_device(q, s)
+        keep.append(packed)
+        ws.append(w)
+        xs.append(dev(x))
+        ys.append(torch.zeros((M, N), dtype=torch.int16, device="cuda"))
+        probs.append((x, q, s))
+    seq = make_seq(ws, xs, ys, M, "persistent")
+    seq.replay()
+    torch.cuda.synchronize()
+    assert seq.status() == 0
+    got = [host(y).copy() for y in ys]
+    for i, (x, q, s) in enumerate(probs):
+        assert_close(got[i], oracle.linear(x, q, s), "N=%d K=%d" % RAGGED[i])
+    for y in ys:
+        y.fill_(0)
+    seq.replay()
+    torch.cuda.synchronize()
+    for i in range(len(ys)):
+        assert np.array_equal(host(ys[i]), got[i])
+    seq.close()
+
+
+@pytest.mark.parametrize("M", [4, 16])
+def test_full_layer_shapes_step_small_batch_sampled(M):
+    """Four layers of the real projection shapes at M tokens through the
+    persistent step kernel (the launch configuration the small-batch step is
+    timed in: K splits on every projection at 16 tokens), every projection
+    checked against the oracle on sampled rows."""
+    CONFIG = 3
+    keep, ws, xs, ys, meta = [], [], [], [], []
+    for layer in range(4):
+        for pid, proj in enumerate(LAYER):
+            N, K = LAYER[proj]
+            packed, w = synth_weight(CONFIG, layer, pid, N, K)
+            x = synth.x_full(synth.seed_of(CONFIG, layer, pid, synth.T_X), M, K)
+            keep.append(packed)
+            ws.append(w)
+            xs.append(dev(x))
+            ys.append(torch.zeros((M, N), dtype=torch.int16, device="cuda"))
+            meta.append((layer, pid, N, K, x))
+    seq = make_seq(ws, xs, ys, M, "persistent")
+    seq.replay()
+    seq.replay()
+    torch.cuda.synchronize()
+    assert seq.status() == 0
+    rng = np.random.default_rng(12)
+    for i, (layer, pid, N, K, x) in enumerate(meta):
+        rows = np.unique(np.concatenate([[0, 15, 16, N - 1], rng.integers(0, N, 20)]))
+        ref, _ = oracle_rows(CONFIG, layer, pid, M, N, K, rows, x_bits=x)
+        assert_close(host(ys[i])[:, rows], ref, "layer %d proj %d" % (layer, pid))
+    seq.close()
+
+
 def check_step(meta, ys, CONFIG, M):
     rng = np.random.default_rng(11)
     for i, (layer, pid, N, K, x) in enumerate(meta):
