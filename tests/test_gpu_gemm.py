@@ -27,9 +27,9 @@ def run(x, w, N, M):
     return host(y)
 
 
-# Token tiles are 192 wide and weight tiles 128 rows (8 bands): the cases
-# straddle both boundaries (M = 191, 192, 193, 385, 576; N with a partial
-# band and a partial 8-band tile) and include a call that splits K.
+# Token tiles are 128 or 192 wide and weight tiles 128 rows (8 bands): the
+# cases straddle both boundaries (M = 128, 191, 192, 193, 385, 576; N with a
+# partial band and a partial 8-band tile) and include a call that splits K.
 @pytest.mark.parametrize("M,N,K", [(17, 64, 256), (40, 136, 384), (128, 256, 512), (512, 256, 1024),
                                    (512, 200, 1280), (300, 128, 2048), (1, 64, 256), (16, 64, 256),
                                    (191, 200, 1024), (192, 128, 512), (193, 136, 4096), (385, 264, 768),
