@@ -171,11 +171,38 @@ def time_replays(torch, fn, reps: int) -> float:
     return a.elapsed_time(b) / reps
 
 
+def code_only(src: str) -> str:
+    """C/C++ source without its comments, blank space collapsed (string and
+    character literals kept as written)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_digest() -> str:
+    """The step kernel's sources, comments and blank space removed (so the ncu
+    figures taken on the same code stay valid across comment edits)."""
     h = hashlib.sha256()
     for name in ("step.cu", "step_launch.h", "decode_common.cuh", "w4_internal.cuh", "w4_device.cuh", "tc_ptx.cuh"):
-        with open(os.path.join(ROOT, "int4_weight_only_pack_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "int4_weight_only_pack_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -229,11 +229,6 @@ __device__ __forceinline__ void for_frag(const float (&acc)[(MP + 7) / 8][4], in
     }
 }
 
-// Finish band `band` of projection o from per-lane outputs (visit(f) calls
-// f(row, m, value) for each output this lane holds; every output of the band
-// is held by exactly one lane of the warp).  S == 1: write y.  S > 1: publish
-// this split's partial; the arrival that completes the band adds the S
-// partials in split order and writes y.
 // The final FP32 sums of band `band` of a K-split projection: publish this
 // split's partial; the arrival that completes the band adds the S partials in
 // split order and hands each sum to emit(row, m, sum).  False for every other
