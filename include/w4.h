@@ -261,15 +261,20 @@ w4_status w4_decode_seq_run_host(w4_seq* seq, const void* x_host, void* x_dev,
 size_t w4_decode_seq_workspace_bytes(const w4_weight* w, int n, int M);
 
 /* The same projection chain as w4_decode_seq_create, run by ONE persistent
- * cooperative kernel (two CTAs per SM) captured as a one-node graph.  Each
- * CTA's producer streams the weights of every projection back to back into a
- * shared-memory ring, never waiting on the chain, while its consumers compute
- * projection i only after every CTA has finished projection i - 1 (completion
- * counters in `workspace`), so the data dependency of a real decode step
- * (x[i] computed from y[i-1]) is honoured.  Same arithmetic and results as
- * w4a16_gemv.  `workspace` holds the projection table, the counters and
- * K-split partials; it must stay alive and unshared while the sequence
- * exists, and replays of one sequence must not overlap on the GPU.
+ * cooperative kernel (one CTA of 16 warps per SM) captured as a one-node
+ * graph.  Each warp streams its share of the weights of every projection
+ * back to back into its own shared-memory ring, never waiting on the chain,
+ * and computes projection i only after every CTA has finished projection
+ * i - 1 (completion counters in `workspace`), so the data dependency of a
+ * real decode step (x[i] computed from y[i-1]) is honoured.  Same arithmetic
+ * as w4a16_gemv; where the two cut K differently the last bits can differ.
+ * Every replay gives the same bits.  `workspace` (of
+ * w4_decode_seq_workspace_bytes, 256-byte aligned: W4_ERR_WORKSPACE /
+ * W4_ERR_ALIGN otherwise) holds the completion counters, the status word and
+ * the K-split partials; the projection table travels in the launch's
+ * parameters.  The workspace must stay alive and unshared while the sequence
+ * exists, and replays of one sequence must not overlap on the GPU.  At most
+ * 448 projections; W4_ERR_UNSUPPORTED for a sequence the kernel cannot take.
  * Synchronous (initialises the workspace). */
 w4_status w4_decode_seq_create_persistent(const w4_weight* w, const void* const* x,
                                           void* const* y, int n, int M, void* workspace,

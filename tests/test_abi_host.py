@@ -121,3 +121,44 @@ def test_default_configs_of_the_layer_shapes():
             c = w4.w4a16_gemv_default_config(M, N, K)
             assert c.bands_per_cta in (1, 2, 4) and 1 <= c.splits <= 8 and 8 <= c.depth <= 96 and c.depth % 8 == 0
             assert c.ctas_per_sm in (1, 2)
+
+
+def _sm_count_is_152_or_no_gpu():
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return torch.cuda.get_device_properties(0).multi_processor_count == 152
+    except ImportError:
+        pass
+    return True  # no device: the planner assumes 152 SMs
+
+
+@pytest.mark.skipif(not _sm_count_is_152_or_no_gpu(), reason="the plan below is GB300's (152 SMs)")
+def test_step_plan_of_the_benchmarked_step():
+    """The persistent step's workspace for the 28-layer sequence pins the
+    planner's K splits: the completion counters and status word (768 bytes for
+    112 projections), plus, per K-split projection, an arrival counter per band
+    and FP32 partials [bands][S][16 M] (each 256-byte aligned).  At one token
+    only down is split (4 ways), at two tokens only down (8 ways)."""
+    layer = [(4608, 3584), (3584, 3584), (37888, 3584), (3584, 18944)]
+    ws = [w4.w4_weight_view(0x100000, N, K) for _ in range(28) for N, K in layer]
+
+    def align(v):
+        return (v + 255) // 256 * 256
+
+    def down_split(S, M):
+        bands = 3584 // 16
+        return align(4 * bands) + align(4 * bands * S * 16 * M)
+
+    assert w4.w4_decode_seq_workspace_bytes(ws, 1) == 768 + 28 * down_split(4, 1)
+    assert w4.w4_decode_seq_workspace_bytes(ws, 2) == 768 + 28 * down_split(8, 2)
+    sizes = [w4.w4_decode_seq_workspace_bytes(ws, M) for M in range(1, 17)]
+    assert all(a <= b for a, b in zip(sizes, sizes[1:]))  # partials grow with the tokens
+
+
+def test_step_workspace_argument_checks():
+    w = w4.w4_weight_view(0x1000, 16, 128)
+    assert w4.w4_decode_seq_workspace_bytes([w], 1) == 512  # counters only: one tile is never split
+    for M in (0, 17):
+        assert w4.w4_decode_seq_workspace_bytes([w], M) == 0
+    assert w4.w4_decode_seq_workspace_bytes([w4.Weight(0x1000, 16, 128, 0x12345678, 1)], 1) == 0
