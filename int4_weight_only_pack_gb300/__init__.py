@@ -294,8 +294,8 @@ class DecodeSeq:
                                                             ctypes.byref(self._h)))
         else:
             if act != "fp16" or op_flags is not None:
-                raise ValueError("bfloat16 activations and projection options need the persistent sequence "
-                                 "(pass a workspace)")
+                raise ValueError("bfloat16 or INT8 activations and projection options need the persistent "
+                                 "sequence (pass a workspace)")
             _check(lib().w4_decode_seq_create(self._w, self._x, self._y, n, M, int(use_pdl), _stream(stream),
                                               ctypes.byref(self._h)))
 
