@@ -70,7 +70,7 @@ int w4_version(void);
 
 /* ------------------------------------------------------------------------
  * Packed layout (the offline repack).  The pages describe a "ValueShuffle"
- * layout that interleaves even and odd nibbles for the byte-permute
+ * layout in which even and odd nibbles alternate, to suit the byte-permute
  * datapath ("Building a Custom LLM Inference Runtime ...", "The .nanoqwen
  * File Format and Safety Protocols"; "The Architecture of Modern Inference
  * ...", "Data Integrity and Serialization: The .nanoqwen Format"), without the
@@ -334,8 +334,8 @@ void w4_decode_seq_destroy(w4_seq* seq);
 
 /* ------------------------------------------------------------------------
  * Packed-weight file.  The pages keep their quantised weights in a
- * memory-mappable file that opens with a 256-byte header starting with a
- * magic string, and refuse to load a file whose magic does not match
+ * memory-mappable file whose first 256 bytes are a header that begins with
+ * a magic string, and refuse to load a file whose magic does not match
  * ("Building a Custom LLM Inference Runtime ...", "The .nanoqwen File Format
  * and Safety Protocols"; "The Architecture of Modern Inference ...", "Data
  * Integrity and Serialization: The .nanoqwen Format").  Here a file holds ONE

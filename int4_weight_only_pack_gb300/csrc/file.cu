@@ -3,8 +3,8 @@
 // with nothing to parse.
 //
 // The pages' runtime keeps its quantised weights in a memory-mappable file
-// that opens with a 256-byte header starting with a magic string, and refuses
-// to load anything whose magic does not match ("Building a Custom LLM
+// whose first 256 bytes are a header that begins with a magic string, and
+// refuses to load anything whose magic does not match ("Building a Custom LLM
 // Inference Runtime ...", "The .nanoqwen File Format and Safety Protocols";
 // "The Architecture of Modern Inference ...", "Data Integrity and
 // Serialization: The .nanoqwen Format").  This file holds one weight in this
