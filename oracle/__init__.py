@@ -37,35 +37,41 @@ def lib():
     global _lib
     if _lib is None:
         build()
-        L = ctypes.CDLL(_LIB)
-        L.w4o_double_from_half.restype = ctypes.c_double
-        L.w4o_double_from_half.argtypes = [ctypes.c_uint16]
-        L.w4o_half_from_double.restype = ctypes.c_uint16
-        L.w4o_half_from_double.argtypes = [ctypes.c_double]
-        L.w4o_double_from_bf16.restype = ctypes.c_double
-        L.w4o_double_from_bf16.argtypes = [ctypes.c_uint16]
-        L.w4o_bf16_from_double.restype = ctypes.c_uint16
-        L.w4o_bf16_from_double.argtypes = [ctypes.c_double]
-        L.w4o_linear_act.restype = ctypes.c_int
-        L.w4o_linear_act.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
-                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
-                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
-        L.w4o_quantize_x8.restype = None
-        L.w4o_quantize_x8.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
-                                      ctypes.c_void_p]
-        L.w4o_linear_q8.restype = ctypes.c_int
-        L.w4o_linear_q8.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                                    ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
-                                    ctypes.c_void_p, ctypes.c_void_p]
-        L.w4o_linear.restype = ctypes.c_int
-        L.w4o_linear.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        _lib = load(_LIB)
+    return _lib
+
+
+def load(path: str) -> ctypes.CDLL:
+    """The oracle library at `path` with its entry points typed (a test may
+    load a copy built from a modified source)."""
+    L = ctypes.CDLL(path)
+    L.w4o_double_from_half.restype = ctypes.c_double
+    L.w4o_double_from_half.argtypes = [ctypes.c_uint16]
+    L.w4o_half_from_double.restype = ctypes.c_uint16
+    L.w4o_half_from_double.argtypes = [ctypes.c_double]
+    L.w4o_double_from_bf16.restype = ctypes.c_double
+    L.w4o_double_from_bf16.argtypes = [ctypes.c_uint16]
+    L.w4o_bf16_from_double.restype = ctypes.c_uint16
+    L.w4o_bf16_from_double.argtypes = [ctypes.c_double]
+    L.w4o_linear_act.restype = ctypes.c_int
+    L.w4o_linear_act.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
-        L.w4o_pack_layout.restype = ctypes.c_int
-        L.w4o_pack_layout.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
-                                      ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
-        _lib = L
-    return _lib
+    L.w4o_quantize_x8.restype = None
+    L.w4o_quantize_x8.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                  ctypes.c_void_p]
+    L.w4o_linear_q8.restype = ctypes.c_int
+    L.w4o_linear_q8.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                ctypes.c_void_p, ctypes.c_void_p]
+    L.w4o_linear.restype = ctypes.c_int
+    L.w4o_linear.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    L.w4o_pack_layout.restype = ctypes.c_int
+    L.w4o_pack_layout.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                  ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
+    return L
 
 
 def double_from_half(h: int) -> float:

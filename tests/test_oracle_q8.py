@@ -42,6 +42,18 @@ def test_quantisation_matches_numpy_binary32(scale):
         assert np.all(err <= 0.5 * float(sx[m]) + 1e-4 * float(sx[m]) + 1e-30)
 
 
+def test_quantisation_ties_go_to_even():
+    """With max|x| = 127 the step sx is exactly 1, so x / sx = x and every
+    half-integer x is a tie: round half to even, as the reading of the
+    quantisation states (not half away from zero)."""
+    vals = [127.0, 0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 126.5, -125.5, 4.0, -7.25]
+    want = [127, 0, 2, 2, 4, 0, -2, -2, 126, -126, 4, -7]
+    x = np.array([vals], dtype=np.float16).view(np.uint16)
+    xq, sx = oracle.quantize_x8(x)
+    assert float(sx[0]) == 1.0
+    assert xq[0].tolist() == want
+
+
 def test_zero_row_quantises_to_zero():
     x = np.zeros((2, 256), dtype=np.uint16)
     xq, sx = oracle.quantize_x8(x)
