@@ -1,7 +1,8 @@
 """The oracle's pins catch plausible mistakes.  Each case plants one mistake
 in a copy of the oracle's C source (a wrong group index, a dropped term, a
 tie rounded the wrong way, a transposed layout offset, a wrong sign or
-stride), builds the copy with gcc and runs every oracle pin of the
+stride; for the gated MLP output, which the oracle forms in Python, a copy
+of that function), builds the copy with gcc and runs every oracle pin of the
 `test_oracle_*` files against it: at least one pin must fail.  An unmodified
 copy built the same way passes them all, so a failure comes from the planted
 mistake, not from the harness.  Nothing here touches a GPU."""
@@ -45,6 +46,15 @@ MUTANTS = {
     "Path A ties rounded away": [("r = lrintf(t);", "r = lroundf(t);", 0)],
     "Path A scale of token 0 for every token": [("(double)sx[m] * (double)isum", "(double)sx[0] * (double)isum", 0)],
     "Path A step from 128 instead of 127": [("const float scale = amax / 127.0f;", "const float scale = amax / 128.0f;", 0)],
+}
+
+# The gated MLP output is formed in Python (oracle.swiglu): its mistakes are
+# planted in a copy of that function.  name -> (text, replacement)
+PY_MUTANTS = {
+    "SwiGLU sigmoid sign": ("h = g / (1.0 + np.exp(-g)) * u", "h = g / (1.0 + np.exp(g)) * u"),
+    "SwiGLU gate and up swapped": ("g, u = acc[:, :I], acc[:, I:]", "u, g = acc[:, :I], acc[:, I:]"),
+    "SwiGLU gate rounded to binary16 first": ("g, u = acc[:, :I], acc[:, I:]",
+                                              "g, u = acc[:, :I].astype(np.float16).astype(np.float64), acc[:, I:]"),
 }
 
 
@@ -124,4 +134,16 @@ def test_unmodified_copy_passes_every_pin(tmp_path, monkeypatch):
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_planted_mistake_fails_a_pin(tmp_path, monkeypatch, name):
     failed = _failing_pins(monkeypatch, _build(tmp_path, MUTANTS[name]))
+    assert failed, "no pin catches: " + name
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_planted_swiglu_mistake_fails_a_pin(monkeypatch, name):
+    old, new = PY_MUTANTS[name]
+    src = inspect.getsource(oracle.swiglu)
+    assert old in src, "mutation target not found: %r" % old
+    ns = dict(vars(oracle))
+    exec(src.replace(old, new), ns)
+    monkeypatch.setattr(oracle, "swiglu", ns["swiglu"])
+    failed = _failing_pins(monkeypatch, oracle.lib())
     assert failed, "no pin catches: " + name
