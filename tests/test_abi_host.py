@@ -162,3 +162,15 @@ def test_step_workspace_argument_checks():
     for M in (0, 17):
         assert w4.w4_decode_seq_workspace_bytes([w], M) == 0
     assert w4.w4_decode_seq_workspace_bytes([w4.Weight(0x1000, 16, 128, 0x12345678, 1)], 1) == 0
+
+
+@pytest.mark.skipif(not _sm_count_is_152_or_no_gpu(), reason="the plan below is GB300's (152 SMs)")
+def test_prefill_plan_of_a_512_token_prompt():
+    """The prefill workspace pins the GEMM planner's K splits: a 256-byte head
+    (status word) plus FP32 partials [splits][M][N] when K is split.  At 512
+    tokens qkv, o and gate_up are not split and down is split 5 ways."""
+    head = 256
+    for N, K, splits in [(4608, 3584, 1), (3584, 3584, 1), (37888, 3584, 1), (3584, 18944, 5)]:
+        want = head + (splits * 512 * N * 4 if splits > 1 else 0)
+        assert w4.w4_workspace_bytes(512, N, K) == want, (N, K)
+    assert w4.w4_workspace_bytes(16, 3584, 18944) == 0  # the decode kernel needs none
