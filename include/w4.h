@@ -225,6 +225,16 @@ w4_status w4a16_gemm(const void* x, const w4_weight* w, void* y, int M,
 #define W4_STATIC_SCRATCH_BYTES (4u << 20)
 w4_status w4a16_gemm_static_scratch(const void* x, const w4_weight* w, void* y, int M, void* stream);
 
+/* Status word of the static scratch on the current device: what the last
+ * w4a16_gemm_static_scratch call with M > 16 left there.  0 when every
+ * pipeline wait of that call completed; non-zero when one gave up after
+ * about a second (that call's y is then not valid), which the caller cannot
+ * otherwise see, since the word lives in the library's private array.
+ * Synchronous: a plain device-to-host copy of 4 bytes.  Synchronise the
+ * call's stream first (a non-blocking stream is not waited for).  -1 if the
+ * word cannot be read (w4_last_error() says why).  Allocates nothing. */
+int w4a16_gemm_static_scratch_status(void);
+
 /* ------------------------------------------------------------------------
  * Decode step sequence ("Building a Custom LLM Inference Runtime ...",
  * "The Impact of CUDA Graphs": capturing the whole decode step in one CUDA

@@ -61,6 +61,7 @@ _SIGNATURES = {
     "w4a16_gemv_default_config": (_int, [_int, _i64, _i64, ctypes.POINTER(GemvConfig)]),
     "w4a16_gemm": (_int, [_vp, ctypes.POINTER(Weight), _vp, _int, _vp, _sz, _vp]),
     "w4a16_gemm_static_scratch": (_int, [_vp, ctypes.POINTER(Weight), _vp, _int, _vp]),
+    "w4a16_gemm_static_scratch_status": (_int, []),
     "w4_decode_seq_create": (_int, [ctypes.POINTER(Weight), ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _int,
                                     _int, _vp, ctypes.POINTER(_vp)]),
     "w4_decode_seq_replay": (_int, [_vp, _vp]),
@@ -256,6 +257,12 @@ W4_STATIC_SCRATCH_BYTES = 4 << 20
 def w4a16_gemm_static_scratch(x, w: Weight, y, M: int, stream=None):
     """w4a16_gemm without a workspace: the library's static device scratch."""
     _check(lib().w4a16_gemm_static_scratch(_addr(x), ctypes.byref(w), _addr(y), M, _stream(stream)))
+
+
+def w4a16_gemm_static_scratch_status() -> int:
+    """Status word the last static-scratch prefill left on the current device
+    (0 = every pipeline wait completed; synchronise its stream first)."""
+    return lib().w4a16_gemm_static_scratch_status()
 
 
 def w4_decode_seq_workspace_bytes(weights, M: int) -> int:

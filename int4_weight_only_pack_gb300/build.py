@@ -7,15 +7,19 @@ from __future__ import annotations
 
 import concurrent.futures
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
+import sys
+import time
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libw4.so")
+DIGEST = LIB + ".digest"  # content digest of the sources the library was built from
 BUILD_DIR = os.path.join(ROOT, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -35,14 +39,30 @@ def _sources():
 
 
 def _deps():
-    return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(INCLUDE, "w4.h")]
+    """Every file the library's compilation reads: the translation units, every
+    header beside them and the public header."""
+    return sorted(_sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) +
+                  [os.path.join(INCLUDE, "w4.h")])
+
+
+def source_digest() -> str:
+    """SHA-256 over the names and contents of every dependency and the
+    compiler flags: the library is rebuilt whenever any of them changes,
+    whatever the files' timestamps say."""
+    h = hashlib.sha256()
+    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    for p in _deps():
+        h.update(os.path.relpath(p, ROOT).encode() + b"\0")
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not (os.path.exists(LIB) and os.path.exists(DIGEST)):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in _deps())
+    with open(DIGEST) as f:
+        return f.read().strip() == source_digest()
 
 
 def _compile(src: str, extra) -> str:
@@ -54,9 +74,15 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
+def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = False) -> str:
+    """Compile libw4.so unless it was built from exactly the current sources;
+    prints one line saying which happened (to stderr, unless quiet)."""
+    digest = source_digest()
     if not force and up_to_date():
+        if not quiet:
+            print("libw4.so: reused (built from the current sources, digest %s)" % digest[:12], file=sys.stderr)
         return LIB
+    t0 = time.time()
     os.makedirs(BUILD_DIR, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
     srcs = _sources()
@@ -68,6 +94,11 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stdout + r.stderr))
     os.replace(tmp, LIB)
+    with open(DIGEST, "w") as f:
+        f.write(digest + "\n")
+    if not quiet:
+        print("libw4.so: compiled %d translation units with nvcc for sm_103a in %.1f s (digest %s)"
+              % (len(srcs), time.time() - t0, digest[:12]), file=sys.stderr)
     return LIB
 
 

@@ -1,4 +1,6 @@
 // Error reporting and version of libw4.so.
+#include <mutex>
+
 #include "w4_internal.cuh"
 
 namespace w4 {
@@ -41,6 +43,20 @@ w4_status check_weight(const w4_weight* w) {
         return W4_ERR_ALIGN;
     }
     return W4_OK;
+}
+
+int device_sm_count() {
+    static std::mutex mu;
+    static int cache[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kDefaultSms;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = kDefaultSms;
+        cache[dev] = n;
+    }
+    return cache[dev];
 }
 
 }  // namespace w4

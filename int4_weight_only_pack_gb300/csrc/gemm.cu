@@ -352,7 +352,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // Tile width and K splits of one call, from a cost in units of one group's
 // work on one SM at the 192-token width (~0.9 us measured): waves of CTAs
-// (152 SMs) x groups per CTA x the width's relative group time (a 128-token
+// (the device's SMs) x groups per CTA x the width's relative group time (a 128-token
 // group measured 0.89 of a 192-token one), plus, for s > 1, the FP32
 // partials written and read back by the reduce (8 bytes per output and split,
 // ~6.2 MB of HBM traffic per unit).  Each split keeps >= 4 groups.  At
@@ -363,13 +363,14 @@ struct GemmPlan {
 };
 GemmPlan gemm_plan(int M, int64_t N, int64_t K) {
     const int G = (int)(K / kGroupK);
+    const int sms = device_sm_count();
     GemmPlan best{192, 1};
     double best_t = 1e300;
     for (int bn : {192, 128}) {
         const int64_t tiles = ((N + kBM - 1) / kBM) * ((M + bn - 1) / bn);
         const double rel = bn == 128 ? 0.89 : 1.0;
         for (int s = 1; s <= 16 && (G + s - 1) / s >= 4; ++s) {
-            const double waves = (double)((tiles * s + 151) / 152);
+            const double waves = (double)((tiles * s + sms - 1) / sms);
             const double t =
                 waves * ((G + s - 1) / s) * rel + (s > 1 ? (double)s * M * (double)N * 8.0 / 6.2e6 : 0.0);
             if (t < best_t - 1e-9) {
@@ -386,15 +387,33 @@ size_t gemm_workspace(int M, int64_t N, int64_t K) {
     return kStatusBytes + (s > 1 ? (size_t)s * M * N * sizeof(float) : 0);
 }
 
+// Raise the prefill kernel's dynamic shared-memory limit on the current
+// device.  The attribute belongs to the (device, kernel) pair, so it is set
+// once per device for each tile width; a failed attempt is not remembered and
+// is retried on the next call.
+template <int BN>
+w4_status allow_tile_smem() {
+    static std::mutex mu;
+    static bool done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) {
+        set_error("device ordinal %d out of range", dev);
+        return W4_ERR_UNSUPPORTED;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return W4_OK;
+    e = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile<BN>::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill)");
+    done[dev] = true;
+    return W4_OK;
+}
+
 template <int BN>
 w4_status launch_tile(const CUtensorMap& map, const GemmParams& p, cudaStream_t stream) {
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        Tile<BN>::kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(prefill)");
+    const w4_status st = allow_tile_smem<BN>();
+    if (st != W4_OK) return st;
     const dim3 grid((unsigned)((p.M + BN - 1) / BN), (unsigned)((p.N + kBM - 1) / kBM), (unsigned)p.splits);
     gemm_tc_kernel<BN><<<grid, kThreads, Tile<BN>::kSmemBytes, stream>>>(map, p);
     W4_CUDA_TRY(cudaGetLastError());
@@ -454,7 +473,8 @@ w4_status launch_gemm_tc(const void* x, const w4_weight* w, void* y, int M, void
     if (p.splits > 1) {
         const size_t count = (size_t)M * p.N;
         size_t blocks = (count + 255) / 256;
-        if (blocks > 152 * 16) blocks = 152 * 16;
+        const size_t cap = (size_t)device_sm_count() * 16;  // enough resident blocks to cover every SM
+        if (blocks > cap) blocks = cap;
         splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p.part, p.splits, count, p.y);
         W4_CUDA_TRY(cudaGetLastError());
     }
@@ -474,8 +494,6 @@ namespace w4 {
 namespace {
 
 __device__ __align__(256) unsigned char g_static_scratch[W4_STATIC_SCRATCH_BYTES];
-
-constexpr int kMaxDevices = 64;
 
 // Device address of g_static_scratch on the current device, looked up once per
 // device (with that device current).  In host code the array's name is only a
@@ -531,6 +549,19 @@ extern "C" w4_status w4a16_gemm_static_scratch(const void* x, const w4_weight* w
     st = static_scratch_address(&scratch);
     if (st != W4_OK) return st;
     return launch_gemm_tc(x, w, y, M, scratch, W4_STATIC_SCRATCH_BYTES, s);
+}
+
+extern "C" int w4a16_gemm_static_scratch_status(void) {
+    clear_error();
+    void* scratch = nullptr;
+    if (static_scratch_address(&scratch) != W4_OK) return -1;
+    int v = 0;
+    const cudaError_t e = cudaMemcpy(&v, scratch, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+        cuda_fail(e, "cudaMemcpy(static scratch status)");
+        return -1;
+    }
+    return v;
 }
 
 extern "C" size_t w4_workspace_bytes(int M, int64_t N, int64_t K) {

@@ -16,15 +16,18 @@
 //    at once, so the next projection's CTAs can do the same.
 //  * Eight consumer warps consume every slot in order, warp w taking the
 //    slot's tile w, and all eight hand the slot back.  Unpacking: one
-//    32-bit word per lane and k16 step holds eight nibbles; two LOP3 masks
-//    with the fp16 exponent pattern 0x6400 (and the same after a shift by 8)
-//    give 1024 + u and 1024 + 16u, and one f16x2 subtract or FMA turns them
-//    into q exactly: an m16n8k16 A fragment.
+//    32-bit word per lane and k16 step holds eight offset-binary nibbles u;
+//    two masks (0x000F000F and 0x00F000F0, and the same after a shift by 8)
+//    leave four f16x2 registers whose halves are u itself as exact fp16
+//    subnormals, u * 2^-24 (rows r) and u * 2^-20 (rows r + 8): an m16n8k16
+//    A fragment with no floating-point conversion (5 integer ops per word).
 //  * MACs: mma.sync m16n8k16 (FP16 x FP16 products are exact, FP32
-//    accumulation) per 128-wide group; the group's FP32 partial is scaled by
-//    the group's FP32 scale and added in FP32.  x is the B operand (tokens
-//    padded to 8 or 16), staged once per CTA in shared memory in fragment
-//    order after the wait on the previous grid.
+//    accumulation) per 128-wide group gives D = sum_k x * u * 2^-24 (2^-20);
+//    the group's exact partial sum_k x * q = 2^24 * D - 8 * sum_k x (2^20
+//    for rows r + 8) is scaled by the group's FP32 scale and added in FP32.
+//    x is the B operand (tokens padded to 8 or 16), staged once per CTA in
+//    shared memory in fragment order after the wait on the previous grid,
+//    with its per-group sums sum_k x computed once at staging.
 //  * Work unit: a block of `bands_per_cta` 16-row bands over the CTA's K range.
 //    Per block, the warps' partials are summed in fixed order in shared
 //    memory; with a K split, every non-leader CTA of the cluster stores its
@@ -50,21 +53,6 @@ constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr int kMaxSmem = 220 * 1024;
 constexpr int kDefaultRing = 64;
 constexpr int kMaxRing = 96;
-
-// SM count of the current device (looked up once per device).
-static int sm_count() {
-    static std::mutex mu;
-    static int cache[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!cache[dev]) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 152;
-        cache[dev] = n;
-    }
-    return cache[dev];
-}
 
 struct GemvParams {
     const uint32_t* x;  // fp16 pairs, [M, K/2]
@@ -345,7 +333,7 @@ static const TunedShape kTuned[] = {
 void default_gemv_config(int M, int64_t N, int64_t K, w4_gemv_config* c) {
     const int64_t bands = num_bands(N);
     const int G = (int)num_groups(K);
-    const int sms = sm_count();
+    const int sms = device_sm_count();
     for (const TunedShape& t : kTuned)
         if (t.N == N && t.K == K && M >= t.m_lo && M <= t.m_hi &&
             gemv_smem_bytes(M, G, t.c.bands_per_cta, t.c.splits, t.c.depth) <=
@@ -443,7 +431,7 @@ w4_status launch_gemv(const void* x, const w4_weight* w, void* y, int M, const w
     p.nblocks = (p.bands + c.bands_per_cta - 1) / c.bands_per_cta;
     p.ring = c.depth;
     p.early_trigger = c.pdl == 2 ? 1 : 0;
-    const int clusters = c.ctas_per_sm * sm_count() / c.splits;
+    const int clusters = c.ctas_per_sm * device_sm_count() / c.splits;
     const int P = p.nblocks < clusters ? p.nblocks : clusters;
 
     cudaLaunchConfig_t cfg = {};

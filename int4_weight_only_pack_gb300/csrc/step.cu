@@ -677,29 +677,21 @@ static bool plan_step(const w4_weight* w, int n, int M, int NC, bool gated, Step
     return x_budget_fallback(MP) != x_budget(MP) && plan_step_with(w, n, M, NC, x_budget_fallback(MP), shares, pl);
 }
 
-static int sm_count_now() {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-        return 152;
-    return sms;
-}
-
 // One resident CTA per SM, or 0 if the kernel cannot be resident.
 static int step_grid(int MP, int act, int smem) {
     int per_sm = 0;
     StepKernel fn = step_fn(MP, act);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess) return 0;
-    return per_sm >= 1 ? sm_count_now() : 0;
+    return per_sm >= 1 ? device_sm_count() : 0;
 }
 
 // Enough for the sequence with or without gated projections (the plans can
 // differ in their splits).
 size_t step_workspace_bytes(const w4_weight* w, int n, int M) {
     StepPlan plain, gated;
-    plan_step(w, n, M, sm_count_now(), false, &plain);
-    plan_step(w, n, M, sm_count_now(), true, &gated);
+    plan_step(w, n, M, device_sm_count(), false, &plain);
+    plan_step(w, n, M, device_sm_count(), true, &gated);
     return std::max(plain.total, gated.total);
 }
 
@@ -709,7 +701,7 @@ w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y,
     bool gated = false;
     for (int i = 0; i < n && op_flags; ++i) gated = gated || (op_flags[i] & W4_OP_SWIGLU);
     StepPlan pl;
-    if (!plan_step(w, n, M, sm_count_now(), gated, &pl)) {
+    if (!plan_step(w, n, M, device_sm_count(), gated, &pl)) {
         set_error("the persistent step kernel cannot take this sequence (%d projections; at most %d, and each "
                   "must fit its shared-memory and index limits)",
                   n, kMaxStepOps);

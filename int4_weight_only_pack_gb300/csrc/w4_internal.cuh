@@ -41,6 +41,15 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 w4_status check_weight(const w4_weight* w);
 
+// ---- devices ---------------------------------------------------------------
+// Device ordinals the per-device caches of the library cover.
+constexpr int kMaxDevices = 64;
+// SM count assumed when no device can be queried (a GB300 has 152).
+constexpr int kDefaultSms = 152;
+// SM count of the current device, looked up once per device; kDefaultSms
+// when no device is available (host-only planning).
+int device_sm_count();
+
 // ---- device primitives -----------------------------------------------------
 // Programmatic dependent launch: wait for the previous grid on the stream to
 // finish (and its memory to be visible), and allow the next grid to start.
