@@ -331,6 +331,16 @@ w4_status w4_decode_seq_create_persistent_ex(const w4_weight* w, const void* con
                                              size_t workspace_bytes, void* stream,
                                              w4_seq** out);
 
+/* The K split of every projection of the persistent sequence these weights
+ * would run at M tokens with activation type act and options op_flags (as
+ * for w4_decode_seq_create_persistent_ex) on the current device:
+ * splits[n] receives S, the number of CTAs that share each band's K range
+ * (S > 1: their FP32 partials are added through the workspace).  Planning
+ * only: no device work, no allocation; without a device the plan assumes
+ * 152 SMs. */
+w4_status w4_decode_seq_splits(const w4_weight* w, int n, int M, int act,
+                               const uint32_t* op_flags, int* splits);
+
 /* Status word of a persistent sequence (a synchronous device read): 0 when
  * every wait of its replays so far completed, non-zero when one gave up after
  * about a second (the outputs of that replay are then invalid).  0 for graph

@@ -79,6 +79,8 @@ _SIGNATURES = {
                                                   _int, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
     "w4_pack_glu": (_int, [_vp, _vp, _i64, _i64, _vp, _sz, _int, _vp, ctypes.POINTER(Weight)]),
     "w4_decode_seq_status": (_int, [_vp]),
+    "w4_decode_seq_splits": (_int, [ctypes.POINTER(Weight), _int, _int, _int, ctypes.POINTER(ctypes.c_uint32),
+                                     ctypes.POINTER(_int)]),
     "w4_decode_seq_destroy": (None, [_vp]),
     "w4_file_write": (_int, [ctypes.c_char_p, ctypes.POINTER(Weight), _int, _vp]),
     "w4_file_info": (_int, [ctypes.c_char_p, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_sz)]),
@@ -263,6 +265,15 @@ def w4a16_gemm_static_scratch_status() -> int:
     """Status word the last static-scratch prefill left on the current device
     (0 = every pipeline wait completed; synchronise its stream first)."""
     return lib().w4a16_gemm_static_scratch_status()
+
+
+def w4_decode_seq_splits(weights, M: int, act: str = "fp16", op_flags=None):
+    """K split per projection of the persistent sequence's plan."""
+    n = len(weights)
+    flags = (ctypes.c_uint32 * n)(*op_flags) if op_flags is not None else None
+    out = (_int * n)()
+    _check(lib().w4_decode_seq_splits((Weight * n)(*weights), n, M, DecodeSeq.ACT[act], flags, out))
+    return list(out)
 
 
 def w4_decode_seq_workspace_bytes(weights, M: int) -> int:

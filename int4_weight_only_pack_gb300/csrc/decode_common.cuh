@@ -190,6 +190,43 @@ __device__ __forceinline__ void stage_x(const uint32_t* x, int M, int K, int g_l
     tc::named_barrier(1, kConsumers);
 }
 
+// Sum x over every group gl < Gs and token m < M into xsum[gl *
+// xsum_stride(MP) + m], each lane adding the four values at word offsets
+// word(gl, m) and word(gl, m) + 1 (the layout's fragment positions of lane
+// class (lane >> 1) & 3, k16 step 2 * (lane >> 3) + (lane & 1)), then a
+// butterfly over the warp: the same order, so the same bits, whatever the
+// layout.  Warp w takes groups w, w + NW, ...; four groups' reductions are
+// interleaved, and no index is divided by the run-time token count.
+template <int MP, int NW, int ACT, typename Word>
+__device__ __forceinline__ void sum_groups(const uint32_t* xs, float* xsum, int M, int Gs, int warp, int lane,
+                                           Word&& word) {
+    constexpr int kBatch = 4;
+    for (int g0 = warp; g0 < Gs; g0 += NW * kBatch) {
+        for (int m = 0; m < M; ++m) {
+            float sum[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int gl = g0 + b * NW;
+                sum[b] = 0.f;
+                if (gl < Gs) {
+                    const uint32_t* src = xs + word(gl, m);
+                    const float2 f0 = ActOps<ACT>::to_float2(src[0]);
+                    const float2 f1 = ActOps<ACT>::to_float2(src[1]);
+                    sum[b] = (f0.x + f0.y) + (f1.x + f1.y);
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) sum[b] += __shfl_xor_sync(0xFFFFFFFFu, sum[b], off);
+            if (lane == 0)
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b)
+                    if (g0 + b * NW < Gs) xsum[(g0 + b * NW) * xsum_stride(MP) + m] = sum[b];
+        }
+    }
+}
+
 // The same staging as stage_x, with every 8-byte piece (the b0, b1 words of
 // one lane class and k16 step) copied from global memory straight into its
 // fragment slot by a cp.async, all issued before any is waited for: one
@@ -220,17 +257,10 @@ __device__ __forceinline__ void stage_x_async(const uint32_t* x, int M, int K, i
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     tc::named_barrier(1, NCONS);
-    for (int idx = warp; idx < Gs * M; idx += kWarps) {
-        const int gl = idx / M, m = idx - gl * M;
-        const int q = lane >> 3, c = (lane >> 1) & 3, e = (lane & 1) * 2;
-        const uint32_t* src = xs + gl * (MP * 64) + q * (MP * 16) + (m * 4 + c) * 4 + e;
-        const float2 f0 = ActOps<ACT>::to_float2(src[0]);
-        const float2 f1 = ActOps<ACT>::to_float2(src[1]);
-        float sum = (f0.x + f0.y) + (f1.x + f1.y);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-        if (lane == 0) xsum[gl * xsum_stride(MP) + m] = sum;
-    }
+    const int q = lane >> 3, c = (lane >> 1) & 3, e = (lane & 1) * 2;
+    sum_groups<MP, kWarps, ACT>(xs, xsum, M, Gs, warp, lane, [&](int gl, int m) {
+        return gl * (MP * 64) + q * (MP * 16) + (m * 4 + c) * 4 + e;
+    });
     tc::named_barrier(1, NCONS);
 }
 
@@ -267,18 +297,10 @@ __device__ __forceinline__ bool stage_x_bulk(const uint32_t* x, int M, int K, in
         xs[m * row_w + w] = 0;
     }
     const bool ok = tc::mbar_wait(bar, phase);
-    for (int idx = warp; idx < Gs * M; idx += kWarps) {
-        const int gl = idx / M, m = idx - gl * M;
-        const int q = lane >> 3, c = (lane >> 1) & 3, e = (lane & 1) * 2;
-        const int st = 2 * q + (e >> 1);  // k16 step; the lane's k are 4c .. 4c+3 of it
-        const uint32_t* src = xs + m * row_w + gl * 64 + st * 8 + c * 2;
-        const float2 f0 = ActOps<ACT>::to_float2(src[0]);
-        const float2 f1 = ActOps<ACT>::to_float2(src[1]);
-        float sum = (f0.x + f0.y) + (f1.x + f1.y);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-        if (lane == 0) xsum[gl * xsum_stride(MP) + m] = sum;
-    }
+    const int q = lane >> 3, c = (lane >> 1) & 3, e = (lane & 1) * 2;
+    const int st = 2 * q + (e >> 1);  // k16 step; the lane's k are 4c .. 4c+3 of it
+    sum_groups<MP, kWarps, ACT>(xs, xsum, M, Gs, warp, lane,
+                                [&](int gl, int m) { return m * row_w + gl * 64 + st * 8 + c * 2; });
     tc::named_barrier(1, NCONS);
     return ok;
 }

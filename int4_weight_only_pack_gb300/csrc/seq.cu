@@ -169,6 +169,31 @@ extern "C" size_t w4_decode_seq_workspace_bytes(const w4_weight* w, int n, int M
     return step_workspace_bytes(w, n, M);
 }
 
+extern "C" w4_status w4_decode_seq_splits(const w4_weight* w, int n, int M, int act, const uint32_t* op_flags,
+                                          int* splits) {
+    clear_error();
+    if (!w || !splits || n < 1 || n > kMaxStepOps) {
+        set_error("NULL argument or n outside 1..%d", kMaxStepOps);
+        return W4_ERR_ARG;
+    }
+    if (M < 1 || M > 16) {
+        set_error("M=%d: the persistent sequence takes 1 <= M <= 16", M);
+        return W4_ERR_SHAPE;
+    }
+    if (act != W4_ACT_F16 && act != W4_ACT_BF16 && act != W4_ACT_I8) {
+        set_error("unknown activation type %d", act);
+        return W4_ERR_ARG;
+    }
+    bool gated = false;
+    for (int i = 0; i < n; ++i) {
+        const w4_status st = check_weight(&w[i]);
+        if (st != W4_OK) return st;
+        gated = gated || (op_flags && (op_flags[i] & W4_OP_SWIGLU));
+    }
+    step_splits(w, n, M, act, gated, splits);
+    return W4_OK;
+}
+
 extern "C" w4_status w4_decode_seq_create_persistent_ex(const w4_weight* w, const void* const* x,
                                                         void* const* y, const uint32_t* op_flags, int n, int M,
                                                         int act, void* workspace, size_t workspace_bytes,

@@ -347,8 +347,9 @@ __device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, in
         return;
     __syncwarp();
     const int I = o.N / 2;
-    for (int oi = lane; oi < 8 * M; oi += 32) {
-        const int rr = oi / M, m = oi - rr * M;
+    for (int oi = lane; oi < 8 * MPT; oi += 32) {
+        const int rr = oi / MPT, m = oi % MPT;  // MPT is a power of two: shifts
+        if (m >= M) continue;
         const float g = scratch[rr * MP + m], u = scratch[(rr + 8) * MP + m];
         const int n = band * 8 + rr;
         if (n < I) o.y[(size_t)m * I + n] = Ops::round(g / (1.f + expf(-g)) * u);
@@ -511,8 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             const int bs = u_first * q.Gs, be = bs + q.Gs;
             if (warp > 0 && t0 < Tc && t0 != bs && warp_lo(Tc, warp - 1) <= bs) {
                 finish_band<ACT, MP>(o, q.ub + u_first, q.r, M, lane, [&](auto&& f) {
-                    for (int oi = lane; oi < 16 * M; oi += 32) {
-                        const int row = oi / M, m = oi - row * M;
+                    // outputs strided by the padded token count (a power of two: no division)
+                    for (int oi = lane; oi < 16 * MP; oi += 32) {
+                        const int row = oi / MP, m = oi % MP;
+                        if (m >= M) continue;
                         float sum = 0.f;
                         for (int w2 = warp - 1; w2 < kWarps; ++w2) {
                             const int lo = warp_lo(Tc, w2), hi = warp_lo(Tc, w2 + 1);
@@ -693,6 +696,13 @@ size_t step_workspace_bytes(const w4_weight* w, int n, int M) {
     plan_step(w, n, M, device_sm_count(), false, &plain);
     plan_step(w, n, M, device_sm_count(), true, &gated);
     return std::max(plain.total, gated.total);
+}
+
+void step_splits(const w4_weight* w, int n, int M, int act, bool gated, int* splits) {
+    (void)act;
+    StepPlan pl;
+    plan_step(w, n, M, device_sm_count(), gated, &pl);
+    for (int i = 0; i < n; ++i) splits[i] = pl.ops[i].S;
 }
 
 w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y, const uint32_t* op_flags, int n,

@@ -27,5 +27,7 @@ w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y,
 w4_status step_launch(const StepLaunch& s, cudaStream_t stream);
 int step_status(const StepLaunch& s);
 size_t step_workspace_bytes(const w4_weight* w, int n, int M);
+// K split per projection of the plan the current device would run.
+void step_splits(const w4_weight* w, int n, int M, int act, bool gated, int* splits);
 
 }  // namespace w4

@@ -135,13 +135,20 @@ def _sm_count_is_152_or_no_gpu():
 
 @pytest.mark.skipif(not _sm_count_is_152_or_no_gpu(), reason="the plan below is GB300's (152 SMs)")
 def test_step_plan_of_the_benchmarked_step():
-    """The persistent step's workspace for the 28-layer sequence pins the
-    planner's K splits: the completion counters and status word (768 bytes for
-    112 projections), plus, per K-split projection, an arrival counter per band
-    and FP32 partials [bands][S][16 M] (each 256-byte aligned).  At one token
-    only down is split (4 ways), at two tokens only down (8 ways)."""
+    """The persistent step's planner on the benchmarked 28-layer sequence
+    (qkv, o, gate_up, down per layer).  At one token only down's K is split,
+    four ways (its x slice then fits beside three ring slots per warp), at two
+    tokens eight ways, the same for bfloat16 and INT8 activations.  The
+    workspace holds the completion counters and status word (768 bytes for
+    112 projections) plus, per split projection, an arrival counter per band
+    and FP32 partials [bands][S][16 M] (each 256-byte aligned)."""
     layer = [(4608, 3584), (3584, 3584), (37888, 3584), (3584, 18944)]
     ws = [w4.w4_weight_view(0x100000, N, K) for _ in range(28) for N, K in layer]
+    for act in ("fp16", "bf16", "int8"):
+        assert w4.w4_decode_seq_splits(ws, 1, act) == [1, 1, 1, 4] * 28
+        assert w4.w4_decode_seq_splits(ws, 2, act) == [1, 1, 1, 8] * 28
+    gated = [0, 0, w4.W4_OP_SWIGLU, 0] * 28
+    assert w4.w4_decode_seq_splits(ws, 1, "fp16", gated) == [1, 1, 1, 4] * 28
 
     def align(v):
         return (v + 255) // 256 * 256
@@ -154,6 +161,16 @@ def test_step_plan_of_the_benchmarked_step():
     assert w4.w4_decode_seq_workspace_bytes(ws, 2) == 768 + 28 * down_split(8, 2)
     sizes = [w4.w4_decode_seq_workspace_bytes(ws, M) for M in range(1, 17)]
     assert all(a <= b for a, b in zip(sizes, sizes[1:]))  # partials grow with the tokens
+
+
+def test_step_splits_argument_checks():
+    w = w4.w4_weight_view(0x1000, 16, 128)
+    assert w4.w4_decode_seq_splits([w], 1) == [1]  # one tile is never split
+    for bad in (0, 17):
+        with pytest.raises(w4.W4Error):
+            w4.w4_decode_seq_splits([w], bad)
+    with pytest.raises(w4.W4Error):
+        w4.w4_decode_seq_splits([w4.Weight(0x1000, 16, 128, 0x12345678, 1)], 1)
 
 
 def test_step_workspace_argument_checks():
