@@ -171,6 +171,24 @@ def time_replays(torch, fn, reps: int) -> float:
     return a.elapsed_time(b) / reps
 
 
+def replay_spread(torch, fn, reps: int = 100) -> dict:
+    """Per-call device times of `reps` back-to-back calls of fn(): one CUDA
+    event between consecutive calls on the current stream, so each interval
+    is one call as the stream saw it (the gap to the next launch included).
+    Median and the 10th and 90th percentiles, in microseconds."""
+    s = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(s)
+    for k in range(reps):
+        fn()
+        ev[k + 1].record(s)
+    torch.cuda.synchronize()
+    us = np.array([ev[k].elapsed_time(ev[k + 1]) * 1e3 for k in range(reps)])
+    return {"reps": reps, "median_us": float(np.median(us)), "p10_us": float(np.percentile(us, 10)),
+            "p90_us": float(np.percentile(us, 90)), "min_us": float(us.min()), "max_us": float(us.max())}
+
+
 def code_only(src: str) -> str:
     """C/C++ source without its comments, blank space collapsed (string and
     character literals kept as written)."""
@@ -266,6 +284,26 @@ def run_reference(args):
     return 0
 
 
+def cpu_single_gemv_one_thread(oracle, synth, budget_s: float = 4.0):
+    """The oracle on one host thread over the single-GEMV workload (qkv
+    4608x3584, M = 1), every 16th output row: GB/s of weight bytes."""
+    _, N, K = LAYER[0]
+    rows = np.arange(0, N, 16)
+    q, s, x = synth.projection_inputs(CONFIG_ID, 0, 0, 1, N, K, rows=rows)
+    nbytes = len(rows) * ((K // 2) + (K // 128) * 2)
+    oracle.linear(x, q, s, threads=1)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.linear(x, q, s, threads=1)
+        n += 1
+        if time.perf_counter() - t0 > budget_s or n >= 200:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "qkv 4608x3584 at M=1, every 16th output row (%d weight+scale bytes), %d passes, one thread"
+                      % (nbytes, n)}
+
+
 def cpu_baseline(oracle, synth, budget_s: float = 12.0):
     cores = host_cores()
     probs, nbytes = oracle_sample(synth)
@@ -329,6 +367,45 @@ def run_one_projection(args):
     return 0
 
 
+def single_gemv_rotated(torch, w4, synth, st, copies=32, reps=20):
+    """The single-GEMV workload (qkv 4608x3584, M = 1) through w4a16_gemv over
+    `copies` distinct packed weights launched in turn (32 x 8.5 MB = 272 MB,
+    over twice the 129 MB L2, so every launch reads its weight from DRAM):
+    us per GEMV and weight GB/s, with the spread of the per-launch times."""
+    dev = torch.device("cuda")
+    pid = 0
+    _, N, K = LAYER[pid]
+    G = K // 128
+    idx = [i for i, m in enumerate(st["meta"]) if m[1] == pid]
+    ws = [st["ws"][i] for i in idx]
+    keep = []
+    layer = LAYERS
+    while len(ws) < copies:  # more seeded qkv weights beyond the step's 28 layers
+        q = torch.empty((N, K), dtype=torch.int8, device=dev)
+        s = torch.empty((N, G), dtype=torch.int16, device=dev)
+        synth.q_device(synth.seed_of(CONFIG_ID, layer, pid, synth.T_Q), N, K, q)
+        synth.scale_device(synth.seed_of(CONFIG_ID, layer, pid, synth.T_SCALE), N, G, s)
+        packed = torch.empty(w4.w4_packed_bytes(N, K), dtype=torch.uint8, device=dev)
+        ws.append(w4.w4_pack(q, s, N, K, packed))
+        keep.append(packed)
+        layer += 1
+    x = st["xs"][idx[0]]
+    y = torch.zeros((1, N), dtype=torch.int16, device=dev)
+    k = [0]
+
+    def one():
+        w4.w4a16_gemv(x, ws[k[0] % copies], y, 1)
+        k[0] += 1
+
+    for _ in range(2 * copies):
+        one()
+    spread = replay_spread(torch, one, reps * copies)
+    nb = (N * K) // 2 + N * G * 2
+    return {"copies": copies, "bytes_per_copy": nb, "rotated_bytes": nb * copies,
+            "us_per_gemv": spread["median_us"], "GB/s": nb / (spread["median_us"] * 1e-6) / 1e9,
+            "spread": spread, "launch": "w4a16_gemv (decode kernel, library launch shape), one stream, back to back"}
+
+
 def small_batch_sweep(torch, w4, synth, st, Ms=(2, 4, 8, 16), reps=50):
     """The full 112-projection step at M tokens (same weights): us/step and
     weight GB/s; weight bytes are read once per step whatever M."""
@@ -352,7 +429,8 @@ def small_batch_sweep(torch, w4, synth, st, Ms=(2, 4, 8, 16), reps=50):
                 seq.replay()
             ms = time_replays(torch, seq.replay, reps)
             entry[mode] = {"us_per_step": ms * 1e3, "GB/s": BYTES_PER_STEP / (ms * 1e-3) / 1e9,
-                           "frac_of_hbm": BYTES_PER_STEP / (ms * 1e-3) / 1e9 / peak}
+                           "frac_of_hbm": BYTES_PER_STEP / (ms * 1e-3) / 1e9 / peak,
+                           "spread": replay_spread(torch, seq.replay, reps)}
             if mode == "persistent":
                 entry[mode]["status_word"] = seq.status()
             seq.close()
@@ -380,7 +458,13 @@ def prefill_layer(torch, w4, synth, st, M=512, layers=4, reps=5):
         run()
         ms = time_replays(torch, run, reps) / len(idx)
         tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        k = [0]
+
+        def one():
+            w4.w4a16_gemm(x, st["ws"][idx[k[0] % len(idx)]], y, M, wsb, nb)
+            k[0] += 1
         out[name] = {"us": ms * 1e3, "TFLOP/s": tf, "frac_of_dense_peak": tf / peak,
+                     "spread": replay_spread(torch, one, 50),
                      "status_word": int(wsb[:4].view(torch.int32).item())}
     tot_us = sum(v["us"] for v in out.values())
     out["layer"] = {"us": tot_us, "TFLOP/s": 2.0 * M * sum(N * K for _, N, K in LAYER) / (tot_us * 1e-6) / 1e12,
@@ -650,6 +734,8 @@ def main():
             one.close()
             del wb1
         extras["per_projection_persistent_chain_28_layers"] = perp
+        extras["step_replay_spread_M1"] = replay_spread(torch, seq.replay, 100)
+        extras["single_gemv_qkv_M1_rotated"] = single_gemv_rotated(torch, w4, synth, st)
         extras["small_batch_step"] = small_batch_sweep(torch, w4, synth, st)
         extras["prefill_M512"] = prefill_layer(torch, w4, synth, st)
         extras["packed_file_layer0"] = packed_file_load(torch, w4, st)
@@ -673,6 +759,7 @@ def main():
     if rank == 0 and not args.no_extras:
         import oracle
         cpu = cpu_baseline(oracle, synth)
+        extras["cpu_oracle_single_gemv_one_thread"] = cpu_single_gemv_one_thread(oracle, synth)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

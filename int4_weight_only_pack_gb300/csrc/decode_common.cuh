@@ -227,6 +227,51 @@ __device__ __forceinline__ void sum_groups(const uint32_t* xs, float* xsum, int 
     }
 }
 
+// Sum x over every group gl < Gs and token m < M of a natural-order slice
+// (token rows of row_w words) into xsum[gl * xsum_stride(MP) + m]: eight
+// threads per (group, token) pair, each adding its 16 consecutive values in a
+// fixed order, then a three-step butterfly over the eight.  The work is spread
+// over every thread whatever M is (a warp per pair left most lanes of a
+// butterfly idle at 8 and 16 tokens).
+template <int MP, int NCONS, int ACT>
+__device__ __forceinline__ void sum_groups_nat(const uint32_t* xs, float* xsum, int M, int Gs, int row_w) {
+    const int tid = threadIdx.x, sub = tid & 7;
+    const int pairs = Gs * M;
+    constexpr int kStep = NCONS / 8;  // pairs per pass
+    // pair p = gl * M + m, walked without dividing by M: (gl, m) advance together
+    int gl = 0, m = tid >> 3;
+    while (m >= M) {
+        m -= M;
+        ++gl;
+    }
+    // every lane runs every pass (the butterflies need the whole warp); lanes past the end add nothing
+    for (int base = 0; base < pairs; base += kStep) {
+        const bool live = base + (tid >> 3) < pairs;
+        float sum = 0.f;
+        if (live) {
+            const uint4* src = reinterpret_cast<const uint4*>(xs + m * row_w + gl * 64 + sub * 8);
+            const uint4 a = src[0], b = src[1];
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            float t[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float2 f = ActOps<ACT>::to_float2(w[k]);
+                t[k] = f.x + f.y;
+            }
+            sum = ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+        }
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+        if (live && sub == 0) xsum[gl * xsum_stride(MP) + m] = sum;
+        m += kStep;
+        while (m >= M) {
+            m -= M;
+            ++gl;
+        }
+    }
+}
+
 // The same staging as stage_x, with every 8-byte piece (the b0, b1 words of
 // one lane class and k16 step) copied from global memory straight into its
 // fragment slot by a cp.async, all issued before any is waited for: one
@@ -297,10 +342,7 @@ __device__ __forceinline__ bool stage_x_bulk(const uint32_t* x, int M, int K, in
         xs[m * row_w + w] = 0;
     }
     const bool ok = tc::mbar_wait(bar, phase);
-    const int q = lane >> 3, c = (lane >> 1) & 3, e = (lane & 1) * 2;
-    const int st = 2 * q + (e >> 1);  // k16 step; the lane's k are 4c .. 4c+3 of it
-    sum_groups<MP, kWarps, ACT>(xs, xsum, M, Gs, warp, lane,
-                                [&](int gl, int m) { return m * row_w + gl * 64 + st * 8 + c * 2; });
+    sum_groups_nat<MP, NCONS, ACT>(xs, xsum, M, Gs, row_w);
     tc::named_barrier(1, NCONS);
     return ok;
 }

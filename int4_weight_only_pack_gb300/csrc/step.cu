@@ -289,6 +289,9 @@ __device__ __forceinline__ bool combine_splits(const StepOp& o, int band, int r,
             emit(row, m, sum);
         });
     } else {
+    // (row, token) of output idx = row * M + m without an integer division: idx < 256, so the float
+    // quotient, truncated, is exact
+    const float inv_m = 1.f / (float)M;
     for (int o0 = 0; o0 < pb; o0 += 32 * kCombineOut) {
         float sum[kCombineOut];
 #pragma unroll
@@ -311,7 +314,10 @@ __device__ __forceinline__ bool combine_splits(const StepOp& o, int band, int r,
 #pragma unroll
         for (int j = 0; j < kCombineOut; ++j) {
             const int idx = o0 + 32 * j + lane;
-            if (idx < pb) emit(idx / M, idx % M, sum[j]);
+            if (idx < pb) {
+                const int row = __float2int_rz(((float)idx + 0.5f) * inv_m);
+                emit(row, idx - row * M, sum[j]);
+            }
         }
     }
     }
