@@ -512,11 +512,38 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 }
             }
             __syncthreads();
-            // a band cut between warps is added up, in warp order, by the
-            // lowest warp whose range starts strictly inside it (warp - 1
-            // then holds the band's first tile)
             const int bs = u_first * q.Gs, be = bs + q.Gs;
-            if (warp > 0 && t0 < Tc && t0 != bs && warp_lo(Tc, warp - 1) <= bs) {
+            if (MP >= 8 && o.S == 1 && !(o.flags & W4_OP_SWIGLU)) {
+                // a plain band cut between warps is added up, in warp order, by every warp whose range
+                // begins inside it, each taking every nh-th batch of 32 outputs (the others are idle here;
+                // measured slower below 8 tokens, where a band has at most 64 outputs)
+                if (t0 < t1 && !(bs == t0 && be <= t1)) {
+                    int hidx = 0, nh = 0, wa = 0;
+#pragma unroll
+                    for (int w2 = 0; w2 < kWarps; ++w2) {
+                        const int lo = warp_lo(Tc, w2), hi = warp_lo(Tc, w2 + 1);
+                        if (lo < hi && lo >= bs && lo < be) {
+                            hidx += w2 < warp;
+                            ++nh;
+                        }
+                        if (lo < hi && lo <= bs) wa = w2;  // the warp holding the band's first tile
+                    }
+                    for (int oi = lane + 32 * hidx; oi < 16 * MP; oi += 32 * nh) {
+                        const int row = oi / MP, m = oi % MP;  // MP is a power of two: shifts
+                        if (m >= M) continue;
+                        float sum = 0.f;
+                        for (int w2 = wa; w2 < kWarps; ++w2) {
+                            const int lo = warp_lo(Tc, w2), hi = warp_lo(Tc, w2 + 1);
+                            if (lo >= be) break;
+                            if (lo < hi) sum += park[(w2 * PS + (lo >= bs ? 0 : 1)) * PB + row * MP + m];
+                        }
+                        const int n0 = (q.ub + u_first) * 16;
+                        if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = dec::ActOps<ACT>::round(sum);
+                    }
+                }
+            } else if (warp > 0 && t0 < Tc && t0 != bs && warp_lo(Tc, warp - 1) <= bs) {
+                // a split or gated band cut between warps is added up, in warp order, by the lowest warp
+                // whose range starts strictly inside it (warp - 1 then holds the band's first tile)
                 finish_band<ACT, MP>(o, q.ub + u_first, q.r, M, lane, [&](auto&& f) {
                     // outputs strided by the padded token count (a power of two: no division)
                     for (int oi = lane; oi < 16 * MP; oi += 32) {
