@@ -134,62 +134,6 @@ __host__ __device__ constexpr int xsum_bytes(int MP, int Gs) {
     return ((Gs * xsum_stride(MP) + 8 + 16) * 4 + 15) & ~15;  // + 16 floats: per-token scales (INT8 path)
 }
 
-// Stage x[0:M, 128*g_lo : 128*(g_lo+Gs)) (fp16 pairs; row stride K/2 words)
-// into `xs` in fragment order -- word (gl, q, m, c, e) at
-// gl*MP*64 + q*MP*16 + (m*4 + c)*4 + e holds k16 step 2q + (e >> 1) of group
-// gl, k 4c + 2(e & 1) .. +1 -- with rows M..MP-1 zero, and the sum of x over
-// every group and token m < M into xsum[gl*xsum_stride(MP) + m].  Called by the
-// consumer threads only; returns with all of them synchronised.
-template <int MP, int NCONS = kConsumers>
-__device__ __forceinline__ void stage_x(const uint32_t* x, int M, int K, int g_lo, int Gs, uint32_t* xs,
-                                        float* xsum) {
-    constexpr int kConsumers = NCONS, kConsumerWarps = NCONS / 32;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int per_row = Gs * 64;  // fp16 pairs of this K range
-    const uint32_t* xg = x + (size_t)g_lo * 64;
-    const int kp = K / 2;
-    const int total = MP * per_row;
-    // eight independent loads in flight per thread, then the stores
-    for (int base = tid; base < total; base += 8 * kConsumers) {
-        uint32_t v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int idx = base + u * kConsumers;
-            v[u] = 0;
-            if (idx < total) {
-                const int m = idx / per_row, r = idx - m * per_row;
-                if (m < M) v[u] = __ldcg(xg + (size_t)m * kp + r);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int idx = base + u * kConsumers;
-            if (idx < total) {
-                const int m = idx / per_row, r = idx - m * per_row;
-                // pair kk2 of the group = k 2*kk2, 2*kk2+1; lane class c owns
-                // k 4c..4c+3 of each k16 step (lower pair is b0, upper b1)
-                const int gl = r >> 6, kk2 = r & 63;
-                const int j = kk2 >> 3, c = (kk2 >> 1) & 3, hi = kk2 & 1;
-                xs[gl * (MP * 64) + (j >> 1) * (MP * 16) + (m * 4 + c) * 4 + (j & 1) * 2 + hi] = v[u];
-            }
-        }
-    }
-    tc::named_barrier(1, kConsumers);
-    // FP32 sums in a fixed order: four values per lane, then a butterfly
-    for (int idx = warp; idx < Gs * M; idx += kConsumerWarps) {
-        const int gl = idx / M, m = idx - gl * M;
-        const int q = lane >> 3, c = (lane >> 1) & 3, e = (lane & 1) * 2;
-        const uint32_t* src = xs + gl * (MP * 64) + q * (MP * 16) + (m * 4 + c) * 4 + e;
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(src));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(src + 1));
-        float sum = (f0.x + f0.y) + (f1.x + f1.y);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-        if (lane == 0) xsum[gl * xsum_stride(MP) + m] = sum;
-    }
-    tc::named_barrier(1, kConsumers);
-}
-
 // Sum x over every group gl < Gs and token m < M into xsum[gl *
 // xsum_stride(MP) + m], each lane adding the four values at word offsets
 // word(gl, m) and word(gl, m) + 1 (the layout's fragment positions of lane
@@ -272,10 +216,17 @@ __device__ __forceinline__ void sum_groups_nat(const uint32_t* xs, float* xsum, 
     }
 }
 
-// The same staging as stage_x, with every 8-byte piece (the b0, b1 words of
-// one lane class and k16 step) copied from global memory straight into its
-// fragment slot by a cp.async, all issued before any is waited for: one
-// memory round trip whatever the slice size.  x must be 8-byte aligned.
+// Stage x[0:M, 128*g_lo : 128*(g_lo+Gs)) (fp16 pairs; row stride K/2 words)
+// into `xs` in fragment order -- word (gl, q, m, c, e) at
+// gl*MP*64 + q*MP*16 + (m*4 + c)*4 + e holds k16 step 2q + (e >> 1) of group
+// gl, k 4c + 2(e & 1) .. +1 -- with rows M..MP-1 zero, and the sum of x over
+// every group and token m < M into xsum[gl*xsum_stride(MP) + m].  Every
+// 8-byte piece (the b0, b1 words of one lane class and k16 step) is copied
+// from global memory straight into its fragment slot by a cp.async, all
+// issued before any is waited for: one memory round trip whatever the slice
+// size (synchronous loads, eight in flight per thread, took 2.6-4 us per
+// decode-kernel launch).  Called by the NCONS threads tid < NCONS; returns
+// with them synchronised.  x must be 8-byte aligned.
 template <int MP, int NCONS, int ACT = kActF16>
 __device__ __forceinline__ void stage_x_async(const uint32_t* x, int M, int K, int g_lo, int Gs, uint32_t* xs,
                                               float* xsum) {

@@ -166,8 +166,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(GemvParams p) {
         // ---- consumers -----------------------------------------------------------
         // x may be produced by the previous kernel on the stream: read it only now.
         pdl_wait();
-        dec::stage_x<MP>(p.x, M, p.K, g_lo, Gs, reinterpret_cast<uint32_t*>(smem + L.x),
-                         reinterpret_cast<float*>(smem + L.xsum));
+        dec::stage_x_async<MP, dec::kConsumers>(p.x, M, p.K, g_lo, Gs, reinterpret_cast<uint32_t*>(smem + L.x),
+                                                reinterpret_cast<float*>(smem + L.xsum));
         // everything this CTA's consumers read from the previous grid is read
         pdl_launch_dependents();
 
