@@ -72,15 +72,23 @@ __device__ __forceinline__ void mma16816_bf_zero(float (&c)[4], const uint32_t (
 //   sum_k x * q = kLo * D - kBias * sum_k x      (kHi for rows r + 8)
 //  * binary16: nibbles as exact subnormals u * 2^-24 (rows r) and u * 2^-20
 //    (rows r + 8), 5 integer ops per word; kLo = 2^24, kHi = 2^20, kBias = 8.
-//  * bfloat16: a subnormal product would fall below FP32's normal range, so
-//    every nibble is moved to bits 0..3 of its half and OR-ed with the
-//    exponent of 128: the exact bfloat16 value 128 + u = q + 136 (7 integer
-//    ops per word); kLo = kHi = 1, kBias = 136.
+//  * bfloat16: x is rescaled per (group, token) by a power of two 2^e that
+//    puts the group's largest |x| in [2^14, 2^15), rounded to binary16 in
+//    shared memory when it is staged, and then takes the binary16 path (the
+//    5-op unpack; a bfloat16 unpack needs 7 ops per word, since a bfloat16
+//    subnormal product would fall below FP32's normal range: that cost the
+//    28-layer one-token step 1129 against 908 us).  Every x within 2^-28 of
+//    its group's largest magnitude converts exactly (binary16 holds 11
+//    significant bits to bfloat16's 8); smaller ones round to a multiple of
+//    2^-24 * 2^-e, at most 2^-40 of the group's largest |x| away.  The group
+//    partial is c' * D + d with c' = 2^(24-e) (2^(20-e) for rows r + 8) and
+//    d = -8 * 2^-e * sum_k x', both per (group, token) from the staging.
 template <int ACT>
 struct ActOps;
 template <>
 struct ActOps<kActF16> {
     static constexpr float kLo = 16777216.f, kHi = 1048576.f, kBias = 8.f;
+    static constexpr bool kScaled = false;
     __device__ static __forceinline__ float2 to_float2(uint32_t v) {
         return __half22float2(*reinterpret_cast<const __half2*>(&v));
     }
@@ -95,31 +103,20 @@ struct ActOps<kActF16> {
     }
 };
 template <>
-struct ActOps<kActBF16> {
-    static constexpr float kLo = 1.f, kHi = 1.f, kBias = 136.f;
+struct ActOps<kActBF16> : ActOps<kActF16> {
+    static constexpr bool kScaled = true;  // x staged as rescaled binary16 (above)
+    // the staged input's pairs (before rescaling)
     __device__ static __forceinline__ float2 to_float2(uint32_t v) {
         return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
     }
     __device__ static __forceinline__ uint16_t round(float v) {
         return __bfloat16_as_ushort(__float2bfloat16_rn(v));
     }
-    __device__ static __forceinline__ void unpack(uint32_t v, uint32_t (&a)[4]) {
-        a[0] = (v & 0x000F000Fu) | 0x43004300u;          // rows r,     k 4c, 4c+1
-        a[1] = ((v >> 4) & 0x000F000Fu) | 0x43004300u;   // rows r + 8, k 4c, 4c+1
-        a[2] = ((v >> 8) & 0x000F000Fu) | 0x43004300u;   // rows r,     k 4c+2, 4c+3
-        a[3] = ((v >> 12) & 0x000F000Fu) | 0x43004300u;  // rows r + 8, k 4c+2, 4c+3
-    }
-    __device__ static __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
-                                               bool first) {
-        if (first)
-            mma16816_bf_zero(c, a, b0, b1);
-        else
-            mma16816_bf(c, a, b0, b1);
-    }
 };
 
 template <>
 struct ActOps<kActI8> {
+    static constexpr bool kScaled = false;
     __device__ static __forceinline__ uint16_t round(float v) { return __half_as_ushort(__float2half_rn(v)); }
 };
 
@@ -130,8 +127,30 @@ struct ActOps<kActI8> {
 // sizes are multiples of 16 bytes, so what follows them stays 16-byte aligned.
 __host__ __device__ constexpr int x_bytes(int MP, int Gs) { return MP * Gs * 256; }
 __host__ __device__ constexpr int xsum_stride(int MP) { return MP < 2 ? 2 : MP; }
-__host__ __device__ constexpr int xsum_bytes(int MP, int Gs) {
-    return ((Gs * xsum_stride(MP) + 8 + 16) * 4 + 15) & ~15;  // + 16 floats: per-token scales (INT8 path)
+// Rescaled binary16 x (bfloat16 input): per group d for tokens m at
+// xsum[gl * xsum_gstride + m] and c' at + xsum_cofs (at one token the pair
+// (d, c') fills the slot of the token and its padding neighbour).
+__host__ __device__ constexpr int xsum_gstride(int MP, bool scaled) {
+    return scaled && MP > 1 ? 2 * xsum_stride(MP) : xsum_stride(MP);
+}
+__host__ __device__ constexpr int xsum_cofs(int MP) { return MP > 1 ? xsum_stride(MP) : 1; }
+__host__ __device__ constexpr int xsum_bytes(int MP, int Gs, bool scaled = false) {
+    return ((Gs * xsum_gstride(MP, scaled) + 8 + 16) * 4 + 15) & ~15;  // + 16 floats: per-token scales (INT8 path)
+}
+
+// The power of two 2^e of a (group, token) of rescaled x, from the largest
+// magnitude amax: e = 14 - floor(log2 amax), so that amax * 2^e lies in
+// [2^14, 2^15), clamped to [-103, 126] (zero groups take 126).  Returns
+// 2^e; c1 = 2^(24-e), the group's c' for rows r.
+__device__ __forceinline__ float x_scale_of(float amax, float& c1) {
+    const int E = (__float_as_int(amax) >> 23) & 0xFF;  // biased exponent of amax (0 for zero)
+    const int e = min(126, max(-103, 141 - E));
+    c1 = __int_as_float((151 - e) << 23);
+    return __int_as_float((127 + e) << 23);
+}
+__device__ __forceinline__ uint32_t to_half2_bits(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Sum x over every group gl < Gs and token m < M into xsum[gl *
@@ -142,21 +161,62 @@ __host__ __device__ constexpr int xsum_bytes(int MP, int Gs) {
 // layout.  Warp w takes groups w, w + NW, ...; four groups' reductions are
 // interleaved, and no index is divided by the run-time token count.
 template <int MP, int NW, int ACT, typename Word>
-__device__ __forceinline__ void sum_groups(const uint32_t* xs, float* xsum, int M, int Gs, int warp, int lane,
+__device__ __forceinline__ void sum_groups(uint32_t* xs, float* xsum, int M, int Gs, int warp, int lane,
                                            Word&& word) {
     constexpr int kBatch = 4;
+    constexpr bool kScaled = ActOps<ACT>::kScaled;
+    constexpr int kG = xsum_gstride(MP, kScaled);
     for (int g0 = warp; g0 < Gs; g0 += NW * kBatch) {
         for (int m = 0; m < M; ++m) {
-            float sum[kBatch];
+            float sum[kBatch], c1[kBatch];
+            if constexpr (kScaled) {
+                // rescale each group by its power of two and round to binary16 in place: the four
+                // groups' maxima first (their butterflies interleaved), then the conversions
+                float2 f[kBatch][2], amax[kBatch];
 #pragma unroll
-            for (int b = 0; b < kBatch; ++b) {
-                const int gl = g0 + b * NW;
-                sum[b] = 0.f;
-                if (gl < Gs) {
-                    const uint32_t* src = xs + word(gl, m);
-                    const float2 f0 = ActOps<ACT>::to_float2(src[0]);
-                    const float2 f1 = ActOps<ACT>::to_float2(src[1]);
-                    sum[b] = (f0.x + f0.y) + (f1.x + f1.y);
+                for (int b = 0; b < kBatch; ++b) {
+                    const int gl = g0 + b * NW;
+                    f[b][0] = f[b][1] = make_float2(0.f, 0.f);
+                    if (gl < Gs) {
+                        const uint32_t* src = xs + word(gl, m);
+                        f[b][0] = ActOps<ACT>::to_float2(src[0]);
+                        f[b][1] = ActOps<ACT>::to_float2(src[1]);
+                    }
+                    amax[b].x = fmaxf(fmaxf(fabsf(f[b][0].x), fabsf(f[b][0].y)),
+                                      fmaxf(fabsf(f[b][1].x), fabsf(f[b][1].y)));
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                    for (int b = 0; b < kBatch; ++b)
+                        amax[b].x = fmaxf(amax[b].x, __shfl_xor_sync(0xFFFFFFFFu, amax[b].x, off));
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    const int gl = g0 + b * NW;
+                    const float sc = x_scale_of(amax[b].x, c1[b]);
+                    const uint32_t h0 = to_half2_bits(f[b][0].x * sc, f[b][0].y * sc);
+                    const uint32_t h1 = to_half2_bits(f[b][1].x * sc, f[b][1].y * sc);
+                    sum[b] = 0.f;
+                    if (gl < Gs) {
+                        uint32_t* dst = xs + word(gl, m);
+                        dst[0] = h0;
+                        dst[1] = h1;
+                        const float2 e0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
+                        const float2 e1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+                        sum[b] = (e0.x + e0.y) + (e1.x + e1.y);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    const int gl = g0 + b * NW;
+                    sum[b] = 0.f;
+                    if (gl < Gs) {
+                        const uint32_t* src = xs + word(gl, m);
+                        const float2 f0 = ActOps<ACT>::to_float2(src[0]);
+                        const float2 f1 = ActOps<ACT>::to_float2(src[1]);
+                        sum[b] = (f0.x + f0.y) + (f1.x + f1.y);
+                    }
                 }
             }
 #pragma unroll
@@ -166,7 +226,14 @@ __device__ __forceinline__ void sum_groups(const uint32_t* xs, float* xsum, int 
             if (lane == 0)
 #pragma unroll
                 for (int b = 0; b < kBatch; ++b)
-                    if (g0 + b * NW < Gs) xsum[(g0 + b * NW) * xsum_stride(MP) + m] = sum[b];
+                    if (g0 + b * NW < Gs) {
+                        if constexpr (kScaled) {  // d = -8 * 2^-e * sum, c' = 2^(24-e)
+                            xsum[(g0 + b * NW) * kG + m] = -sum[b] * c1[b] * 0x1p-21f;
+                            xsum[(g0 + b * NW) * kG + xsum_cofs(MP) + m] = c1[b];
+                        } else {
+                            xsum[(g0 + b * NW) * kG + m] = sum[b];
+                        }
+                    }
         }
     }
 }
@@ -178,7 +245,9 @@ __device__ __forceinline__ void sum_groups(const uint32_t* xs, float* xsum, int 
 // over every thread whatever M is (a warp per pair left most lanes of a
 // butterfly idle at 8 and 16 tokens).
 template <int MP, int NCONS, int ACT>
-__device__ __forceinline__ void sum_groups_nat(const uint32_t* xs, float* xsum, int M, int Gs, int row_w) {
+__device__ __forceinline__ void sum_groups_nat(uint32_t* xs, float* xsum, int M, int Gs, int row_w) {
+    constexpr bool kScaled = ActOps<ACT>::kScaled;
+    constexpr int kG = xsum_gstride(MP, kScaled);
     const int tid = threadIdx.x, sub = tid & 7;
     const int pairs = Gs * M;
     constexpr int kStep = NCONS / 8;  // pairs per pass
@@ -191,15 +260,42 @@ __device__ __forceinline__ void sum_groups_nat(const uint32_t* xs, float* xsum, 
     // every lane runs every pass (the butterflies need the whole warp); lanes past the end add nothing
     for (int base = 0; base < pairs; base += kStep) {
         const bool live = base + (tid >> 3) < pairs;
-        float sum = 0.f;
+        float sum = 0.f, c1 = 0.f;
+        uint4* src = reinterpret_cast<uint4*>(xs + m * row_w + gl * 64 + sub * 8);
+        uint4 a = make_uint4(0, 0, 0, 0), b = a;
         if (live) {
-            const uint4* src = reinterpret_cast<const uint4*>(xs + m * row_w + gl * 64 + sub * 8);
-            const uint4 a = src[0], b = src[1];
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            float t[8];
+            a = src[0];
+            b = src[1];
+        }
+        uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        if constexpr (kScaled) {
+            // rescale by the (group, token)'s power of two and round to binary16 in place
+            float amax = 0.f;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const float2 f = ActOps<ACT>::to_float2(w[k]);
+                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+            const float sc = x_scale_of(amax, c1);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float2 f = ActOps<ACT>::to_float2(w[k]);
+                w[k] = to_half2_bits(f.x * sc, f.y * sc);
+            }
+            if (live) {
+                src[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                src[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+        }
+        if (live) {
+            float t[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float2 f = kScaled ? __half22float2(*reinterpret_cast<const __half2*>(&w[k]))
+                                         : ActOps<ACT>::to_float2(w[k]);
                 t[k] = f.x + f.y;
             }
             sum = ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
@@ -207,7 +303,14 @@ __device__ __forceinline__ void sum_groups_nat(const uint32_t* xs, float* xsum, 
         sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
         sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
         sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-        if (live && sub == 0) xsum[gl * xsum_stride(MP) + m] = sum;
+        if (live && sub == 0) {
+            if constexpr (kScaled) {  // d = -8 * 2^-e * sum, c' = 2^(24-e)
+                xsum[gl * kG + m] = -sum * c1 * 0x1p-21f;
+                xsum[gl * kG + xsum_cofs(MP) + m] = c1;
+            } else {
+                xsum[gl * kG + m] = sum;
+            }
+        }
         m += kStep;
         while (m >= M) {
             m -= M;
@@ -334,7 +437,8 @@ struct TileMac {
     uint32_t xsum;                           // this lane's token pair's sums of group 0
     uint32_t xl, sl;                         // load predicates: x fragments, group sums
     uint4 xv[4][NT];                         // x fragments of up to four tiles
-    float2 X[4][NT];                         // group sums of up to four tiles
+    float2 X[4][NT];                         // group sums (rescaled x: d) of up to four tiles
+    float2 C[Ops::kScaled && MP > 1 ? 4 : 1][NT];  // rescaled x, two or more tokens: c' of the token pair
     int xrow = 0;                            // natural x layout: bytes per token row
 
     __device__ __forceinline__ TileMac(uint32_t x_smem, uint32_t xsum_smem, int lane, int /*Gs*/ = 0) {
@@ -350,6 +454,10 @@ struct TileMac {
                 xv[n][nt] = make_uint4(0, 0, 0, 0);
                 X[n][nt] = make_float2(0.f, 0.f);
             }
+#pragma unroll
+        for (int n = 0; n < (Ops::kScaled && MP > 1 ? 4 : 1); ++n)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) C[n][nt] = make_float2(0.f, 0.f);
     }
 
     // Read x from the natural layout of stage_x_bulk (rows of row_bytes)
@@ -376,9 +484,13 @@ struct TileMac {
             wd[n][0] = lo.x, wd[n][1] = lo.y, wd[n][2] = lo.z, wd[n][3] = lo.w;
             wd[n][4] = hi.x, wd[n][5] = hi.y, wd[n][6] = hi.z, wd[n][7] = hi.w;
             sc[n] = lds32(tn + kScaleOffset + 4 * (lane >> 2));
+            constexpr int kG = xsum_gstride(MP, Ops::kScaled);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                lds64f_if(X[n][nt], xsum + (uint32_t)(((gl + n) * xsum_stride(MP) + nt * 8) * 4), sl);
+            for (int nt = 0; nt < NT; ++nt) {
+                lds64f_if(X[n][nt], xsum + (uint32_t)(((gl + n) * kG + nt * 8) * 4), sl);
+                if constexpr (Ops::kScaled && MP > 1)
+                    lds64f_if(C[n][nt], xsum + (uint32_t)(((gl + n) * kG + xsum_cofs(MP) + nt * 8) * 4), sl);
+            }
         }
         const uint32_t xa0 = NAT ? xfrag + (uint32_t)gl * 256 : xfrag + (uint32_t)gl * (MP * 256);
         float pe[NTL][NT][4], po[NTL][NT][4];
@@ -414,9 +526,20 @@ struct TileMac {
             for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
                 for (int e = 0; e < NE; ++e) {
-                    const float mbx = -Ops::kBias * (e ? X[n][nt].y : X[n][nt].x);
-                    acc[nt][e] = fmaf(s.x, fmaf(Ops::kLo, pe[n][nt][e] + po[n][nt][e], mbx), acc[nt][e]);
-                    acc[nt][2 + e] = fmaf(s.y, fmaf(Ops::kHi, pe[n][nt][2 + e] + po[n][nt][2 + e], mbx), acc[nt][2 + e]);
+                    if constexpr (Ops::kScaled) {
+                        // d and c' of the token: at one token the pair (d, c') of the group's slot
+                        const float d = e ? X[n][nt].y : X[n][nt].x;
+                        const float c1 = MP == 1 ? X[n][nt].y : (e ? C[n % (MP > 1 ? 4 : 1)][nt].y
+                                                                   : C[n % (MP > 1 ? 4 : 1)][nt].x);
+                        acc[nt][e] = fmaf(s.x, fmaf(c1, pe[n][nt][e] + po[n][nt][e], d), acc[nt][e]);
+                        acc[nt][2 + e] =
+                            fmaf(s.y, fmaf(c1 * 0.0625f, pe[n][nt][2 + e] + po[n][nt][2 + e], d), acc[nt][2 + e]);
+                    } else {
+                        const float mbx = -Ops::kBias * (e ? X[n][nt].y : X[n][nt].x);
+                        acc[nt][e] = fmaf(s.x, fmaf(Ops::kLo, pe[n][nt][e] + po[n][nt][e], mbx), acc[nt][e]);
+                        acc[nt][2 + e] =
+                            fmaf(s.y, fmaf(Ops::kHi, pe[n][nt][2 + e] + po[n][nt][2 + e], mbx), acc[nt][2 + e]);
+                    }
                 }
             }
         }

@@ -85,6 +85,14 @@ constexpr int kMaxRing = 32;             // slots per warp (one mbarrier per lan
 constexpr int kSplitPenalty = 64;        // tiles: the cost of combining K-split partials (~2 us of streaming),
                                          // plus 4 per split
 constexpr int kMaxCtaTiles = 1 << 22;    // per-CTA tiles of one projection (float division below)
+// From 8 tokens on, a K-split projection is finished in two phases: every CTA
+// stores its FP32 partials with plain stores and counts itself on the
+// projection's counter; once all have, each CTA adds up an equal share of the
+// bands (split order) and writes y.  One more grid-wide wait per projection,
+// but no fence and atomic per band, and no CTA left holding the combines of
+// whichever bands it happened to complete last.
+constexpr int16_t kOpTwoPhase = 0x4000;  // internal flag bit of StepOp::flags
+constexpr int kTwoPhaseMinMP = 8;
 // x slice + its group sums: small for one or two tokens so that the rings keep
 // three slots per warp; 60 KB from 3 tokens on, where a K = 3584 projection
 // needs no K split up to 8 tokens and two at 16 (the partials cost far more
@@ -107,14 +115,14 @@ __host__ __device__ constexpr int step_x_bytes(int MP, int Gs) {
 
 struct StepSmem {
     int R, bar, xbar, geo, x, xsum, park, total;
-    __host__ __device__ StepSmem(int R_, int MP, int gpc_max, int nops, int shares) {
+    __host__ __device__ StepSmem(int R_, int MP, int gpc_max, int nops, int shares, bool scaled) {
         R = R_;
         bar = kWarps * R * kSlotTiles * kTileBytes;  // rings first: warp w's at w*R*4*1056
         xbar = bar + kWarps * R * 8;                 // x staging (natural layout only)
         geo = xbar + (step_x_natural(MP) ? 16 : 0);
         x = (geo + nops * 16 + 127) & ~127;
         xsum = x + step_x_bytes(MP, gpc_max);
-        park = xsum + dec::xsum_bytes(MP, gpc_max);
+        park = xsum + dec::xsum_bytes(MP, gpc_max, scaled);
         total = park + kWarps * shares * 16 * MP * 4;  // two parked shares (+ a finishing scratch) per warp
     }
 };
@@ -336,6 +344,11 @@ __device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, in
                                             float* scratch, int MP) {
     using Ops = dec::ActOps<ACT>;
     const int n0 = band * 16;
+    if (o.flags & kOpTwoPhase) {
+        float* mine = o.part + ((size_t)band * o.S + r) * (16 * M);
+        visit([&](int row, int m, float v) { mine[row * M + m] = v; });
+        return;
+    }
     if (!(o.flags & W4_OP_SWIGLU)) {
         auto to_y = [&](int row, int m, float v) {
             if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = Ops::round(v);
@@ -363,6 +376,58 @@ __device__ __forceinline__ void finish_band(const StepOp& o, int band, int r, in
     __syncwarp();
 }
 
+// Second phase of a two-phase projection: CTA c of NC adds up the partials of
+// bands [bands*c/NC, bands*(c+1)/NC), each output over its S splits in split
+// order, and writes y (a gated projection: silu(gate) * up of rows r and
+// r + 8 of each band).  Every thread takes outputs strided by the block, with
+// the loads of up to eight splits of an output in flight at once (batching
+// eight outputs per thread as well measured slower: 16 tokens 1813 -> 1930
+// us per step).
+template <int MP, int ACT, bool GATED>
+__device__ __forceinline__ void combine_share_of(const StepOp& o, int b0, int total, int M) {
+    using Ops = dec::ActOps<ACT>;
+    constexpr int kLogMP = MP == 1 ? 0 : MP == 2 ? 1 : MP == 4 ? 2 : MP == 8 ? 3 : 4;
+    constexpr int sh = (GATED ? 3 : 4) + kLogMP;  // outputs per band: (8 or 16 rows) x MP
+    const int pb = 16 * M, S = o.S;
+    for (int idx = threadIdx.x; idx < total; idx += kThreads) {
+        const int rem = idx & ((1 << sh) - 1), band = b0 + (idx >> sh);
+        const int row = rem >> kLogMP, m = rem & (MP - 1);
+        if (m >= M) continue;
+        const float* pp = o.part + (size_t)band * S * pb + row * M + m;
+        float g = 0.f, u = 0.f;
+        for (int s0 = 0; s0 < S; s0 += 8) {
+            float v[8], w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                v[e] = s0 + e < S ? __ldcg(pp + (size_t)(s0 + e) * pb) : 0.f;
+                if constexpr (GATED) w[e] = s0 + e < S ? __ldcg(pp + (size_t)(s0 + e) * pb + 8 * M) : 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (s0 + e < S) {  // the first split starts the sum: 0 + -0 would flip a zero's sign
+                    g = s0 + e == 0 ? v[e] : g + v[e];
+                    if constexpr (GATED) u = s0 + e == 0 ? w[e] : u + w[e];
+                }
+        }
+        if constexpr (!GATED) {
+            const int n = band * 16 + row;
+            if (n < o.N) o.y[(size_t)m * o.N + n] = Ops::round(g);
+        } else {
+            const int I = o.N / 2, n = band * 8 + row;
+            if (n < I) o.y[(size_t)m * I + n] = Ops::round(g / (1.f + expf(-g)) * u);
+        }
+    }
+}
+template <int MP, int ACT>
+__device__ __forceinline__ void combine_share(const StepOp& o, int c, int NC, int M) {
+    constexpr int kLogMP = MP == 1 ? 0 : MP == 2 ? 1 : MP == 4 ? 2 : MP == 8 ? 3 : 4;
+    const int b0 = (int)((long long)o.bands * c / NC), b1 = (int)((long long)o.bands * (c + 1) / NC);
+    if (o.flags & W4_OP_SWIGLU)
+        combine_share_of<MP, ACT, true>(o, b0, (b1 - b0) << (3 + kLogMP), M);
+    else
+        combine_share_of<MP, ACT, false>(o, b0, (b1 - b0) << (4 + kLogMP), M);
+}
+
 template <int MP, int ACT>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepArgs a) {
     constexpr int NT = (MP + 7) / 8;
@@ -372,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     const int NC = gridDim.x, c = blockIdx.x, M = a.M, nops = a.nops;
     // parked shares: 3 below 16 tokens, else from the table
     const int PS = MP >= 16 ? (a.ring >> 16) : 3;
-    const StepSmem L(MP >= 16 ? (a.ring & 0xFFFF) : a.ring, MP, a.gpc_max, nops, PS);
+    const StepSmem L(MP >= 16 ? (a.ring & 0xFFFF) : a.ring, MP, a.gpc_max, nops, PS, dec::ActOps<ACT>::kScaled);
     const int R = L.R;
     const uint32_t sbase = tc::smem_addr(smem);
     const uint32_t ring_w = sbase + (uint32_t)(warp * R * kSlotTiles * kTileBytes);
@@ -467,7 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     if (__all_sync(0xFFFFFFFFu, got)) {
                         --inflight;
                         static_assert(kSlotTiles == 4, "chunk cases below");
-                        if constexpr (MP >= 16) {  // register budget: at most two tiles at once
+                        // register budget: at most two tiles at once (16 tokens; 4 tokens of rescaled x)
+                        if constexpr (MP >= 16 || (MP == 4 && dec::ActOps<ACT>::kScaled)) {
                             if (n >= 2) mac.template run_tiles<2, kNat>(ta, gl, lane, acc);
                             if (n == 4) mac.template run_tiles<2, kNat>(ta + 2 * kTileBytes, gl + 2, lane, acc);
                             if (n & 1)
@@ -513,7 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             }
             __syncthreads();
             const int bs = u_first * q.Gs, be = bs + q.Gs;
-            if (MP >= 8 && o.S == 1 && !(o.flags & W4_OP_SWIGLU)) {
+            const bool two = o.flags & kOpTwoPhase;
+            if (MP >= 8 && (two || (o.S == 1 && !(o.flags & W4_OP_SWIGLU)))) {
                 // a plain band cut between warps is added up, in warp order, by every warp whose range
                 // begins inside it, each taking every nh-th batch of 32 outputs (the others are idle here;
                 // measured slower below 8 tokens, where a band has at most 64 outputs)
@@ -537,8 +604,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                             if (lo >= be) break;
                             if (lo < hi) sum += park[(w2 * PS + (lo >= bs ? 0 : 1)) * PB + row * MP + m];
                         }
-                        const int n0 = (q.ub + u_first) * 16;
-                        if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = dec::ActOps<ACT>::round(sum);
+                        if (two) {
+                            o.part[((size_t)(q.ub + u_first) * o.S + q.r) * (16 * M) + row * M + m] = sum;
+                        } else {
+                            const int n0 = (q.ub + u_first) * 16;
+                            if (n0 + row < o.N) o.y[(size_t)m * o.N + n0 + row] = dec::ActOps<ACT>::round(sum);
+                        }
                     }
                 }
             } else if (warp > 0 && t0 < Tc && t0 != bs && warp_lo(Tc, warp - 1) <= bs) {
@@ -564,6 +635,22 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         // thread's y stores before thread 0's fence, which makes them visible
         // before the completion count
         __syncthreads();
+        if (MP >= kTwoPhaseMinMP && (o.flags & kOpTwoPhase)) {
+            // the same for the partials, then wait for every CTA's and add up this CTA's share
+            if (threadIdx.x == 0) {
+                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(o.cnt) : "memory");
+                const long long t0 = clock64();
+                while (ld_acquire(o.cnt) < (unsigned)NC) {
+                    if (clock64() - t0 > (1ll << 31)) {
+                        atomicOr(a.status, 16);
+                        break;
+                    }
+                }
+            }
+            __syncthreads();
+            combine_share<MP, ACT>(o, c, NC, M);
+            __syncthreads();
+        }
         if (threadIdx.x == 0)
             asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.done + i) : "memory");
     }
@@ -581,7 +668,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     if (threadIdx.x == 0) {
         __threadfence();
         if (atomicAdd(a.exit_cnt, 1u) == (unsigned)(NC - 1)) {
-            for (int i = 0; i < nops; ++i) a.done[i] = 0;
+            for (int i = 0; i < nops; ++i) {
+                a.done[i] = 0;
+                if (a.ops[i].flags & kOpTwoPhase) *a.ops[i].cnt = 0;
+            }
             *a.exit_cnt = 0;
             __threadfence();
         }
@@ -625,13 +715,13 @@ struct StepPlan {
 // the x slice fits its budget, and the largest per-CTA share of tiles (plus a
 // fixed cost for combining partials when S > 1, plus the x slice's staging
 // for up to 4 tokens) is smallest.  0 if no split fits.
-static int choose_split(int bands, int G, int MP, int NC, int budget) {
+static int choose_split(int bands, int G, int MP, int NC, int budget, bool scaled) {
     int best = 0;
     long best_cost = LONG_MAX;
     for (int S = 1; S <= std::min(G, NC); ++S) {
         if (NC % S) continue;
         const int Gs = (G + S - 1) / S;
-        if (step_x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs) > budget) continue;
+        if (step_x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs, scaled) > budget) continue;
         const int cps = NC / S;
         // up to 4 tokens, staging the x slice (an L2 round trip plus ~3 tile-times per KB
         // under load) is counted too; from 8 tokens on, more splits cost more in partials
@@ -649,7 +739,8 @@ static int choose_split(int bands, int G, int MP, int NC, int budget) {
 // Splits, shared-memory sizing (the rings take what the rest leaves) and the
 // workspace layout for x slices of at most `budget` bytes and `shares` parked
 // partials per warp.  False if some projection cannot be planned.
-static bool plan_step_with(const w4_weight* w, int n, int M, int NC, int budget, int shares, StepPlan* pl) {
+static bool plan_step_with(const w4_weight* w, int n, int M, int NC, int budget, int shares, bool scaled,
+                           StepPlan* pl) {
     pl->MP = padded(M);
     pl->shares = shares;
     pl->NC = NC;
@@ -664,7 +755,7 @@ static bool plan_step_with(const w4_weight* w, int n, int M, int NC, int budget,
         o.K = (int)w[i].K;
         o.G = (int)(w[i].K / kGroupK);
         o.bands = (int)num_bands(w[i].N);
-        o.S = choose_split(o.bands, o.G, pl->MP, NC, budget);
+        o.S = choose_split(o.bands, o.G, pl->MP, NC, budget, scaled);
         if (o.S == 0) {
             fits = false;
             o.S = 1;
@@ -677,10 +768,10 @@ static bool plan_step_with(const w4_weight* w, int n, int M, int NC, int budget,
             fits = false;
         pl->gpc_max = std::max(pl->gpc_max, (o.G + o.S - 1) / o.S);
     }
-    const int fixed = StepSmem(0, pl->MP, pl->gpc_max, n, shares).total;
+    const int fixed = StepSmem(0, pl->MP, pl->gpc_max, n, shares, scaled).total;
     pl->R = std::min(kMaxRing, (kSmemBudget - fixed) / (kWarps * (kSlotTiles * kTileBytes + 8)));
-    while (pl->R > 0 && StepSmem(pl->R, pl->MP, pl->gpc_max, n, shares).total > kSmemBudget) --pl->R;
-    pl->smem = StepSmem(pl->R, pl->MP, pl->gpc_max, n, shares).total;
+    while (pl->R > 0 && StepSmem(pl->R, pl->MP, pl->gpc_max, n, shares, scaled).total > kSmemBudget) --pl->R;
+    pl->smem = StepSmem(pl->R, pl->MP, pl->gpc_max, n, shares, scaled).total;
     size_t off = 0;
     pl->done_off = off;
     off = align_up(off + sizeof(unsigned) * n);
@@ -707,10 +798,12 @@ static bool plan_step_with(const w4_weight* w, int n, int M, int NC, int budget,
 // keep two ring slots: 3689 -> 3418 us.  Below 16 tokens the kernel keeps
 // three shares as a constant (its code is unchanged there: a run-time share
 // count or ring mask measured 4-35 us slower at 1-8 tokens).
-static bool plan_step(const w4_weight* w, int n, int M, int NC, bool gated, StepPlan* pl) {
+static bool plan_step(const w4_weight* w, int n, int M, int NC, bool gated, int act, StepPlan* pl) {
     const int MP = padded(M), shares = (gated || MP < 16) ? 3 : 2;
-    if (plan_step_with(w, n, M, NC, x_budget(MP), shares, pl)) return true;
-    return x_budget_fallback(MP) != x_budget(MP) && plan_step_with(w, n, M, NC, x_budget_fallback(MP), shares, pl);
+    const bool scaled = act == dec::kActBF16;  // x staged as rescaled binary16: a second float per group sum
+    if (plan_step_with(w, n, M, NC, x_budget(MP), shares, scaled, pl)) return true;
+    return x_budget_fallback(MP) != x_budget(MP) &&
+           plan_step_with(w, n, M, NC, x_budget_fallback(MP), shares, scaled, pl);
 }
 
 // One resident CTA per SM, or 0 if the kernel cannot be resident.
@@ -722,19 +815,22 @@ static int step_grid(int MP, int act, int smem) {
     return per_sm >= 1 ? device_sm_count() : 0;
 }
 
-// Enough for the sequence with or without gated projections (the plans can
-// differ in their splits).
+// Enough for the sequence with or without gated projections and for every
+// activation type (the plans can differ in their splits).
 size_t step_workspace_bytes(const w4_weight* w, int n, int M) {
-    StepPlan plain, gated;
-    plan_step(w, n, M, device_sm_count(), false, &plain);
-    plan_step(w, n, M, device_sm_count(), true, &gated);
-    return std::max(plain.total, gated.total);
+    size_t most = 0;
+    for (int act : {(int)dec::kActF16, (int)dec::kActBF16, (int)dec::kActI8})
+        for (bool gated : {false, true}) {
+            StepPlan pl;
+            plan_step(w, n, M, device_sm_count(), gated, act, &pl);
+            most = std::max(most, pl.total);
+        }
+    return most;
 }
 
 void step_splits(const w4_weight* w, int n, int M, int act, bool gated, int* splits) {
-    (void)act;
     StepPlan pl;
-    plan_step(w, n, M, device_sm_count(), gated, &pl);
+    plan_step(w, n, M, device_sm_count(), gated, act, &pl);
     for (int i = 0; i < n; ++i) splits[i] = pl.ops[i].S;
 }
 
@@ -744,7 +840,7 @@ w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y,
     bool gated = false;
     for (int i = 0; i < n && op_flags; ++i) gated = gated || (op_flags[i] & W4_OP_SWIGLU);
     StepPlan pl;
-    if (!plan_step(w, n, M, device_sm_count(), gated, &pl)) {
+    if (!plan_step(w, n, M, device_sm_count(), gated, act, &pl)) {
         set_error("the persistent step kernel cannot take this sequence (%d projections; at most %d, and each "
                   "must fit its shared-memory and index limits)",
                   n, kMaxStepOps);
@@ -767,6 +863,7 @@ w4_status step_prepare(const w4_weight* w, const void* const* x, void* const* y,
     for (int i = 0; i < n; ++i) {
         StepOp& o = pl.ops[i];
         o.flags = (int16_t)(op_flags ? op_flags[i] : 0u);
+        if (o.S > 1 && pl.MP >= kTwoPhaseMinMP) o.flags |= kOpTwoPhase;
         o.w = static_cast<const uint8_t*>(w[i].data);
         o.x = static_cast<const uint32_t*>(x[i]);
         o.y = static_cast<uint16_t*>(y[i]);

@@ -293,7 +293,8 @@ def test_bf16_activation_type_is_checked():
     assert rc == 1 and not h.value  # W4_ERR_ARG, nothing created
 
 
-@pytest.mark.parametrize("M,act", [(1, "fp16"), (5, "fp16"), (16, "fp16"), (1, "bf16"), (3, "bf16")])
+@pytest.mark.parametrize("M,act", [(1, "fp16"), (5, "fp16"), (11, "fp16"), (16, "fp16"), (1, "bf16"), (3, "bf16"),
+                                   (8, "bf16")])
 def test_swiglu_projection_in_sequence(M, act):
     """Gated MLP projections (W4_OP_SWIGLU, weights from w4_pack_glu) mixed
     with plain ones in one persistent sequence, against the oracle's
