@@ -381,8 +381,7 @@ __host__ __device__ constexpr int x_bytes_nat(int MP, int Gs) { return MP * x_ro
 template <int MP, int NCONS, int ACT = kActF16>
 __device__ __forceinline__ bool stage_x_bulk(const uint32_t* x, int M, int K, int g_lo, int Gs, uint32_t* xs,
                                              float* xsum, uint32_t bar, uint32_t phase) {
-    constexpr int kWarps = NCONS / 32;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int row = x_row_bytes(Gs), row_w = row / 4;
     if (tid == 0) {
         tc::mbar_arrive_expect_tx(bar, (uint32_t)(M * Gs * 256));

@@ -418,11 +418,41 @@ __device__ __forceinline__ void combine_share_of(const StepOp& o, int b0, int to
         }
     }
 }
+// The same for two splits of a plain projection: every output's two loads,
+// for up to eight outputs per thread, in flight at once (at 16 tokens a
+// CTA's share of gate_up is about 4000 outputs: eight per thread).
+template <int MP, int ACT>
+__device__ __forceinline__ void combine_share_two(const StepOp& o, int b0, int total, int M) {
+    using Ops = dec::ActOps<ACT>;
+    constexpr int kLogMP = MP == 1 ? 0 : MP == 2 ? 1 : MP == 4 ? 2 : MP == 8 ? 3 : 4;
+    constexpr int sh = 4 + kLogMP, kOut = 8;
+    const int pb = 16 * M;
+    for (int r0 = threadIdx.x; r0 < total; r0 += kThreads * kOut) {
+        float v0[kOut], v1[kOut];
+#pragma unroll
+        for (int j = 0; j < kOut; ++j) {
+            const int idx = r0 + j * kThreads, rem = idx & ((1 << sh) - 1);
+            const int row = rem >> kLogMP, m = rem & (MP - 1);
+            const float* pp = o.part + (size_t)(b0 + (idx >> sh)) * 2 * pb + row * M + m;
+            const bool live = idx < total && m < M;
+            v0[j] = live ? __ldcg(pp) : 0.f;
+            v1[j] = live ? __ldcg(pp + pb) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < kOut; ++j) {
+            const int idx = r0 + j * kThreads, rem = idx & ((1 << sh) - 1);
+            const int row = rem >> kLogMP, m = rem & (MP - 1), n = (b0 + (idx >> sh)) * 16 + row;
+            if (idx < total && m < M && n < o.N) o.y[(size_t)m * o.N + n] = Ops::round(v0[j] + v1[j]);
+        }
+    }
+}
 template <int MP, int ACT>
 __device__ __forceinline__ void combine_share(const StepOp& o, int c, int NC, int M) {
     constexpr int kLogMP = MP == 1 ? 0 : MP == 2 ? 1 : MP == 4 ? 2 : MP == 8 ? 3 : 4;
     const int b0 = (int)((long long)o.bands * c / NC), b1 = (int)((long long)o.bands * (c + 1) / NC);
-    if (o.flags & W4_OP_SWIGLU)
+    if (o.S == 2 && !(o.flags & W4_OP_SWIGLU))
+        combine_share_two<MP, ACT>(o, b0, (b1 - b0) << (4 + kLogMP), M);
+    else if (o.flags & W4_OP_SWIGLU)
         combine_share_of<MP, ACT, true>(o, b0, (b1 - b0) << (3 + kLogMP), M);
     else
         combine_share_of<MP, ACT, false>(o, b0, (b1 - b0) << (4 + kLogMP), M);
@@ -726,7 +756,7 @@ static int choose_split(int bands, int G, int MP, int NC, int budget, bool scale
         // up to 4 tokens, staging the x slice (an L2 round trip plus ~3 tile-times per KB
         // under load) is counted too; from 8 tokens on, more splits cost more in partials
         // than they save in staging, and the plain count measured better
-        const long x_cost = MP <= 4 ? 3L * (step_x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs)) / 1024 : 0;
+        const long x_cost = MP <= 4 ? 3L * (step_x_bytes(MP, Gs) + dec::xsum_bytes(MP, Gs, scaled)) / 1024 : 0;
         const long cost = (long)((bands + cps - 1) / cps) * Gs + (S > 1 ? kSplitPenalty + 4 * S : 0) + x_cost;
         if (cost < best_cost) {
             best_cost = cost;
