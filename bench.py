@@ -603,6 +603,8 @@ def main():
                          "case for a profiler")
     ap.add_argument("--act", choices=("fp16", "int8"), default="fp16",
                     help="with --no-extras: activation path of the step (int8 = Path A, x quantised in the kernel)")
+    ap.add_argument("--tokens", type=int, default=1,
+                    help="with --no-extras: tokens per step (1..16; the benchmark line is always M=1)")
     ap.add_argument("--profile-m", type=int, default=1,
                     help="with --profile-projection: tokens (M > 16 runs the prefill GEMM)")
     args = ap.parse_args()
@@ -628,7 +630,7 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.set_device(local)
-    M = 1
+    M = max(1, min(args.tokens, 16)) if args.no_extras else 1
     layers = max(1, min(args.layers, LAYERS)) if args.no_extras else LAYERS
     st = build_step(torch, w4, synth, M, layers)
     nbw = w4.w4_decode_seq_workspace_bytes(st["ws"], M)
@@ -661,10 +663,10 @@ def main():
     barrier()
     clocks = sampler.stop() if sampler else None
     ms = max_over_ranks(torch, ev0.elapsed_time(ev1) / args.steps, world)
-    if layers != LAYERS:
+    if layers != LAYERS or M != 1:
         nb = BYTES_PER_STEP // LAYERS * layers
         if rank == 0:
-            print(json.dumps({"profile_case": "decode step of the first %d layers, M=1, %s activations" % (layers, act),
+            print(json.dumps({"profile_case": "decode step of the first %d layers, M=%d, %s activations" % (layers, M, act),
                               "bytes_per_step": nb, "us_per_step": ms * 1e3, "GB/s": nb / (ms * 1e-3) / 1e9,
                               "status_word": seq.status()}), flush=True)
         seq.close()
