@@ -13,11 +13,13 @@
 // keeps more SMs busy; chosen per call with the K split) tile over a K range,
 // one 128-wide group per pipeline step, with warp-specialised roles:
 //   warp 0     TMA producer: x tile [BN tokens][128 K] as two 128-byte
-//              swizzled boxes (zero fill past M), and the group's 8 packed
-//              weight tiles (bulk copies) into the same shared-memory stage
-//   warp 1     one thread issues 8 tcgen05.mma (128xBNx16) per group, A
-//              from tensor memory and B (x) from shared memory, into one of
-//              two TMEM accumulators, then commits
+//              swizzled boxes (zero fill past M) into a shared-memory stage
+//   warp 3     producer of the group's 8 packed weight tiles (bulk copies)
+//              into the same stage
+//   warps 1-2  one thread each issues 8 tcgen05.mma (128xBNx16) per group
+//              (warp 1 the even groups, warp 2 the odd ones), A from tensor
+//              memory and B (x) from shared memory, into its own TMEM
+//              accumulator, then commits
 //   warps 4-7  dequant: read the group's packed tiles from the stage, unpack
 //              nibbles to exact fp16 q and store them straight into one of
 //              two A slots of tensor memory (16-lane x 256-bit stores: the
@@ -135,9 +137,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // in the same branch as the role's code.
     if (warp < 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
-    if (warp == 0) {
-        // ---- TMA producer ---------------------------------------------------
+    if (warp == 0 || warp == 3) {
+        // ---- producers: warp 0 the x tile (TMA), warp 3 the group's packed tiles ----
+        // (two threads: one thread issuing all ten copies of a group took ~560 ns, near the group's MMA time)
         if (lane == 0) {
+            const bool xs = warp == 0;
+            const uint32_t full = xs ? x_full : w_full;
             const int nb = min(8, p.bands - band0);
             int issued = 0;
             for (int it = 0; it < ng; ++it) {
@@ -147,32 +152,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     atomicOr(p.status, 1);
                     break;
                 }
-                const uint32_t dst = tc::smem_addr(sB + s * kBStage);
-                tc::mbar_arrive_expect_tx(x_full + 8 * s, kBStage);
-                const int k0 = (g_lo + it) * 128;
-                tc::tma_load_2d(dst, &xmap, k0, tok0, x_full + 8 * s);
-                tc::tma_load_2d(dst + kBStage / 2, &xmap, k0 + 64, tok0, x_full + 8 * s);
-                // the group's packed tiles, one per band of this CTA
-                tc::mbar_arrive_expect_tx(w_full + 8 * s, (uint32_t)(nb * kTileBytes));
-                const uint32_t wdst = tc::smem_addr(sW + s * kWStage);
-                for (int bi = 0; bi < nb; ++bi)
-                    tc::bulk_load(wdst + (uint32_t)(bi * kTileBytes),
-                                  p.w + ((size_t)(band0 + bi) * p.G + g_lo + it) * kTileBytes, kTileBytes,
-                                  w_full + 8 * s);
+                if (xs) {
+                    const uint32_t dst = tc::smem_addr(sB + s * kBStage);
+                    tc::mbar_arrive_expect_tx(x_full + 8 * s, kBStage);
+                    const int k0 = (g_lo + it) * 128;
+                    tc::tma_load_2d(dst, &xmap, k0, tok0, x_full + 8 * s);
+                    tc::tma_load_2d(dst + kBStage / 2, &xmap, k0 + 64, tok0, x_full + 8 * s);
+                } else {
+                    // the group's packed tiles, one per band of this CTA
+                    tc::mbar_arrive_expect_tx(w_full + 8 * s, (uint32_t)(nb * kTileBytes));
+                    const uint32_t wdst = tc::smem_addr(sW + s * kWStage);
+                    for (int bi = 0; bi < nb; ++bi)
+                        tc::bulk_load(wdst + (uint32_t)(bi * kTileBytes),
+                                      p.w + ((size_t)(band0 + bi) * p.G + g_lo + it) * kTileBytes, kTileBytes,
+                                      w_full + 8 * s);
+                }
                 ++issued;
             }
             // drain: the last loads of every stage have landed before the CTA exits
-            for (int it = issued - 1; it >= 0 && it >= issued - kStages; --it) {
-                if (!tc::mbar_wait(x_full + 8 * (it % kStages), (it / kStages) & 1)) atomicOr(p.status, 2);
-                if (!tc::mbar_wait(w_full + 8 * (it % kStages), (it / kStages) & 1)) atomicOr(p.status, 2);
-            }
+            for (int it = issued - 1; it >= 0 && it >= issued - kStages; --it)
+                if (!tc::mbar_wait(full + 8 * (it % kStages), (it / kStages) & 1)) atomicOr(p.status, 2);
         }
-    } else if (warp == 1) {
-        // ---- MMA issuer -------------------------------------------------------
+    } else if (warp == 1 || warp == 2) {
+        // ---- MMA issuers: warp 1 the even groups (accumulator 0, A slot 0), warp 2 the odd ones ----
+        // One thread issuing every group left the tensor pipe idle between groups (the 8 MMAs are
+        // accepted only as fast as they run, and the next group's waits and commits came after
+        // them: 717 ns per group for 457 ns of MMAs); with two, one waits while the other issues.
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_f16_f32(kBM, kBN);
             int done = 0;
-            for (int it = 0; it < ng; ++it) {
+            for (int it = warp - 1; it < ng; it += 2) {
                 const int s = it % kStages, a = it % kASlots, b = it & 1;
                 const uint32_t ph = (it / kStages) & 1, aph = (it / kASlots) & 1;
                 // accumulator b was read out (two groups back) by the promote warps
