@@ -172,28 +172,29 @@ __device__ __forceinline__ void sum_groups(uint32_t* xs, float* xsum, int M, int
             if constexpr (kScaled) {
                 // rescale each group by its power of two and round to binary16 in place: the four
                 // groups' maxima first (their butterflies interleaved), then the conversions
-                float2 f[kBatch][2], amax[kBatch];
+                // (the largest magnitude as an integer warp reduction of the bfloat16 magnitude bits, which
+                // order like the values: one redux per group instead of a five-step shuffle butterfly)
+                float2 f[kBatch][2];
+                uint32_t mag[kBatch];
 #pragma unroll
                 for (int b = 0; b < kBatch; ++b) {
                     const int gl = g0 + b * NW;
-                    f[b][0] = f[b][1] = make_float2(0.f, 0.f);
+                    uint32_t w0 = 0, w1 = 0;
                     if (gl < Gs) {
                         const uint32_t* src = xs + word(gl, m);
-                        f[b][0] = ActOps<ACT>::to_float2(src[0]);
-                        f[b][1] = ActOps<ACT>::to_float2(src[1]);
+                        w0 = src[0];
+                        w1 = src[1];
                     }
-                    amax[b].x = fmaxf(fmaxf(fabsf(f[b][0].x), fabsf(f[b][0].y)),
-                                      fmaxf(fabsf(f[b][1].x), fabsf(f[b][1].y)));
+                    f[b][0] = ActOps<ACT>::to_float2(w0);
+                    f[b][1] = ActOps<ACT>::to_float2(w1);
+                    mag[b] = max(max(w0 & 0x7FFFu, (w0 >> 16) & 0x7FFFu), max(w1 & 0x7FFFu, (w1 >> 16) & 0x7FFFu));
                 }
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-                    for (int b = 0; b < kBatch; ++b)
-                        amax[b].x = fmaxf(amax[b].x, __shfl_xor_sync(0xFFFFFFFFu, amax[b].x, off));
+                for (int b = 0; b < kBatch; ++b) mag[b] = __reduce_max_sync(0xFFFFFFFFu, mag[b]);
 #pragma unroll
                 for (int b = 0; b < kBatch; ++b) {
                     const int gl = g0 + b * NW;
-                    const float sc = x_scale_of(amax[b].x, c1[b]);
+                    const float sc = x_scale_of(__uint_as_float(mag[b] << 16), c1[b]);
                     const uint32_t h0 = to_half2_bits(f[b][0].x * sc, f[b][0].y * sc);
                     const uint32_t h1 = to_half2_bits(f[b][1].x * sc, f[b][1].y * sc);
                     sum[b] = 0.f;
