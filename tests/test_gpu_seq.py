@@ -271,6 +271,66 @@ def test_bf16_sequence_matches_oracle(M):
     seq.close()
 
 
+def to_bf16_bits(a):
+    """float32 values -> bfloat16 bits, round to nearest even (finite values)."""
+    u = np.asarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def extreme_bf16_tokens(rng, K):
+    """Five tokens of bfloat16 x whose groups of 128 span what binary16 cannot
+    hold as they are: ~1e30 (above binary16's range), ~1e-30 (below it),
+    all zero, per-group alternation of those with N(0,1), and groups with one
+    element of 1e4 among elements of ~1e-6 (a range of 2^33 inside a group,
+    wider than the 2^28 the rescale keeps exact)."""
+    G = K // 128
+    z = rng.standard_normal((5, K)).astype(np.float32)
+    x = np.empty_like(z)
+    x[0] = z[0] * 1e30
+    x[1] = z[1] * 1e-30
+    x[2] = 0.0
+    scale = np.array([1e30, 1e-30, 0.0, 1.0])[np.arange(G) % 4]
+    x[3] = (z[3].reshape(G, 128) * scale[:, None]).ravel()
+    x[4] = z[4] * 1e-6
+    x[4].reshape(G, 128)[:, 7] = 1e4
+    return to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("M", [1, 2, 5])
+def test_bf16_rescale_extreme_ranges(M):
+    """The bfloat16 path stages x as binary16 after a power-of-two rescale per
+    (group, token): x far above and below binary16's range, zero groups, and a
+    group range wider than the rescale keeps exact all come out within the
+    bfloat16 tolerance of the oracle, token by token (one- and two-token
+    fragment staging, five tokens in natural order; the down shape splits K)."""
+    rng = np.random.default_rng(700 + M)
+    shapes = [(64, 768), (48, 1280), (3584, 18944)]
+    for N, K in shapes:
+        xall = extreme_bf16_tokens(rng, K)
+        for first in range(0, 5, M):
+            x = xall[first:first + M]
+            if x.shape[0] < M:
+                x = np.concatenate([x, xall[:M - x.shape[0]]])
+            q = rng.integers(-8, 8, (N, K)).astype(np.int8)
+            s = (0.005 + 0.015 * rng.random((N, K // 128))).astype(np.float16).view(np.uint16)
+            packed, w = pack_on_device(q, s)
+            y = torch.zeros((M, N), dtype=torch.int16, device="cuda")
+            nb = w4.w4_decode_seq_workspace_bytes([w], M)
+            buf = torch.zeros(nb + 256, dtype=torch.uint8, device="cuda")
+            off = (-buf.data_ptr()) % 256
+            seq = w4.DecodeSeq([w], [dev(x)], [y], M, workspace=buf[off:off + nb], act="bf16")
+            seq.replay()
+            torch.cuda.synchronize()
+            assert seq.status() == 0
+            got = host(y)
+            ref = oracle.linear(x, q, s, act="bf16")
+            for m in range(M):
+                assert_close(got[m:m + 1], ref[m:m + 1], "N=%d K=%d token %d of %d" % (N, K, first + m, M),
+                             act="bf16")
+            seq.close()
+            del packed
+
+
 def test_bf16_activation_type_is_checked():
     rng = np.random.default_rng(1)
     x, q, s = rand_problem(rng, 1, 128, 256)
