@@ -295,7 +295,7 @@ w4_status w4_decode_seq_create_persistent(const w4_weight* w, const void* const*
 #define W4_ACT_BF16 1 /* x and y bfloat16; scales stay binary16.  The kernel rescales each
                          group of 128 x of a token by a power of two and rounds it to
                          binary16 (exact for every x within 2^-28 of the group's largest
-                         magnitude) and runs the binary16 arithmetic on it */
+                         magnitude; |x| below 2^116) and runs the binary16 arithmetic on it */
 #define W4_ACT_I8 2   /* the pages' Path A ("3. The INT8 vs. FP16 Activation Trade-off"):
                          x binary16, quantised per token to INT8 inside the kernel
                          (sx = max|x| / 127 and xq = rne(x / sx) in IEEE binary32),

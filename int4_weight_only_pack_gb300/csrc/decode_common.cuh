@@ -140,8 +140,10 @@ __host__ __device__ constexpr int xsum_bytes(int MP, int Gs, bool scaled = false
 
 // The power of two 2^e of a (group, token) of rescaled x, from the largest
 // magnitude amax: e = 14 - floor(log2 amax), so that amax * 2^e lies in
-// [2^14, 2^15), clamped to [-103, 126] (zero groups take 126).  Returns
-// 2^e; c1 = 2^(24-e), the group's c' for rows r.
+// [2^14, 2^15), clamped to [-103, 126] (zero groups take 126; |x| must stay
+// below 2^116).  Returns 2^e; c1 = 2^(24-e), the group's c' for rows r.  The
+// group's d = -8 * 2^-e * sum is formed as -sum * (c1 * 2^-21): for large x,
+// sum * c1 alone would leave FP32's range although d does not.
 __device__ __forceinline__ float x_scale_of(float amax, float& c1) {
     const int E = (__float_as_int(amax) >> 23) & 0xFF;  // biased exponent of amax (0 for zero)
     const int e = min(126, max(-103, 141 - E));
@@ -229,7 +231,7 @@ __device__ __forceinline__ void sum_groups(uint32_t* xs, float* xsum, int M, int
                 for (int b = 0; b < kBatch; ++b)
                     if (g0 + b * NW < Gs) {
                         if constexpr (kScaled) {  // d = -8 * 2^-e * sum, c' = 2^(24-e)
-                            xsum[(g0 + b * NW) * kG + m] = -sum[b] * c1[b] * 0x1p-21f;
+                            xsum[(g0 + b * NW) * kG + m] = -sum[b] * (c1[b] * 0x1p-21f);
                             xsum[(g0 + b * NW) * kG + xsum_cofs(MP) + m] = c1[b];
                         } else {
                             xsum[(g0 + b * NW) * kG + m] = sum[b];
@@ -306,7 +308,7 @@ __device__ __forceinline__ void sum_groups_nat(uint32_t* xs, float* xsum, int M,
         sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
         if (live && sub == 0) {
             if constexpr (kScaled) {  // d = -8 * 2^-e * sum, c' = 2^(24-e)
-                xsum[gl * kG + m] = -sum * c1 * 0x1p-21f;
+                xsum[gl * kG + m] = -sum * (c1 * 0x1p-21f);
                 xsum[gl * kG + xsum_cofs(MP) + m] = c1;
             } else {
                 xsum[gl * kG + m] = sum;
