@@ -78,6 +78,7 @@ struct Tile {
 // add up to the 128 x 512 the CTA is launched with.
 constexpr int kRegsLow = 112, kRegsHigh = 144;
 static_assert(2 * kRegsLow + 2 * kRegsHigh == 4 * 128, "register split");
+static_assert(kWStage % 128 == 0, "weight stages start 128-byte aligned (TMA destination)");
 constexpr size_t kStatusBytes = 256;       // workspace head: status word (+ padding)
 
 struct GemmParams {
@@ -89,7 +90,8 @@ struct GemmParams {
 };
 
 template <int BN>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, GemmParams p) {
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                              const __grid_constant__ CUtensorMap wmap, GemmParams p) {
     constexpr int kBN = BN, kBStage = Tile<BN>::kBStage, kACol0 = Tile<BN>::kACol0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -143,7 +145,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         if (lane == 0) {
             const bool xs = warp == 0;
             const uint32_t full = xs ? x_full : w_full;
-            const int nb = min(8, p.bands - band0);
             int issued = 0;
             for (int it = 0; it < ng; ++it) {
                 const int s = it % kStages;
@@ -159,13 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     tc::tma_load_2d(dst, &xmap, k0, tok0, x_full + 8 * s);
                     tc::tma_load_2d(dst + kBStage / 2, &xmap, k0 + 64, tok0, x_full + 8 * s);
                 } else {
-                    // the group's packed tiles, one per band of this CTA
-                    tc::mbar_arrive_expect_tx(w_full + 8 * s, (uint32_t)(nb * kTileBytes));
-                    const uint32_t wdst = tc::smem_addr(sW + s * kWStage);
-                    for (int bi = 0; bi < nb; ++bi)
-                        tc::bulk_load(wdst + (uint32_t)(bi * kTileBytes),
-                                      p.w + ((size_t)(band0 + bi) * p.G + g_lo + it) * kTileBytes, kTileBytes,
-                                      w_full + 8 * s);
+                    // the group's packed tiles of this CTA's 8 bands in one 2-D copy (rows = bands, 1056
+                    // bytes each; rows past the last band are zero-filled and never read)
+                    tc::mbar_arrive_expect_tx(w_full + 8 * s, (uint32_t)kWStage);
+                    tc::tma_load_2d(tc::smem_addr(sW + s * kWStage), &wmap, (g_lo + it) * (kTileBytes / 8), band0,
+                                    w_full + 8 * s);
                 }
                 ++issued;
             }
@@ -420,11 +419,11 @@ w4_status allow_tile_smem() {
 }
 
 template <int BN>
-w4_status launch_tile(const CUtensorMap& map, const GemmParams& p, cudaStream_t stream) {
+w4_status launch_tile(const CUtensorMap& map, const CUtensorMap& wmap, const GemmParams& p, cudaStream_t stream) {
     const w4_status st = allow_tile_smem<BN>();
     if (st != W4_OK) return st;
     const dim3 grid((unsigned)((p.M + BN - 1) / BN), (unsigned)((p.N + kBM - 1) / kBM), (unsigned)p.splits);
-    gemm_tc_kernel<BN><<<grid, kThreads, Tile<BN>::kSmemBytes, stream>>>(map, p);
+    gemm_tc_kernel<BN><<<grid, kThreads, Tile<BN>::kSmemBytes, stream>>>(map, wmap, p);
     W4_CUDA_TRY(cudaGetLastError());
     return W4_OK;
 }
@@ -464,6 +463,20 @@ w4_status launch_gemm_tc(const void* x, const w4_weight* w, void* y, int M, void
         set_error("cuTensorMapEncodeTiled failed (%d)", (int)cr);
         return W4_ERR_CUDA;
     }
+    // the packed weight as rows of bands (G tiles of 1056 bytes each, in 8-byte
+    // elements): a box of 8 bands x one tile is a group's tiles for one CTA
+    CUtensorMap wmap;
+    const int64_t G = num_groups(w->K), bands = num_bands(w->N);
+    const cuuint64_t wdim[2] = {(cuuint64_t)(G * (kTileBytes / 8)), (cuuint64_t)bands};
+    const cuuint64_t wstride[1] = {(cuuint64_t)(G * kTileBytes)};
+    const cuuint32_t wbox[2] = {(cuuint32_t)(kTileBytes / 8), 8};
+    cr = encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(w->data), wdim, wstride, wbox, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled (weight) failed (%d)", (int)cr);
+        return W4_ERR_CUDA;
+    }
     GemmParams p;
     p.w = static_cast<const uint8_t*>(w->data);
     p.y = static_cast<uint16_t*>(y);
@@ -477,7 +490,8 @@ w4_status launch_gemm_tc(const void* x, const w4_weight* w, void* y, int M, void
     p.part = p.splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(ws) + kStatusBytes) : nullptr;
 
     W4_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(int), stream));
-    const w4_status st = plan.bn == 128 ? launch_tile<128>(map, p, stream) : launch_tile<192>(map, p, stream);
+    const w4_status st =
+        plan.bn == 128 ? launch_tile<128>(map, wmap, p, stream) : launch_tile<192>(map, wmap, p, stream);
     if (st != W4_OK) return st;
     if (p.splits > 1) {
         const size_t count = (size_t)M * p.N;
