@@ -76,8 +76,13 @@ struct Tile {
 // Registers per thread after the split: warpgroups 0-1 (producer, issuer,
 // dequant) give up registers to warpgroups 2-3 (promote).  The four shares
 // add up to the 128 x 512 the CTA is launched with.
-constexpr int kRegsLow = 112, kRegsHigh = 144;
-static_assert(2 * kRegsLow + 2 * kRegsHigh == 4 * 128, "register split");
+// Registers per thread after the split: warpgroup 0 (producers, MMA issuers:
+// one busy thread per warp) 48, warpgroup 1 (dequant) 112, warpgroups 2-3
+// (promote) 176, which lets a promote thread hold two 32-column pieces of a
+// partial beside its 96 accumulators.  The four shares add up to the 128 x
+// 512 the CTA is launched with.
+constexpr int kRegsIssue = 48, kRegsDequant = 112, kRegsHigh = 176;
+static_assert(kRegsIssue + kRegsDequant + 2 * kRegsHigh == 4 * 128, "register split");
 static_assert(kWStage % 128 == 0, "weight stages start 128-byte aligned (TMA destination)");
 constexpr size_t kStatusBytes = 256;       // workspace head: status word (+ padding)
 
@@ -137,8 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
     // Each role runs under its warpgroup's register limit: the limit is set
     // in the same branch as the role's code.
-    if (warp < 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
     if (warp == 0 || warp == 3) {
         // ---- producers: warp 0 the x tile (TMA), warp 3 the group's packed tiles ----
         // (two threads: one thread issuing all ten copies of a group took ~560 ns, near the group's MMA time)
@@ -205,7 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             if (done > 0 && !tc::mbar_wait(d_full + 8 * ((done - 1) & 1), ((done - 1) >> 1) & 1))
                 atomicOr(p.status, 8);
         }
-    } else if (warp >= 4) {
+    }
+    } else if (warp < 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDequant));
+    {
         // ---- dequant: 2 bands per warp, TMEM lanes 32*dw .. 32*dw + 31 -------
         const int dw = warp - 4;
         for (int it = 0; it < ng; ++it) {
@@ -302,19 +310,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             }
             tc::fence_after_sync();
             const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + b * kBN + kCols * half;
-            uint32_t v[32];
+            // two 32-column pieces per tensor-memory wait (one at a time, three waits per group at
+            // 192 tokens held the accumulator ~100 ns longer)
+            static_assert(kCols == 64 || kCols == 96, "promote pieces");
+            uint32_t v[2][32];
+            tc::tmem_ld_32x32(taddr, v[0]);
+            tc::tmem_ld_32x32(taddr + 32, v[1]);
+            tc::tmem_wait_ld();
+            if (kCols == 64) {
+                // the whole partial is in registers: hand the accumulator back
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(d_empty + 8 * b);
+            }
 #pragma unroll
-            for (int c = 0; c < kCols / 32; ++c) {
-                tc::tmem_ld_32x32(taddr + 32 * c, v);
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    acc[32 * c + i] = fmaf(s_cur, __uint_as_float(v[c][i]), acc[32 * c + i]);
+            if (kCols == 96) {
+                tc::tmem_ld_32x32(taddr + 64, v[0]);
                 tc::tmem_wait_ld();
-                if (c == kCols / 32 - 1) {
-                    // the whole partial is in registers: hand the accumulator back
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(d_empty + 8 * b);
-                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(d_empty + 8 * b);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(s_cur, __uint_as_float(v[i]), acc[32 * c + i]);
+                for (int i = 0; i < 32; ++i) acc[64 + i] = fmaf(s_cur, __uint_as_float(v[0][i]), acc[64 + i]);
             }
             s_cur = s_nxt;
             s_nxt = s_far;
