@@ -42,6 +42,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "tc_ptx.cuh"
@@ -92,7 +93,23 @@ struct GemmParams {
     float* part;  // split-K partials [splits][M][N], or null
     int* status;
     int M, N, K, G, bands, splits;
+    int tiles_x, tiles_y, tiles;  // token blocks, row blocks, tiles (x fastest, then row block, then split)
 };
+
+// Tile t of the call: its first token and band, its K split and group range.
+struct TileAt {
+    int tok0, band0, split, g_lo, ng;
+};
+__device__ __forceinline__ TileAt tile_at(const GemmParams& p, int t, int bn) {
+    const int x = t % p.tiles_x, r = t / p.tiles_x, yb = r % p.tiles_y, z = r / p.tiles_y;
+    TileAt a;
+    a.tok0 = x * bn;
+    a.band0 = yb * (kBM / 16);
+    a.split = z;
+    a.g_lo = (int)((long long)p.G * z / p.splits);
+    a.ng = (int)((long long)p.G * (z + 1) / p.splits) - a.g_lo;
+    return a;
+}
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
@@ -110,12 +127,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     __shared__ uint32_t tmem_base_sh;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tok0 = blockIdx.x * kBN;
-    const int band0 = blockIdx.y * (kBM / 16);
-    const int split = blockIdx.z;
-    const int g_lo = (int)((long long)p.G * split / p.splits);
-    const int g_hi = (int)((long long)p.G * (split + 1) / p.splits);
-    const int ng = g_hi - g_lo;
+    // Persistent: CTA c takes tiles c, c + gridDim.x, ...; every role walks the same tiles and
+    // groups, and a running group count gi (across tiles) picks stages, A slots, accumulators and
+    // their phases, so the pipeline runs on from one tile into the next.
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -151,27 +165,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const bool xs = warp == 0;
             const uint32_t full = xs ? x_full : w_full;
             int issued = 0;
-            for (int it = 0; it < ng; ++it) {
-                const int s = it % kStages;
-                const uint32_t ph = (it / kStages) & 1;
-                if (!tc::mbar_wait(empty + 8 * s, ph ^ 1)) {
-                    atomicOr(p.status, 1);
-                    break;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+                const TileAt tl = tile_at(p, t, kBN);
+                for (int it = 0; it < tl.ng; ++it) {
+                    const int s = issued % kStages;
+                    const uint32_t ph = (issued / kStages) & 1;
+                    if (!tc::mbar_wait(empty + 8 * s, ph ^ 1)) {
+                        atomicOr(p.status, 1);
+                        ok = false;
+                        break;
+                    }
+                    if (xs) {
+                        const uint32_t dst = tc::smem_addr(sB + s * kBStage);
+                        tc::mbar_arrive_expect_tx(x_full + 8 * s, kBStage);
+                        const int k0 = (tl.g_lo + it) * 128;
+                        tc::tma_load_2d(dst, &xmap, k0, tl.tok0, x_full + 8 * s);
+                        tc::tma_load_2d(dst + kBStage / 2, &xmap, k0 + 64, tl.tok0, x_full + 8 * s);
+                    } else {
+                        // the group's packed tiles of the tile's 8 bands in one 2-D copy (rows = bands, 1056
+                        // bytes each; rows past the last band are zero-filled and never read)
+                        tc::mbar_arrive_expect_tx(w_full + 8 * s, (uint32_t)kWStage);
+                        tc::tma_load_2d(tc::smem_addr(sW + s * kWStage), &wmap, (tl.g_lo + it) * (kTileBytes / 8),
+                                        tl.band0, w_full + 8 * s);
+                    }
+                    ++issued;
                 }
-                if (xs) {
-                    const uint32_t dst = tc::smem_addr(sB + s * kBStage);
-                    tc::mbar_arrive_expect_tx(x_full + 8 * s, kBStage);
-                    const int k0 = (g_lo + it) * 128;
-                    tc::tma_load_2d(dst, &xmap, k0, tok0, x_full + 8 * s);
-                    tc::tma_load_2d(dst + kBStage / 2, &xmap, k0 + 64, tok0, x_full + 8 * s);
-                } else {
-                    // the group's packed tiles of this CTA's 8 bands in one 2-D copy (rows = bands, 1056
-                    // bytes each; rows past the last band are zero-filled and never read)
-                    tc::mbar_arrive_expect_tx(w_full + 8 * s, (uint32_t)kWStage);
-                    tc::tma_load_2d(tc::smem_addr(sW + s * kWStage), &wmap, (g_lo + it) * (kTileBytes / 8), band0,
-                                    w_full + 8 * s);
-                }
-                ++issued;
             }
             // drain: the last loads of every stage have landed before the CTA exits
             for (int it = issued - 1; it >= 0 && it >= issued - kStages; --it)
@@ -184,8 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         // them: 717 ns per group for 457 ns of MMAs); with two, one waits while the other issues.
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_f16_f32(kBM, kBN);
-            int done = 0;
-            for (int it = warp - 1; it < ng; it += 2) {
+            int done = 0, ngrp = 0;  // groups of this CTA's tiles so far
+            for (int t = blockIdx.x; t < p.tiles; t += gridDim.x) ngrp += tile_at(p, t, kBN).ng;
+            for (int it = warp - 1; it < ngrp; it += 2) {
                 const int s = it % kStages, a = it % kASlots, b = it & 1;
                 const uint32_t ph = (it / kStages) & 1, aph = (it / kASlots) & 1;
                 // accumulator b was read out (two groups back) by the promote warps
@@ -216,15 +236,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     {
         // ---- dequant: 2 bands per warp, TMEM lanes 32*dw .. 32*dw + 31 -------
         const int dw = warp - 4;
-        for (int it = 0; it < ng; ++it) {
-            const int s = it % kStages, a = it % kASlots;
-            const uint32_t ph = (it / kStages) & 1, aph = (it / kASlots) & 1;
+        int gi = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+          const int band0 = tile_at(p, t, kBN).band0, ng = tile_at(p, t, kBN).ng;
+          for (int it = 0; it < ng; ++it, ++gi) {
+            const int s = gi % kStages, a = gi % kASlots;
+            const uint32_t ph = (gi / kStages) & 1, aph = (gi / kASlots) & 1;
             // the packed tiles have landed: unpack them into registers, and only then wait for the A
             // slot (the MMAs that read it kASlots groups back have completed), so that refilling the
             // slot takes only the stores (the issuers had waited ~320 ns per group for the A slot;
             // layer at 512 tokens 264.8 -> 258.2 us)
             if (!tc::mbar_wait(w_full + 8 * s, ph)) {
                 atomicOr(p.status, 16);
+                ok = false;
                 break;
             }
             uint32_t q16[2][2][16];
@@ -263,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             }
             if (!tc::mbar_wait(a_empty + 8 * a, aph ^ 1)) {
                 atomicOr(p.status, 16);
+                ok = false;
                 break;
             }
             tc::fence_after_sync();
@@ -276,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(a_full + 8 * a);
+          }
         }
     }
     } else {
@@ -284,74 +311,81 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         // ---- promote + epilogue -------------------------------------------------
         const int quarter = warp & 3, half = (warp - 8) >> 2;
         const int row = 32 * quarter + lane;  // TMEM lane = weight row within the tile
-        const int bandg = band0 + (row >> 4), rr = row & 15;
-        const bool row_ok = bandg < p.bands;
-        const uint8_t* sc = p.w + (size_t)bandg * p.G * kTileBytes + kScaleOffset + 4 * (rr & 7) + 2 * (rr >> 3);
+        const int rr = row & 15;
         constexpr int kCols = kBN / 2;  // tokens of this thread: the warp's half of the tile
-        float acc[kCols];
-#pragma unroll
-        for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
-        auto scale_of = [&](int it) -> float {
-            if (!row_ok) return 0.f;
-            const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(sc + (size_t)(g_lo + it) * kTileBytes));
-            return __half2float(__ushort_as_half(h));
-        };
-        // scales two groups ahead of the accumulator they multiply
-        float s_cur = ng > 0 ? scale_of(0) : 0.f;
-        float s_nxt = ng > 1 ? scale_of(1) : 0.f;
+        int gi = 0;
         bool ok = true;
-        for (int it = 0; it < ng; ++it) {
-            const int b = it & 1;
-            const float s_far = (it + 2 < ng) ? scale_of(it + 2) : 0.f;
-            if (!tc::mbar_wait(d_full + 8 * b, (it >> 1) & 1)) {
-                atomicOr(p.status, 32);
-                ok = false;
-                break;
-            }
-            tc::fence_after_sync();
-            const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + b * kBN + kCols * half;
-            // two 32-column pieces per tensor-memory wait (one at a time, three waits per group at
-            // 192 tokens held the accumulator ~100 ns longer)
-            static_assert(kCols == 64 || kCols == 96, "promote pieces");
-            uint32_t v[2][32];
-            tc::tmem_ld_32x32(taddr, v[0]);
-            tc::tmem_ld_32x32(taddr + 32, v[1]);
-            tc::tmem_wait_ld();
-            if (kCols == 64) {
-                // the whole partial is in registers: hand the accumulator back
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(d_empty + 8 * b);
-            }
+        for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+            const TileAt tl = tile_at(p, t, kBN);
+            const int bandg = tl.band0 + (row >> 4);
+            const bool row_ok = bandg < p.bands;
+            const uint8_t* sc =
+                p.w + (size_t)bandg * p.G * kTileBytes + kScaleOffset + 4 * (rr & 7) + 2 * (rr >> 3);
+            float acc[kCols];
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    acc[32 * c + i] = fmaf(s_cur, __uint_as_float(v[c][i]), acc[32 * c + i]);
-            if (kCols == 96) {
-                tc::tmem_ld_32x32(taddr + 64, v[0]);
+            for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
+            auto scale_of = [&](int it) -> float {
+                if (!row_ok) return 0.f;
+                const unsigned short h =
+                    __ldg(reinterpret_cast<const unsigned short*>(sc + (size_t)(tl.g_lo + it) * kTileBytes));
+                return __half2float(__ushort_as_half(h));
+            };
+            // scales two groups ahead of the accumulator they multiply
+            float s_cur = tl.ng > 0 ? scale_of(0) : 0.f;
+            float s_nxt = tl.ng > 1 ? scale_of(1) : 0.f;
+            for (int it = 0; it < tl.ng; ++it, ++gi) {
+                const int b = gi & 1;
+                const float s_far = (it + 2 < tl.ng) ? scale_of(it + 2) : 0.f;
+                if (!tc::mbar_wait(d_full + 8 * b, (gi >> 1) & 1)) {
+                    atomicOr(p.status, 32);
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + b * kBN + kCols * half;
+                // two 32-column pieces per tensor-memory wait (one at a time, three waits per group at
+                // 192 tokens held the accumulator ~100 ns longer)
+                static_assert(kCols == 64 || kCols == 96, "promote pieces");
+                uint32_t v[2][32];
+                tc::tmem_ld_32x32(taddr, v[0]);
+                tc::tmem_ld_32x32(taddr + 32, v[1]);
                 tc::tmem_wait_ld();
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(d_empty + 8 * b);
+                if (kCols == 64) {
+                    // the whole partial is in registers: hand the accumulator back
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(d_empty + 8 * b);
+                }
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc[64 + i] = fmaf(s_cur, __uint_as_float(v[0][i]), acc[64 + i]);
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        acc[32 * c + i] = fmaf(s_cur, __uint_as_float(v[c][i]), acc[32 * c + i]);
+                if (kCols == 96) {
+                    tc::tmem_ld_32x32(taddr + 64, v[0]);
+                    tc::tmem_wait_ld();
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(d_empty + 8 * b);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[64 + i] = fmaf(s_cur, __uint_as_float(v[0][i]), acc[64 + i]);
+                }
+                s_cur = s_nxt;
+                s_nxt = s_far;
             }
-            s_cur = s_nxt;
-            s_nxt = s_far;
-        }
-        const int n = band0 * 16 + row;
-        if (ok && row_ok && n < p.N) {
-            const int t0 = tok0 + kCols * half;
-            if (p.part == nullptr) {
+            const int n = tl.band0 * 16 + row;
+            if (ok && row_ok && n < p.N) {
+                const int t0 = tl.tok0 + kCols * half;
+                if (p.part == nullptr) {
 #pragma unroll
-                for (int i = 0; i < kCols; ++i)
-                    if (t0 + i < p.M) p.y[(size_t)(t0 + i) * p.N + n] = __half_as_ushort(__float2half_rn(acc[i]));
-            } else {
-                float* dst = p.part + (size_t)split * p.M * p.N;
+                    for (int i = 0; i < kCols; ++i)
+                        if (t0 + i < p.M) p.y[(size_t)(t0 + i) * p.N + n] = __half_as_ushort(__float2half_rn(acc[i]));
+                } else {
+                    float* dst = p.part + (size_t)tl.split * p.M * p.N;
 #pragma unroll
-                for (int i = 0; i < kCols; ++i)
-                    if (t0 + i < p.M) dst[(size_t)(t0 + i) * p.N + n] = acc[i];
+                    for (int i = 0; i < kCols; ++i)
+                        if (t0 + i < p.M) dst[(size_t)(t0 + i) * p.N + n] = acc[i];
+                }
             }
         }
     }
@@ -453,8 +487,13 @@ template <int BN>
 w4_status launch_tile(const CUtensorMap& map, const CUtensorMap& wmap, const GemmParams& p, cudaStream_t stream) {
     const w4_status st = allow_tile_smem<BN>();
     if (st != W4_OK) return st;
-    const dim3 grid((unsigned)((p.M + BN - 1) / BN), (unsigned)((p.N + kBM - 1) / kBM), (unsigned)p.splits);
-    gemm_tc_kernel<BN><<<grid, kThreads, Tile<BN>::kSmemBytes, stream>>>(map, wmap, p);
+    GemmParams q = p;
+    q.tiles_x = (p.M + BN - 1) / BN;
+    q.tiles_y = (p.N + kBM - 1) / kBM;
+    q.tiles = q.tiles_x * q.tiles_y * p.splits;
+    // persistent: one CTA per SM (or per tile, if fewer), each walking its tiles in turn
+    const unsigned ctas = (unsigned)std::min(q.tiles, device_sm_count());
+    gemm_tc_kernel<BN><<<ctas, kThreads, Tile<BN>::kSmemBytes, stream>>>(map, wmap, q);
     W4_CUDA_TRY(cudaGetLastError());
     return W4_OK;
 }
