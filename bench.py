@@ -401,9 +401,21 @@ def single_gemv_rotated(torch, w4, synth, st, copies=32, reps=20):
         one()
     spread = replay_spread(torch, one, reps * copies)
     nb = (N * K) // 2 + N * G * 2
+    # the same launches captured in one graph (the host's call overhead out of the way): per launch, with
+    # and without programmatic dependent launch between consecutive ones
+    graph = {}
+    for pdl in (False, True):
+        g = w4.DecodeSeq(ws[:copies], [x] * copies, [y] * copies, 1, use_pdl=pdl)
+        for _ in range(3):
+            g.replay()
+        us = time_replays(torch, g.replay, reps) * 1e3 / copies
+        graph["pdl" if pdl else "no_pdl"] = {"us_per_gemv": us, "GB/s": nb / (us * 1e-6) / 1e9}
+        g.close()
     return {"copies": copies, "bytes_per_copy": nb, "rotated_bytes": nb * copies,
             "us_per_gemv": spread["median_us"], "GB/s": nb / (spread["median_us"] * 1e-6) / 1e9,
-            "spread": spread, "launch": "w4a16_gemv (decode kernel, library launch shape), one stream, back to back"}
+            "spread": spread, "launch": "w4a16_gemv (decode kernel, library launch shape) called from Python "
+                                        "once per launch, one stream, back to back (host call overhead included)",
+            "graph_of_rotated_launches": graph}
 
 
 def small_batch_sweep(torch, w4, synth, st, Ms=(2, 4, 8, 16), reps=50):
