@@ -9,13 +9,15 @@
 // its FP32 scale and added in FP32 registers.  The scale is never folded into
 // an FP16 weight, so the weights reach the tensor core exactly.
 //
-// One CTA computes a 128 (weight rows) x BN (tokens: 192, or 128 where that
-// keeps more SMs busy; chosen per call with the K split) tile over a K range,
+// A tile is 128 weight rows x BN tokens (192, or 128 where that keeps more SMs
+// busy; chosen per call with the K split) over a K range.  The CTAs are
+// persistent (one per SM, or per tile if fewer) and walk their tiles in turn,
 // one 128-wide group per pipeline step, with warp-specialised roles:
 //   warp 0     TMA producer: x tile [BN tokens][128 K] as two 128-byte
 //              swizzled boxes (zero fill past M) into a shared-memory stage
-//   warp 3     producer of the group's 8 packed weight tiles (bulk copies)
-//              into the same stage
+//   warp 3     producer of the group's 8 packed weight tiles (one 2-D TMA
+//              copy through a tensor map over the packed weight) into the
+//              same stage
 //   warps 1-2  one thread each issues 8 tcgen05.mma (128xBNx16) per group
 //              (warp 1 the even groups, warp 2 the odd ones), A from tensor
 //              memory and B (x) from shared memory, into its own TMEM
@@ -27,8 +29,8 @@
 //   warps 8-15 promote: read a group's FP32 partial from TMEM, hand the
 //              accumulator back, multiply by the group scale and add to
 //              FP32 accumulators in registers (BN/2 per thread: these two
-//              warpgroups take registers from the other two); finally write
-//              y (or an FP32 split-K partial)
+//              warpgroups take registers from the other two); at the end of
+//              each tile write y (or an FP32 split-K partial)
 // Tile width: the MMA instruction is full rate from N = 128 up, but in this
 // loop (per-group commits and barrier handshakes) 8 MMAs cost about as much
 // at N = 128 as at N = 256, so wide tiles pay.  Two 256-column accumulators
