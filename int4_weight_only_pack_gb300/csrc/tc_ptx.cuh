@@ -31,17 +31,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return done != 0;
 }
-// The same test without suspending: returns at once whether or not the phase
-// has completed (try_wait may park the thread for a while first).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
 // Wait for the phase with this parity to complete; give up after about a
 // second of SM clock (returns false) instead of spinning forever.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
@@ -91,11 +80,6 @@ __device__ __forceinline__ void cluster_sync_all() {
 // Barrier among `count` threads (a multiple of 32) on hardware barrier `id`.
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-// Arrive on hardware barrier `id` (of `count` threads) without waiting: the
-// writes before it are visible to the threads that wait there with bar.sync.
-__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t count) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---- bulk copies ------------------------------------------------------------------
