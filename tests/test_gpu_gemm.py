@@ -41,6 +41,20 @@ def test_parity(M, N, K):
     assert_close(run(x, w, N, M), oracle.linear(x, q, s), "M=%d N=%d K=%d" % (M, N, K))
 
 
+# More tiles than SMs: each persistent CTA walks several tiles (token blocks and
+# row blocks change between them; the second shape also splits K), checked on
+# sampled rows against the oracle (rows are independent outputs).
+@pytest.mark.parametrize("M,N,K", [(600, 5000, 512), (800, 4000, 2560)])
+def test_parity_several_tiles_per_cta(M, N, K):
+    rng = np.random.default_rng(M * 7 + N + K)
+    x, q, s = rand_problem(rng, M, N, K)
+    packed, w = pack_on_device(q, s)
+    y = run(x, w, N, M)
+    rows = np.unique(np.concatenate([[0, 15, 127, 128, 1023, 1024, N - 16, N - 1],
+                                     rng.integers(0, N, 56)]))
+    assert_close(y[:, rows], oracle.linear(x, q[rows], s[rows]), "M=%d N=%d K=%d" % (M, N, K))
+
+
 @pytest.mark.parametrize("proj", list(LAYER))
 def test_full_layer_shapes_m512_sampled(proj):
     M = 512
