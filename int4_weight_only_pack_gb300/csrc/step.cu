@@ -30,9 +30,10 @@
 //    straight from its accumulators.  A band cut between warps is parked in
 //    shared memory by each and summed, in warp order, by one warp after a CTA
 //    barrier.  A band split in K (S > 1) goes through FP32 partials in the
-//    workspace; the arrival that completes the band adds the S partials in
-//    split order and writes y.  Every sum has a fixed order, so results are
-//    identical from run to run.
+//    workspace; below 8 tokens the arrival that completes the band adds the
+//    S partials in split order and writes y, from 8 tokens on every CTA adds
+//    up an equal share of the bands once all partials are in (kOpTwoPhase).
+//    Every sum has a fixed order, so results are identical from run to run.
 //  * Counters reset themselves (the last arrival of a band, the last CTA of
 //    the step), so the launch can be replayed from a graph.
 //  * Every wait is bounded (about a second); a timeout sets the status word,
