@@ -161,12 +161,16 @@ __device__ __forceinline__ uint32_t to_half2_bits(float a, float b) {
 // word(gl, m) and word(gl, m) + 1 (the layout's fragment positions of lane
 // class (lane >> 1) & 3, k16 step 2 * (lane >> 3) + (lane & 1)), then a
 // butterfly over the warp: the same order, so the same bits, whatever the
-// layout.  Warp w takes groups w, w + NW, ...; four groups' reductions are
+// layout.  Warp w takes groups w, w + NW, ...; several groups' reductions are
 // interleaved, and no index is divided by the run-time token count.
 template <int MP, int NW, int ACT, typename Word>
 __device__ __forceinline__ void sum_groups(uint32_t* xs, float* xsum, int M, int Gs, int warp, int lane,
                                            Word&& word) {
-    constexpr int kBatch = 4;
+    // groups reduced together: two per warp with 16 warps (a K = 3584 slice has
+    // 28 groups: four per warp left half of them empty, and the one-token
+    // step took 911 us against 901 with two, 1010 against 986 at two tokens,
+    // 962 against 938 with bfloat16 x), four with fewer warps
+    constexpr int kBatch = NW >= 16 ? 2 : 4;
     constexpr bool kScaled = ActOps<ACT>::kScaled;
     constexpr int kG = xsum_gstride(MP, kScaled);
     for (int g0 = warp; g0 < Gs; g0 += NW * kBatch) {
