@@ -30,7 +30,10 @@
 //              accumulator back, multiply by the group scale and add to
 //              FP32 accumulators in registers (BN/2 per thread: these two
 //              warpgroups take registers from the other two); at the end of
-//              each tile write y (or an FP32 split-K partial)
+//              each tile write y (or an FP32 split-K partial): at 128 tokens
+//              each warp converts its 32 rows x 64 tokens into a shared-memory
+//              slice and one thread issues a TMA store of it, so the warp
+//              goes on to the next tile's groups at once
 // Tile width: the MMA instruction is full rate from N = 128 up, but in this
 // loop (per-group commits and barrier handshakes) 8 MMAs cost about as much
 // at N = 128 as at N = 256, so wide tiles pay.  Two 256-column accumulators
@@ -60,19 +63,26 @@ w4_status check_gemv_args(const void* x, const w4_weight* w, const void* y, int 
 namespace {
 
 constexpr int kBM = 128;                   // weight rows per CTA (8 bands)
-constexpr int kStages = 4;                 // shared-memory stages (one group each)
 constexpr int kASlots = 2;                 // A slots in tensor memory
 constexpr int kWStage = 8 * kTileBytes;    // the group's 8 packed tiles (one per band)
 constexpr int kThreads = 512;
 constexpr int kTmemCols = 512;
 // Per tile width BN (tokens per CTA: 128 or 192): the x stage (BN x 128 fp16),
-// and tensor memory as two BN-column FP32 accumulators followed by one
-// 64-column block of fp16 q pairs (128 rows x 128 K) per A slot.
+// four shared-memory stages (one group each), at 128 tokens the y staging
+// slices (each promote warp's 32 rows x 64 tokens of fp16; at 192 tokens
+// they do not fit beside four stages, and three stages measured slower:
+// gate_up 122 -> 125 us, down 77 -> 87 us at 512 tokens), and tensor memory
+// as two BN-column FP32 accumulators followed by one 64-column block of fp16
+// q pairs (128 rows x 128 K) per A slot.
 template <int BN>
 struct Tile {
     static constexpr int kBStage = BN * 128 * 2;
+    static constexpr int kStages = 4;
+    static constexpr int kYBytes = BN == 128 ? 8 * 32 * (BN / 2) * 2 : 0;
     static constexpr int kACol0 = 2 * BN;
-    static constexpr int kSmemBytes = kStages * (kBStage + kWStage) + 1024 + 256;
+    static constexpr int kSmemBytes = kStages * (kBStage + kWStage) + kYBytes + 1024 + 256;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+    static_assert((kStages * (kBStage + kWStage)) % 128 == 0, "y slices start 128-byte aligned");
     static_assert(kACol0 + 64 * kASlots <= kTmemCols, "tensor memory columns");
     static_assert(BN % 64 == 0 && BN <= 256, "MMA N and promote column blocks");
 };
@@ -96,6 +106,7 @@ struct GemmParams {
     int* status;
     int M, N, K, G, bands, splits;
     int tiles_x, tiles_y, tiles;  // token blocks, row blocks, tiles (x fastest, then row block, then split)
+    int ystore;                   // 1: y leaves through shared memory and TMA stores (ymap)
 };
 
 // Tile t of the call: its first token and band, its K split and group range.
@@ -115,13 +126,15 @@ __device__ __forceinline__ TileAt tile_at(const GemmParams& p, int t, int bn) {
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
-                                                              const __grid_constant__ CUtensorMap wmap, GemmParams p) {
-    constexpr int kBN = BN, kBStage = Tile<BN>::kBStage, kACol0 = Tile<BN>::kACol0;
+                                                              const __grid_constant__ CUtensorMap wmap,
+                                                              const __grid_constant__ CUtensorMap ymap, GemmParams p) {
+    constexpr int kBN = BN, kBStage = Tile<BN>::kBStage, kACol0 = Tile<BN>::kACol0, kStages = Tile<BN>::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sB = smem;
     uint8_t* sW = sB + kStages * kBStage;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sW + kStages * kWStage);
+    uint8_t* sY = sW + kStages * kWStage;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sY + Tile<BN>::kYBytes);
     // barrier slots
     const uint32_t x_full = tc::smem_addr(bars), w_full = x_full + 8 * kStages, empty = w_full + 8 * kStages,
                    a_full = empty + 8 * kStages, a_empty = a_full + 8 * kASlots, d_full = a_empty + 8 * kASlots,
@@ -149,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         tc::mbar_init_fence();
         tc::prefetch_tensormap(&xmap);
+        if (p.ystore) tc::prefetch_tensormap(&ymap);
     }
     if (warp == 1) tc::tmem_alloc(tc::smem_addr(&tmem_base_sh), kTmemCols);
     tc::fence_before_sync();
@@ -376,7 +390,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 s_nxt = s_far;
             }
             const int n = tl.band0 * 16 + row;
-            if (ok && row_ok && n < p.N) {
+            if (Tile<BN>::kYBytes > 0 && ok && p.part == nullptr && p.ystore) {
+                // y through shared memory: this warp's 32 rows x kCols tokens, then one TMA
+                // store (a thread's kCols separate 2-byte global stores had held the promote
+                // warps 2-4 us per tile while the next tile's MMAs waited for the accumulators)
+                const uint32_t ys = tc::smem_addr(sY) + (uint32_t)(warp - 8) * (32 * kCols * 2);
+                if (lane == 0) tc::bulk_wait_read_all();  // the previous tile's store has read the slice
+                __syncwarp();
+                unsigned short* yw = reinterpret_cast<unsigned short*>(sY + (warp - 8) * (32 * kCols * 2)) + lane;
+#pragma unroll
+                for (int i = 0; i < kCols; ++i) yw[32 * i] = __half_as_ushort(__float2half_rn(acc[i]));
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                const int n0 = tl.band0 * 16 + 32 * quarter, t0 = tl.tok0 + kCols * half;
+                if (lane == 0 && n0 < p.N && t0 < p.M) {
+                    tc::tma_store_2d(&ymap, ys, n0, t0);
+                    tc::bulk_commit_group();
+                }
+            } else if (ok && row_ok && n < p.N) {
                 const int t0 = tl.tok0 + kCols * half;
                 if (p.part == nullptr) {
 #pragma unroll
@@ -390,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 }
             }
         }
+        if (lane == 0) tc::bulk_wait_all();  // the y stores are done before the slices go away
     }
     }
 
@@ -486,7 +518,8 @@ w4_status allow_tile_smem() {
 }
 
 template <int BN>
-w4_status launch_tile(const CUtensorMap& map, const CUtensorMap& wmap, const GemmParams& p, cudaStream_t stream) {
+w4_status launch_tile(const CUtensorMap& map, const CUtensorMap& wmap, const CUtensorMap& ymap, const GemmParams& p,
+                      cudaStream_t stream) {
     const w4_status st = allow_tile_smem<BN>();
     if (st != W4_OK) return st;
     GemmParams q = p;
@@ -495,7 +528,7 @@ w4_status launch_tile(const CUtensorMap& map, const CUtensorMap& wmap, const Gem
     q.tiles = q.tiles_x * q.tiles_y * p.splits;
     // persistent: one CTA per SM (or per tile, if fewer), each walking its tiles in turn
     const unsigned ctas = (unsigned)std::min(q.tiles, device_sm_count());
-    gemm_tc_kernel<BN><<<ctas, kThreads, Tile<BN>::kSmemBytes, stream>>>(map, wmap, q);
+    gemm_tc_kernel<BN><<<ctas, kThreads, Tile<BN>::kSmemBytes, stream>>>(map, wmap, ymap, q);
     W4_CUDA_TRY(cudaGetLastError());
     return W4_OK;
 }
@@ -549,7 +582,25 @@ w4_status launch_gemm_tc(const void* x, const w4_weight* w, void* y, int M, void
         set_error("cuTensorMapEncodeTiled (weight) failed (%d)", (int)cr);
         return W4_ERR_CUDA;
     }
+    // y as [M][N] fp16 for the TMA stores of 128-token tiles (a box is one promote warp's 32 rows x 64
+    // tokens); the global stride must be a multiple of 16 bytes and y 16-byte aligned, else y takes plain
+    // stores
+    CUtensorMap ymap = wmap;
+    const bool ystore = plan.bn == 128 && w->N % 8 == 0 && aligned16(y);
+    if (ystore) {
+        const cuuint64_t ydim[2] = {(cuuint64_t)w->N, (cuuint64_t)M};
+        const cuuint64_t ystride[1] = {(cuuint64_t)w->N * 2};
+        const cuuint32_t ybox[2] = {32, (cuuint32_t)(plan.bn / 2)};
+        cr = encode(&ymap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, y, ydim, ystride, ybox, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) {
+            set_error("cuTensorMapEncodeTiled (y) failed (%d)", (int)cr);
+            return W4_ERR_CUDA;
+        }
+    }
     GemmParams p;
+    p.ystore = ystore ? 1 : 0;
     p.w = static_cast<const uint8_t*>(w->data);
     p.y = static_cast<uint16_t*>(y);
     p.status = static_cast<int*>(ws);
@@ -563,7 +614,7 @@ w4_status launch_gemm_tc(const void* x, const w4_weight* w, void* y, int M, void
 
     W4_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(int), stream));
     const w4_status st =
-        plan.bn == 128 ? launch_tile<128>(map, wmap, p, stream) : launch_tile<192>(map, wmap, p, stream);
+        plan.bn == 128 ? launch_tile<128>(map, wmap, ymap, p, stream) : launch_tile<192>(map, wmap, ymap, p, stream);
     if (st != W4_OK) return st;
     if (p.splits > 1) {
         const size_t count = (size_t)M * p.N;

@@ -66,6 +66,27 @@ def test_full_layer_shapes_m512_sampled(proj):
     assert_close(run(x, w, N, M)[:, rows], ref, "%s M=512" % proj)
 
 
+# 128-token tiles leave y through shared memory and one TMA store per promote
+# warp (32 rows x 64 tokens, clipped at M and N) when N is a multiple of 8,
+# else through plain stores: a ragged last row block (1000 = 7 x 128 + 104)
+# and token block (300 = 2 x 128 + 44, 193 = 128 + 65), and N = 130 (no
+# tensor map for y).
+# Nothing is written past y.
+@pytest.mark.parametrize("M,N,K", [(300, 1000, 512), (193, 1000, 768), (100, 130, 512)])
+def test_parity_y_epilogues(M, N, K):
+    rng = np.random.default_rng(M + 3 * N + K)
+    x, q, s = rand_problem(rng, M, N, K)
+    packed, w = pack_on_device(q, s)
+    buf = torch.full((M * N + 64,), -1, dtype=torch.int16, device="cuda")
+    ws = w4.w4_workspace_bytes(M, N, w.K)
+    wsb = torch.empty(max(ws, 16), dtype=torch.uint8, device="cuda")
+    w4.w4a16_gemm(dev(x), w, buf[:M * N], M, wsb if ws else None, ws)
+    torch.cuda.synchronize()
+    got = host(buf)
+    assert_close(got[:M * N].reshape(M, N), oracle.linear(x, q, s), "M=%d N=%d K=%d" % (M, N, K))
+    assert np.all(got[M * N:] == 0xFFFF)
+
+
 def test_deterministic():
     rng = np.random.default_rng(4)
     x, q, s = rand_problem(rng, 256, 512, 1024)
