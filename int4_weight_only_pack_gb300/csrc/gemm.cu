@@ -30,10 +30,13 @@
 //              accumulator back, multiply by the group scale and add to
 //              FP32 accumulators in registers (BN/2 per thread: these two
 //              warpgroups take registers from the other two); at the end of
-//              each tile write y (or an FP32 split-K partial): at 128 tokens
-//              each warp converts its 32 rows x 64 tokens into a shared-memory
-//              slice and one thread issues a TMA store of it, so the warp
-//              goes on to the next tile's groups at once
+//              each tile write y (or an FP32 split-K partial): where K is not
+//              split each warp converts its 32 rows x BN/2 tokens to fp16 in
+//              its slice of the x stage of the tile's last group (free once
+//              that group's MMAs are done) and one thread issues a TMA store
+//              of it; the x producer refills that stage only after the store
+//              has read it (barrier y_done), and the warp goes on to the next
+//              tile's groups at once
 // Tile width: the MMA instruction is full rate from N = 128 up, but in this
 // loop (per-group commits and barrier handshakes) 8 MMAs cost about as much
 // at N = 128 as at N = 256, so wide tiles pay.  Two 256-column accumulators
@@ -67,22 +70,18 @@ constexpr int kASlots = 2;                 // A slots in tensor memory
 constexpr int kWStage = 8 * kTileBytes;    // the group's 8 packed tiles (one per band)
 constexpr int kThreads = 512;
 constexpr int kTmemCols = 512;
-// Per tile width BN (tokens per CTA: 128 or 192): the x stage (BN x 128 fp16),
-// four shared-memory stages (one group each), at 128 tokens the y staging
-// slices (each promote warp's 32 rows x 64 tokens of fp16; at 192 tokens
-// they do not fit beside four stages, and three stages measured slower:
-// gate_up 122 -> 125 us, down 77 -> 87 us at 512 tokens), and tensor memory
-// as two BN-column FP32 accumulators followed by one 64-column block of fp16
-// q pairs (128 rows x 128 K) per A slot.
+// Per tile width BN (tokens per CTA: 128 or 192): the x stage (BN x 128 fp16;
+// at the end of a tile the stage of its last group holds the tile's y, 128
+// rows x BN tokens of fp16, the same size), four shared-memory stages (one
+// group each), and tensor memory as two BN-column FP32 accumulators followed
+// by one 64-column block of fp16 q pairs (128 rows x 128 K) per A slot.
 template <int BN>
 struct Tile {
     static constexpr int kBStage = BN * 128 * 2;
     static constexpr int kStages = 4;
-    static constexpr int kYBytes = BN == 128 ? 8 * 32 * (BN / 2) * 2 : 0;
     static constexpr int kACol0 = 2 * BN;
-    static constexpr int kSmemBytes = kStages * (kBStage + kWStage) + kYBytes + 1024 + 256;
-    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-    static_assert((kStages * (kBStage + kWStage)) % 128 == 0, "y slices start 128-byte aligned");
+    static constexpr int kSmemBytes = kStages * (kBStage + kWStage) + 1024 + 256;
+    static_assert(8 * 32 * (BN / 2) * 2 == kBStage, "a tile's y fills one x stage");
     static_assert(kACol0 + 64 * kASlots <= kTmemCols, "tensor memory columns");
     static_assert(BN % 64 == 0 && BN <= 256, "MMA N and promote column blocks");
 };
@@ -106,7 +105,7 @@ struct GemmParams {
     int* status;
     int M, N, K, G, bands, splits;
     int tiles_x, tiles_y, tiles;  // token blocks, row blocks, tiles (x fastest, then row block, then split)
-    int ystore;                   // 1: y leaves through shared memory and TMA stores (ymap)
+    int ystore;                   // 1: y leaves through an x stage and TMA stores (ymap)
 };
 
 // Tile t of the call: its first token and band, its K split and group range.
@@ -133,12 +132,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sB = smem;
     uint8_t* sW = sB + kStages * kBStage;
-    uint8_t* sY = sW + kStages * kWStage;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sY + Tile<BN>::kYBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sW + kStages * kWStage);
     // barrier slots
     const uint32_t x_full = tc::smem_addr(bars), w_full = x_full + 8 * kStages, empty = w_full + 8 * kStages,
                    a_full = empty + 8 * kStages, a_empty = a_full + 8 * kASlots, d_full = a_empty + 8 * kASlots,
-                   d_empty = d_full + 16;
+                   d_empty = d_full + 16, y_done = d_empty + 16;
     __shared__ uint32_t tmem_base_sh;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -160,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             tc::mbar_init(d_full + 8 * b, 1);
             tc::mbar_init(d_empty + 8 * b, 8);
         }
+        tc::mbar_init(y_done, 8);
         tc::mbar_init_fence();
         tc::prefetch_tensormap(&xmap);
         if (p.ystore) tc::prefetch_tensormap(&ymap);
@@ -182,6 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const uint32_t full = xs ? x_full : w_full;
             int issued = 0;
             bool ok = true;
+            uint32_t ends = 0;  // bit s: the group last loaded into stage s ended its tile
+            int ydone = 0;      // tile ends whose y the promote warps have stored out of their stage
             for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
                 const TileAt tl = tile_at(p, t, kBN);
                 for (int it = 0; it < tl.ng; ++it) {
@@ -192,6 +193,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         ok = false;
                         break;
                     }
+                    if (xs && p.ystore && ((ends >> s) & 1)) {
+                        // the stage held a tile's y: wait until its TMA stores have read it (tile ends are
+                        // >= kStages groups apart, so the one barrier's phases come in order)
+                        if (!tc::mbar_wait(y_done, ydone & 1)) {
+                            atomicOr(p.status, 1);
+                            ok = false;
+                            break;
+                        }
+                        ++ydone;
+                    }
+                    ends = (ends & ~(1u << s)) | ((it == tl.ng - 1 ? 1u : 0u) << s);
                     if (xs) {
                         const uint32_t dst = tc::smem_addr(sB + s * kBStage);
                         tc::mbar_arrive_expect_tx(x_full + 8 * s, kBStage);
@@ -390,22 +402,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 s_nxt = s_far;
             }
             const int n = tl.band0 * 16 + row;
-            if (Tile<BN>::kYBytes > 0 && ok && p.part == nullptr && p.ystore) {
-                // y through shared memory: this warp's 32 rows x kCols tokens, then one TMA
-                // store (a thread's kCols separate 2-byte global stores had held the promote
-                // warps 2-4 us per tile while the next tile's MMAs waited for the accumulators)
-                const uint32_t ys = tc::smem_addr(sY) + (uint32_t)(warp - 8) * (32 * kCols * 2);
-                if (lane == 0) tc::bulk_wait_read_all();  // the previous tile's store has read the slice
-                __syncwarp();
-                unsigned short* yw = reinterpret_cast<unsigned short*>(sY + (warp - 8) * (32 * kCols * 2)) + lane;
+            if (ok && p.ystore) {
+                // y through the x stage of the tile's last group (its MMAs are done): this warp's
+                // 32 rows x kCols tokens as fp16, one TMA store, and once the store has read them
+                // the x producer may refill the stage (a thread's kCols separate 2-byte global
+                // stores had held the promote warps 2-4 us per tile, the next tile's MMAs waiting
+                // for the accumulators meanwhile)
+                // (the slice's shared address is recomputed from the array here: keeping the
+                // stages' base pointer live through the group loop spilled a register)
+                const uint32_t yslice = ((tc::smem_addr(smem_raw) + 1023u) & ~1023u) +
+                                        (uint32_t)(((gi - 1) % kStages) * kBStage + (warp - 8) * (32 * kCols * 2));
 #pragma unroll
-                for (int i = 0; i < kCols; ++i) yw[32 * i] = __half_as_ushort(__float2half_rn(acc[i]));
+                for (int i = 0; i < kCols; ++i)
+                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(yslice + 2 * lane + 64 * i),
+                                 "h"(__half_as_ushort(__float2half_rn(acc[i])))
+                                 : "memory");
                 tc::fence_proxy_async_smem();
                 __syncwarp();
-                const int n0 = tl.band0 * 16 + 32 * quarter, t0 = tl.tok0 + kCols * half;
-                if (lane == 0 && n0 < p.N && t0 < p.M) {
-                    tc::tma_store_2d(&ymap, ys, n0, t0);
-                    tc::bulk_commit_group();
+                if (lane == 0) {
+                    const int n0 = tl.band0 * 16 + 32 * quarter, t0 = tl.tok0 + kCols * half;
+                    if (n0 < p.N && t0 < p.M) {
+                        tc::tma_store_2d(&ymap, yslice, n0, t0);
+                        tc::bulk_commit_group();
+                    }
+                    tc::bulk_wait_read_all();
+                    tc::mbar_arrive(y_done);
                 }
             } else if (ok && row_ok && n < p.N) {
                 const int t0 = tl.tok0 + kCols * half;
@@ -582,11 +603,11 @@ w4_status launch_gemm_tc(const void* x, const w4_weight* w, void* y, int M, void
         set_error("cuTensorMapEncodeTiled (weight) failed (%d)", (int)cr);
         return W4_ERR_CUDA;
     }
-    // y as [M][N] fp16 for the TMA stores of 128-token tiles (a box is one promote warp's 32 rows x 64
-    // tokens); the global stride must be a multiple of 16 bytes and y 16-byte aligned, else y takes plain
-    // stores
+    // y as [M][N] fp16 for the TMA stores (a box is one promote warp's 32 rows x half a tile's tokens):
+    // whole-K tiles of at least 4 groups (one per stage) whose y has a tensor map (the global stride a
+    // multiple of 16 bytes, y 16-byte aligned); otherwise y takes plain stores
     CUtensorMap ymap = wmap;
-    const bool ystore = plan.bn == 128 && w->N % 8 == 0 && aligned16(y);
+    const bool ystore = plan.splits == 1 && w->K >= 4 * kGroupK && w->N % 8 == 0 && aligned16(y);
     if (ystore) {
         const cuuint64_t ydim[2] = {(cuuint64_t)w->N, (cuuint64_t)M};
         const cuuint64_t ystride[1] = {(cuuint64_t)w->N * 2};
