@@ -105,7 +105,8 @@ struct GemmParams {
     int* status;
     int M, N, K, G, bands, splits;
     int tiles_x, tiles_y, tiles;  // token blocks, row blocks, tiles (x fastest, then row block, then split)
-    int ystore;                   // 1: y leaves through an x stage and TMA stores (ymap)
+    int ystore;                   // 1: y (or the split-K partial) leaves through an x stage and TMA stores
+                                  // (omap: y [M][N] fp16, or the partials [splits][M][N] fp32)
 };
 
 // Tile t of the call: its first token and band, its K split and group range.
@@ -126,7 +127,7 @@ __device__ __forceinline__ TileAt tile_at(const GemmParams& p, int t, int bn) {
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
                                                               const __grid_constant__ CUtensorMap wmap,
-                                                              const __grid_constant__ CUtensorMap ymap, GemmParams p) {
+                                                              const __grid_constant__ CUtensorMap omap, GemmParams p) {
     constexpr int kBN = BN, kBStage = Tile<BN>::kBStage, kACol0 = Tile<BN>::kACol0, kStages = Tile<BN>::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         tc::mbar_init(y_done, 8);
         tc::mbar_init_fence();
         tc::prefetch_tensormap(&xmap);
-        if (p.ystore) tc::prefetch_tensormap(&ymap);
+        if (p.ystore) tc::prefetch_tensormap(&omap);
     }
     if (warp == 1) tc::tmem_alloc(tc::smem_addr(&tmem_base_sh), kTmemCols);
     tc::fence_before_sync();
@@ -403,28 +404,53 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             }
             const int n = tl.band0 * 16 + row;
             if (ok && p.ystore) {
-                // y through the x stage of the tile's last group (its MMAs are done): this warp's
-                // 32 rows x kCols tokens as fp16, one TMA store, and once the store has read them
-                // the x producer may refill the stage (a thread's kCols separate 2-byte global
-                // stores had held the promote warps 2-4 us per tile, the next tile's MMAs waiting
-                // for the accumulators meanwhile)
-                // (the slice's shared address is recomputed from the array here: keeping the
-                // stages' base pointer live through the group loop spilled a register)
-                const uint32_t yslice = ((tc::smem_addr(smem_raw) + 1023u) & ~1023u) +
-                                        (uint32_t)(((gi - 1) % kStages) * kBStage + (warp - 8) * (32 * kCols * 2));
+                // y (or the split's FP32 partial) through the x stage of the tile's last group (its
+                // MMAs are done): this warp's 32 rows x kCols tokens into its slice, TMA stores, and
+                // once they have read it the x producer may refill the stage (a thread's kCols
+                // separate global stores had held the promote warps 2-4 us per tile, the next tile's
+                // MMAs waiting for the accumulators meanwhile).  The slice's shared address is
+                // recomputed from the array here: keeping the stages' base pointer live through the
+                // group loop spilled a register.
+                const uint32_t slice = ((tc::smem_addr(smem_raw) + 1023u) & ~1023u) +
+                                       (uint32_t)(((gi - 1) % kStages) * kBStage + (warp - 8) * (32 * kCols * 2));
+                const int n0 = tl.band0 * 16 + 32 * quarter, t0 = tl.tok0 + kCols * half;
+                if (p.part == nullptr) {
+                    // fp16 y: [token][32 rows], one store of 32 rows x kCols tokens
 #pragma unroll
-                for (int i = 0; i < kCols; ++i)
-                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(yslice + 2 * lane + 64 * i),
-                                 "h"(__half_as_ushort(__float2half_rn(acc[i])))
-                                 : "memory");
-                tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const int n0 = tl.band0 * 16 + 32 * quarter, t0 = tl.tok0 + kCols * half;
-                    if (n0 < p.N && t0 < p.M) {
-                        tc::tma_store_2d(&ymap, yslice, n0, t0);
+                    for (int i = 0; i < kCols; ++i)
+                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(slice + 2 * lane + 64 * i),
+                                     "h"(__half_as_ushort(__float2half_rn(acc[i])))
+                                     : "memory");
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && n0 < p.N && t0 < p.M) {
+                        tc::tma_store_2d(&omap, slice, n0, t0);
                         tc::bulk_commit_group();
                     }
+                } else {
+                    // FP32 partial: the slice holds half the warp's tokens, so two rounds of
+                    // [token][32 rows] and a store each (the partials are [split][M][N]: tokens
+                    // past M are clipped, not written into the next split's rows)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        if (r == 1) {
+                            if (lane == 0) tc::bulk_wait_read_all();
+                            __syncwarp();
+                        }
+#pragma unroll
+                        for (int i = 0; i < kCols / 2; ++i)
+                            asm volatile("st.shared.f32 [%0], %1;" ::"r"(slice + 4 * lane + 128 * i),
+                                         "f"(acc[r * (kCols / 2) + i])
+                                         : "memory");
+                        tc::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && n0 < p.N && t0 + r * (kCols / 2) < p.M) {
+                            tc::tma_store_3d(&omap, slice, n0, t0 + r * (kCols / 2), tl.split);
+                            tc::bulk_commit_group();
+                        }
+                    }
+                }
+                if (lane == 0) {
                     tc::bulk_wait_read_all();
                     tc::mbar_arrive(y_done);
                 }
@@ -539,7 +565,7 @@ w4_status allow_tile_smem() {
 }
 
 template <int BN>
-w4_status launch_tile(const CUtensorMap& map, const CUtensorMap& wmap, const CUtensorMap& ymap, const GemmParams& p,
+w4_status launch_tile(const CUtensorMap& map, const CUtensorMap& wmap, const CUtensorMap& omap, const GemmParams& p,
                       cudaStream_t stream) {
     const w4_status st = allow_tile_smem<BN>();
     if (st != W4_OK) return st;
@@ -549,7 +575,7 @@ w4_status launch_tile(const CUtensorMap& map, const CUtensorMap& wmap, const CUt
     q.tiles = q.tiles_x * q.tiles_y * p.splits;
     // persistent: one CTA per SM (or per tile, if fewer), each walking its tiles in turn
     const unsigned ctas = (unsigned)std::min(q.tiles, device_sm_count());
-    gemm_tc_kernel<BN><<<ctas, kThreads, Tile<BN>::kSmemBytes, stream>>>(map, wmap, ymap, q);
+    gemm_tc_kernel<BN><<<ctas, kThreads, Tile<BN>::kSmemBytes, stream>>>(map, wmap, omap, q);
     W4_CUDA_TRY(cudaGetLastError());
     return W4_OK;
 }
@@ -603,25 +629,37 @@ w4_status launch_gemm_tc(const void* x, const w4_weight* w, void* y, int M, void
         set_error("cuTensorMapEncodeTiled (weight) failed (%d)", (int)cr);
         return W4_ERR_CUDA;
     }
-    // y as [M][N] fp16 for the TMA stores (a box is one promote warp's 32 rows x half a tile's tokens):
-    // whole-K tiles of at least 4 groups (one per stage) whose y has a tensor map (the global stride a
-    // multiple of 16 bytes, y 16-byte aligned); otherwise y takes plain stores
-    CUtensorMap ymap = wmap;
-    const bool ystore = plan.splits == 1 && w->K >= 4 * kGroupK && w->N % 8 == 0 && aligned16(y);
-    if (ystore) {
+    // The tiles' output for the TMA stores: y [M][N] fp16 (a box is one promote warp's 32 rows x half a
+    // tile's tokens), or with K split the FP32 partials [splits][M][N] (a box is 32 rows x a quarter of
+    // the tokens).  Only where every tile has at least 4 groups (one per stage: tile ends then come at
+    // least a stage cycle apart) and the tensor can be mapped (row stride a multiple of 16 bytes, base
+    // 16-byte aligned); otherwise the promote warps store the output themselves.
+    const int64_t Gk = num_groups(w->K);
+    CUtensorMap omap = wmap;
+    const bool ostore = Gk >= 4 * (int64_t)plan.splits &&
+                        (plan.splits == 1 ? w->N % 8 == 0 && aligned16(y) : w->N % 4 == 0);
+    if (ostore && plan.splits == 1) {
         const cuuint64_t ydim[2] = {(cuuint64_t)w->N, (cuuint64_t)M};
         const cuuint64_t ystride[1] = {(cuuint64_t)w->N * 2};
         const cuuint32_t ybox[2] = {32, (cuuint32_t)(plan.bn / 2)};
-        cr = encode(&ymap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, y, ydim, ystride, ybox, estride,
+        cr = encode(&omap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, y, ydim, ystride, ybox, estride,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (cr != CUDA_SUCCESS) {
-            set_error("cuTensorMapEncodeTiled (y) failed (%d)", (int)cr);
-            return W4_ERR_CUDA;
-        }
+    } else if (ostore) {
+        const cuuint64_t pdim[3] = {(cuuint64_t)w->N, (cuuint64_t)M, (cuuint64_t)plan.splits};
+        const cuuint64_t pstride[2] = {(cuuint64_t)w->N * 4, (cuuint64_t)M * w->N * 4};
+        const cuuint32_t pbox[3] = {32, (cuuint32_t)(plan.bn / 4), 1};
+        const cuuint32_t pestride[3] = {1, 1, 1};
+        cr = encode(&omap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, static_cast<char*>(ws) + kStatusBytes, pdim, pstride,
+                    pbox, pestride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (ostore && cr != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled (output) failed (%d)", (int)cr);
+        return W4_ERR_CUDA;
     }
     GemmParams p;
-    p.ystore = ystore ? 1 : 0;
+    p.ystore = ostore ? 1 : 0;
     p.w = static_cast<const uint8_t*>(w->data);
     p.y = static_cast<uint16_t*>(y);
     p.status = static_cast<int*>(ws);
@@ -635,7 +673,7 @@ w4_status launch_gemm_tc(const void* x, const w4_weight* w, void* y, int M, void
 
     W4_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(int), stream));
     const w4_status st =
-        plan.bn == 128 ? launch_tile<128>(map, wmap, ymap, p, stream) : launch_tile<192>(map, wmap, ymap, p, stream);
+        plan.bn == 128 ? launch_tile<128>(map, wmap, omap, p, stream) : launch_tile<192>(map, wmap, omap, p, stream);
     if (st != W4_OK) return st;
     if (p.splits > 1) {
         const size_t count = (size_t)M * p.N;
