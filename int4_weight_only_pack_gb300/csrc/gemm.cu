@@ -65,6 +65,29 @@ w4_status check_gemv_args(const void* x, const w4_weight* w, const void* y, int 
 
 namespace {
 
+// ---- TMA stores (the prefill kernel's output) ----------------------------------
+// Tiled store of a shared-memory box to global memory (elements outside the
+// tensor are not written), tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     (uint64_t)map),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     (uint64_t)map),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's committed bulk stores have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... and are complete (their writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// orders this thread's generic-proxy shared-memory writes before later async-proxy (TMA) reads
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 constexpr int kBM = 128;                   // weight rows per CTA (8 bands)
 constexpr int kASlots = 2;                 // A slots in tensor memory
 constexpr int kWStage = 8 * kTileBytes;    // the group's 8 packed tiles (one per band)
@@ -421,11 +444,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         asm volatile("st.shared.u16 [%0], %1;" ::"r"(slice + 2 * lane + 64 * i),
                                      "h"(__half_as_ushort(__float2half_rn(acc[i])))
                                      : "memory");
-                    tc::fence_proxy_async_smem();
+                    fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && n0 < p.N && t0 < p.M) {
-                        tc::tma_store_2d(&omap, slice, n0, t0);
-                        tc::bulk_commit_group();
+                        tma_store_2d(&omap, slice, n0, t0);
+                        bulk_commit_group();
                     }
                 } else {
                     // FP32 partial: the slice holds half the warp's tokens, so two rounds of
@@ -434,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
                         if (r == 1) {
-                            if (lane == 0) tc::bulk_wait_read_all();
+                            if (lane == 0) bulk_wait_read_all();
                             __syncwarp();
                         }
 #pragma unroll
@@ -442,16 +465,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                             asm volatile("st.shared.f32 [%0], %1;" ::"r"(slice + 4 * lane + 128 * i),
                                          "f"(acc[r * (kCols / 2) + i])
                                          : "memory");
-                        tc::fence_proxy_async_smem();
+                        fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0 && n0 < p.N && t0 + r * (kCols / 2) < p.M) {
-                            tc::tma_store_3d(&omap, slice, n0, t0 + r * (kCols / 2), tl.split);
-                            tc::bulk_commit_group();
+                            tma_store_3d(&omap, slice, n0, t0 + r * (kCols / 2), tl.split);
+                            bulk_commit_group();
                         }
                     }
                 }
                 if (lane == 0) {
-                    tc::bulk_wait_read_all();
+                    bulk_wait_read_all();
                     tc::mbar_arrive(y_done);
                 }
             } else if (ok && row_ok && n < p.N) {
@@ -468,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 }
             }
         }
-        if (lane == 0) tc::bulk_wait_all();  // the y stores are done before the slices go away
+        if (lane == 0) bulk_wait_all();  // the y stores are done before the slices go away
     }
     }
 
