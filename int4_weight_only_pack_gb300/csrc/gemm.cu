@@ -65,6 +65,25 @@ w4_status check_gemv_args(const void* x, const w4_weight* w, const void* y, int 
 
 namespace {
 
+// ---- wide tensor-memory loads and stores (fewer tcgen05 instructions per group) ----
+// 32 lanes x 64 columns of 32-bit words in one instruction: thread i receives
+// lane (base + i), columns col .. col + 63 (two 32-column loads' registers,
+// one after the other).
+__device__ __forceinline__ void tmem_ld_32x32_x64(uint32_t taddr, uint32_t (&v)[64]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]), "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
+                 : "r"(taddr)
+                 : "memory");
+}
+// 16 lanes x 256 bits repeated over 8 blocks of 8 columns (64 columns) in
+// one instruction: the registers of two 4-block stores, one after the other
+// (thread 4r + c: v[4i], v[4i+1] to lane base + r, columns col + 8i + 2c, + 1;
+// v[4i+2], v[4i+3] to lane base + r + 8).
+__device__ __forceinline__ void tmem_st_16x256_x8(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+                 : "memory");
+}
+
 // ---- TMA stores (the prefill kernel's output) ----------------------------------
 // Tiled store of a shared-memory box to global memory (elements outside the
 // tensor are not written), tracked by the issuing thread's bulk groups.
@@ -304,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 ok = false;
                 break;
             }
-            uint32_t q16[2][2][16];
+            uint32_t q16[2][32];  // per band: k 0..63 (registers 0..15) then k 64..127
 #pragma unroll
             for (int bi = 0; bi < 2; ++bi) {
                 uint4 lo, hi;
@@ -331,10 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     for (int j = 0; j < 4; ++j) {
                         uint32_t q4[4];
                         unpack_word(wd[j], q4);
-                        q16[bi][h][4 * j + 0] = q4[0];
-                        q16[bi][h][4 * j + 1] = q4[2];
-                        q16[bi][h][4 * j + 2] = q4[1];
-                        q16[bi][h][4 * j + 3] = q4[3];
+                        q16[bi][16 * h + 4 * j + 0] = q4[0];
+                        q16[bi][16 * h + 4 * j + 1] = q4[2];
+                        q16[bi][16 * h + 4 * j + 2] = q4[1];
+                        q16[bi][16 * h + 4 * j + 3] = q4[3];
                     }
                 }
             }
@@ -347,8 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
             for (int bi = 0; bi < 2; ++bi) {
                 const uint32_t taddr = tmem + ((uint32_t)(32 * dw + 16 * bi) << 16) + kACol0 + 64 * a;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) tc::tmem_st_16x256_x4(taddr + 32 * h, q16[bi][h]);
+                tmem_st_16x256_x8(taddr, q16[bi]);
             }
             tc::tmem_wait_st();
             tc::fence_before_sync();
@@ -395,12 +413,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 }
                 tc::fence_after_sync();
                 const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + b * kBN + kCols * half;
-                // two 32-column pieces per tensor-memory wait (one at a time, three waits per group at
-                // 192 tokens held the accumulator ~100 ns longer)
+                // a 64-column piece per tensor-memory wait (one at a time, three waits per group at 192
+                // tokens held the accumulator ~100 ns longer), in one load instruction: every group's
+                // tensor-memory loads and stores share the tensor pipe with its MMAs
                 static_assert(kCols == 64 || kCols == 96, "promote pieces");
-                uint32_t v[2][32];
-                tc::tmem_ld_32x32(taddr, v[0]);
-                tc::tmem_ld_32x32(taddr + 32, v[1]);
+                uint32_t v[64];
+                tmem_ld_32x32_x64(taddr, v);
                 tc::tmem_wait_ld();
                 if (kCols == 64) {
                     // the whole partial is in registers: hand the accumulator back
@@ -409,18 +427,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     if (lane == 0) tc::mbar_arrive(d_empty + 8 * b);
                 }
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        acc[32 * c + i] = fmaf(s_cur, __uint_as_float(v[c][i]), acc[32 * c + i]);
+                for (int i = 0; i < 64; ++i) acc[i] = fmaf(s_cur, __uint_as_float(v[i]), acc[i]);
                 if (kCols == 96) {
-                    tc::tmem_ld_32x32(taddr + 64, v[0]);
+                    uint32_t w3[32];
+                    tc::tmem_ld_32x32(taddr + 64, w3);
                     tc::tmem_wait_ld();
                     tc::fence_before_sync();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(d_empty + 8 * b);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[64 + i] = fmaf(s_cur, __uint_as_float(v[0][i]), acc[64 + i]);
+                    for (int i = 0; i < 32; ++i) acc[64 + i] = fmaf(s_cur, __uint_as_float(w3[i]), acc[64 + i]);
                 }
                 s_cur = s_nxt;
                 s_nxt = s_far;
