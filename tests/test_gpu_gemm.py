@@ -87,6 +87,20 @@ def test_parity_y_epilogues(M, N, K):
     assert np.all(got[M * N:] == 0xFFFF)
 
 
+# K split: the FP32 partials leave through TMA stores when N is a multiple of
+# 4 (300 x 132: 8 splits of 4 groups, the smallest the stage cycle allows),
+# else through the promote warps' own stores (301 x 130, 33 x 130); the reduce
+# then adds four outputs per thread when M * N is a multiple of 4 (300 x 132),
+# else one (301 x 130 and 33 x 130: 39130 and 4290 outputs).
+@pytest.mark.parametrize("M,N,K", [(300, 132, 4096), (301, 130, 4096), (33, 130, 8192)])
+def test_parity_split_epilogues(M, N, K):
+    rng = np.random.default_rng(M * 5 + N + K)
+    x, q, s = rand_problem(rng, M, N, K)
+    packed, w = pack_on_device(q, s)
+    assert w4.w4_workspace_bytes(M, N, K) > 256  # K is split: the partials follow the status word
+    assert_close(run(x, w, N, M), oracle.linear(x, q, s), "M=%d N=%d K=%d" % (M, N, K))
+
+
 def test_deterministic():
     rng = np.random.default_rng(4)
     x, q, s = rand_problem(rng, 256, 512, 1024)
