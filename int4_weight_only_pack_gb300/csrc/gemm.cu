@@ -30,16 +30,17 @@
 //              accumulator back, multiply by the group scale and add to
 //              FP32 accumulators in registers (BN/2 per thread: these two
 //              warpgroups take registers from the other two); at the end of
-//              each tile write y (or an FP32 split-K partial): where K is not
-//              split each warp converts its 32 rows x BN/2 tokens to fp16 in
-//              its slice of the x stage of the tile's last group (free once
-//              that group's MMAs are done) and one thread issues a TMA store
-//              of it; the x producer refills that stage only after the store
-//              has read it (barrier y_done), and the warp goes on to the next
+//              each tile each warp puts its 32 rows x BN/2 tokens of y (fp16;
+//              with K split, its FP32 partial in two halves) into its slice
+//              of the x stage of the tile's last group (free once that
+//              group's MMAs are done) and one thread issues TMA stores of it;
+//              the x producer refills that stage only after the stores have
+//              read it (barrier y_done), and the warp goes on to the next
 //              tile's groups at once
-// Tile width: the MMA instruction is full rate from N = 128 up, but in this
-// loop (per-group commits and barrier handshakes) 8 MMAs cost about as much
-// at N = 128 as at N = 256, so wide tiles pay.  Two 256-column accumulators
+// Tile width: the MMA instruction is full rate from N = 128 up when issued
+// alone, but in this loop, beside the tensor-memory stores of A and the
+// reads of every group's FP32 partial, 8 MMAs take about as long at N = 128
+// as at N = 192 (~130 SM cycles each), so wide tiles pay.  Two 256-column accumulators
 // would fill tensor memory and leave no room for A, and with one accumulator
 // the MMAs wait for every group's partial to be read out; 192 tokens leave
 // room for two accumulators and two A slots (192 + 192 + 2 x 64 = 512
