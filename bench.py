@@ -748,6 +748,17 @@ def main():
             one.close()
             del wb1
         extras["per_projection_persistent_chain_28_layers"] = perp
+        # per projection boundary of the 112-launch graph (all figures CUDA-event timed): its time above
+        # the persistent step kernel's (same chain, one launch) and above the HBM-bound floor of the
+        # step's bytes at the measured copy bandwidth, each divided by the 112 boundaries
+        floor_us = BYTES_PER_STEP / (measured_peaks()[0].get("hbm_gbs", FALLBACK_HBM_GBS) * 1e9) * 1e6
+        nproj = LAYERS * len(LAYER)
+        extras["graph_of_112_kernels_per_boundary_us"] = {
+            "pdl_over_persistent": (extras["graph_of_112_kernels_pdl_us_per_step"] - ms * 1e3) / nproj,
+            "no_pdl_over_persistent": (extras["graph_of_112_kernels_no_pdl_us_per_step"] - ms * 1e3) / nproj,
+            "pdl_over_hbm_floor": (extras["graph_of_112_kernels_pdl_us_per_step"] - floor_us) / nproj,
+            "persistent_over_hbm_floor": (ms * 1e3 - floor_us) / nproj,
+            "hbm_floor_us_per_step": floor_us}
         extras["step_replay_spread_M1"] = replay_spread(torch, seq.replay, 100)
         extras["single_gemv_qkv_M1_rotated"] = single_gemv_rotated(torch, w4, synth, st)
         extras["small_batch_step"] = small_batch_sweep(torch, w4, synth, st)
