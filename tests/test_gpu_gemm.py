@@ -42,9 +42,14 @@ def test_parity(M, N, K):
 
 
 # More tiles than SMs: each persistent CTA walks several tiles (token blocks and
-# row blocks change between them; the second shape also splits K), checked on
-# sampled rows against the oracle (rows are independent outputs).
-@pytest.mark.parametrize("M,N,K", [(600, 5000, 512), (800, 4000, 2560)])
+# row blocks change between them; (800, 4000, 2560) also splits K), checked on
+# sampled rows against the oracle (rows are independent outputs).  y leaves
+# through the x stage of each tile's last group and TMA stores where N is a
+# multiple of 8 (tile ends exactly 4 groups apart at K = 512: the stage cycle),
+# else through plain stores (N = 5002 at 128 tokens, N = 3002 at 192); 2048
+# tokens give 16 token blocks.
+@pytest.mark.parametrize("M,N,K", [(600, 5000, 512), (800, 4000, 2560), (2048, 2000, 512), (600, 5002, 512),
+                                   (1000, 3002, 768)])
 def test_parity_several_tiles_per_cta(M, N, K):
     rng = np.random.default_rng(M * 7 + N + K)
     x, q, s = rand_problem(rng, M, N, K)
