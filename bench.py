@@ -613,8 +613,9 @@ def main():
     ap.add_argument("--profile-projection", choices=[n for n, _, _ in LAYER], default=None,
                     help="launch one projection of layer 0 (library launch shape) --steps times: a small "
                          "case for a profiler")
-    ap.add_argument("--act", choices=("fp16", "int8"), default="fp16",
-                    help="with --no-extras: activation path of the step (int8 = Path A, x quantised in the kernel)")
+    ap.add_argument("--act", choices=("fp16", "bf16", "int8"), default="fp16",
+                    help="with --no-extras: activation path of the step (bf16 = bfloat16 x and y, x drawn from "
+                         "the same seeds; int8 = Path A, x quantised in the kernel)")
     ap.add_argument("--tokens", type=int, default=1,
                     help="with --no-extras: tokens per step (1..16; the benchmark line is always M=1)")
     ap.add_argument("--profile-m", type=int, default=1,
@@ -649,6 +650,9 @@ def main():
     ws_buf = torch.zeros(nbw + 256, dtype=torch.uint8, device="cuda")
     ws_off = (-ws_buf.data_ptr()) % 256
     act = args.act if args.no_extras else "fp16"
+    if act == "bf16":  # bfloat16 x of the same seeds (the binary16 bits would not be valid bfloat16 inputs)
+        st["xs"] = [torch.from_numpy(synth.x_full_bf16(synth.seed_of(CONFIG_ID, layer, pid, synth.T_X), M, K)
+                                     .view(np.int16).ravel()).cuda() for (layer, pid, N, K) in st["meta"]]
     seq = w4.DecodeSeq(st["ws"], st["xs"], st["ys"], M, workspace=ws_buf[ws_off:ws_off + nbw], act=act)
     for _ in range(args.warmup):
         seq.replay()
