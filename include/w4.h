@@ -261,7 +261,12 @@ w4_status w4_decode_seq_eager(w4_seq* seq, void* stream);
 /* End to end with host buffers: copy x_bytes from pinned host memory x_host
  * to the device range x_dev, replay, copy y_bytes from y_dev to y_host, and
  * wait for the stream.  x_dev / y_dev are device ranges that hold the
- * sequence's x and y buffers (e.g. one arena each).  Synchronous. */
+ * sequence's x and y buffers (e.g. one arena each).  Synchronous.  The first
+ * call with a given set of the six buffer arguments captures the two copies
+ * and the step as one CUDA graph (host-side graph objects allocated then,
+ * freed by w4_decode_seq_destroy or the next rebuild) and launches it; later
+ * calls with the same arguments launch that graph again.  Where the capture
+ * fails the operations are issued one by one, with the same results. */
 w4_status w4_decode_seq_run_host(w4_seq* seq, const void* x_host, void* x_dev,
                                  size_t x_bytes, void* y_dev, void* y_host,
                                  size_t y_bytes, void* stream);

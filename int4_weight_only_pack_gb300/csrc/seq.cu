@@ -39,6 +39,14 @@ struct w4_seq {
     w4::StepLaunch step;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
+    // w4_decode_seq_run_host: copy in, the step, copy out as one graph, kept for the
+    // buffers it was built for
+    cudaGraphExec_t io_exec = nullptr;
+    const void* io_xh = nullptr;
+    void* io_xd = nullptr;
+    void* io_yd = nullptr;
+    void* io_yh = nullptr;
+    size_t io_xb = 0, io_yb = 0;
 };
 
 using namespace w4;
@@ -54,6 +62,7 @@ static w4_status enqueue_all(w4_seq* s, cudaStream_t stream) {
 
 extern "C" void w4_decode_seq_destroy(w4_seq* seq) {
     if (!seq) return;
+    if (seq->io_exec) cudaGraphExecDestroy(seq->io_exec);
     if (seq->exec) cudaGraphExecDestroy(seq->exec);
     if (seq->graph) cudaGraphDestroy(seq->graph);
     delete seq;
@@ -152,10 +161,53 @@ extern "C" w4_status w4_decode_seq_run_host(w4_seq* seq, const void* x_host, voi
         return W4_ERR_ARG;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (x_bytes) W4_CUDA_TRY(cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, s));
-    w4_status st = w4_decode_seq_replay(seq, stream);
-    if (st != W4_OK) return st;
-    if (y_bytes) W4_CUDA_TRY(cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, s));
+    const bool same = seq->io_exec && seq->io_xh == x_host && seq->io_xd == x_dev && seq->io_xb == x_bytes &&
+                      seq->io_yd == y_dev && seq->io_yh == y_host && seq->io_yb == y_bytes;
+    if (!same) {
+        // one graph of the copy in, the step and the copy out, launched as one unit on every
+        // later call with the same buffers (961 -> 957 us per call for the 28-layer step: the
+        // rest of the ~55 us beyond the step is the two copies themselves); where it cannot be
+        // captured the operations are issued one by one
+        if (seq->io_exec) cudaGraphExecDestroy(seq->io_exec);
+        seq->io_exec = nullptr;
+        cudaStream_t cap = nullptr;
+        cudaGraph_t g = nullptr;
+        cudaError_t e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+        if (e == cudaSuccess) {
+            if (x_bytes) e = cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, cap);
+            w4_status st = e == cudaSuccess ? enqueue_all(seq, cap) : W4_ERR_CUDA;
+            if (e == cudaSuccess && st == W4_OK && y_bytes)
+                e = cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, cap);
+            const cudaError_t e2 = cudaStreamEndCapture(cap, &g);
+            if (e == cudaSuccess && st == W4_OK && e2 == cudaSuccess && g)
+                e = cudaGraphInstantiateWithFlags(&seq->io_exec, g, 0);
+            else
+                e = cudaErrorUnknown;
+        }
+        if (g) cudaGraphDestroy(g);
+        if (cap) cudaStreamDestroy(cap);
+        if (e != cudaSuccess) {
+            seq->io_exec = nullptr;
+            (void)cudaGetLastError();
+            clear_error();
+        } else {
+            seq->io_xh = x_host;
+            seq->io_xd = x_dev;
+            seq->io_xb = x_bytes;
+            seq->io_yd = y_dev;
+            seq->io_yh = y_host;
+            seq->io_yb = y_bytes;
+        }
+    }
+    if (seq->io_exec) {
+        W4_CUDA_TRY(cudaGraphLaunch(seq->io_exec, s));
+    } else {
+        if (x_bytes) W4_CUDA_TRY(cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, s));
+        w4_status st = w4_decode_seq_replay(seq, stream);
+        if (st != W4_OK) return st;
+        if (y_bytes) W4_CUDA_TRY(cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, s));
+    }
     W4_CUDA_TRY(cudaStreamSynchronize(s));
     return W4_OK;
 }

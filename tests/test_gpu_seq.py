@@ -115,11 +115,25 @@ def test_run_host_copies_in_replays_and_copies_out(mode):
     y_host = torch.zeros(sum(ysz), dtype=torch.int16).pin_memory()
     stream = torch.cuda.current_stream()
     seq.run_host(x_host, x_arena, x_arena.numel() * 2, y_arena, y_host, y_arena.numel() * 2, stream)
-    yh = y_host.numpy().view(np.uint16)
-    yo = 0
-    for (x, q, s), (N, _), ny in zip(probs, shapes, ysz):
-        assert_close(yh[yo:yo + ny].reshape(M, N), oracle.linear(x, q, s))
-        yo += ny
+
+    def check(yh, probs):
+        yo = 0
+        for (x, q, s), (N, _), ny in zip(probs, shapes, ysz):
+            assert_close(yh[yo:yo + ny].reshape(M, N), oracle.linear(x, q, s))
+            yo += ny
+
+    check(y_host.numpy().view(np.uint16), probs)
+    # the same buffers again with new x in the pinned buffer: the graph kept from the first
+    # call copies the new values in
+    probs2 = [(rand_problem(rng, M, N, K)[0], q, s) for (N, K), (_, q, s) in zip(shapes, probs)]
+    x_host.copy_(torch.from_numpy(np.concatenate([p[0].ravel() for p in probs2]).view(np.int16)))
+    seq.run_host(x_host, x_arena, x_arena.numel() * 2, y_arena, y_host, y_arena.numel() * 2, stream)
+    first = y_host.numpy().view(np.uint16).copy()
+    check(first, probs2)
+    # another host output buffer: the graph is built again for it, same bits
+    y_host2 = torch.full((sum(ysz),), -1, dtype=torch.int16).pin_memory()
+    seq.run_host(x_host, x_arena, x_arena.numel() * 2, y_arena, y_host2, y_arena.numel() * 2, stream)
+    assert np.array_equal(y_host2.numpy().view(np.uint16), first)
     seq.close()
 
 
